@@ -1,0 +1,141 @@
+/*
+ * tattn.h -- C ABI of libtattn.so: fused scaled-dot-product attention on one
+ * GB300 (sm_103a) GPU, hand-written tcgen05/TMA kernels.
+ *
+ * Sources of the operations (web pages, by title and section):
+ *   [FA-JVP]  "Triton fused attention tutorial, updated with JVP support"
+ *             (gist _06_fused_attention_blockptr_jvp.py): _attn_fwd,
+ *             _attn_fwd_inner (online softmax, JVP extras), _attn_bwd_preprocess,
+ *             _attn_bwd_dkdv, _attn_bwd_dq, JVPAttn.forward / JVPAttn.backward,
+ *             and the comment thread's non-causal backward fix.
+ *   [PW]      "FlagAttention src/flag_attn/piecewise.py": _fwd_kernel,
+ *             _bwd_preprocess, _bwd_kv_kernel, _bwd_q_kernel, attention().
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are device pointers to contiguous [B, H, S, D] arrays (row-major,
+ *    D fastest).  Queries, dO, O and tangents of queries have S = M rows; keys,
+ *    values and their tangents have S = N rows.  All of q/k/v (and tangents,
+ *    dO) share one element type `dt`; O, dQ, dK, dV and tO are written in `dt`.
+ *  - `lse` is float32 [B, H, M]: the natural-log log-sum-exp of the scaled
+ *    scores of each query row, L_i = ln sum_j exp(sm_scale * q_i . k_j) over
+ *    the visible keys; rows that see no key get O = 0 and L = -inf.
+ *  - causal != 0 keeps key j for query i iff j <= i + (N - M) (bottom-right
+ *    alignment, [PW] _fwd_kernel; for M == N this is j <= i as in [FA-JVP]).
+ *  - sm_scale <= 0 (or not finite) selects 1/sqrt(D), like the pages' None.
+ *  - D must be 64 or 128; dt must be TA_F16 or TA_BF16.
+ *  - Every pointer must be 16-byte aligned (TMA).  B, H >= 1 and M, N >= 0;
+ *    B*H*M == 0 is a no-op returning TA_OK.
+ *  - The caller owns every buffer.  Nothing is allocated on the call path;
+ *    backward scratch lives in the caller's workspace `ws`.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Argument errors are reported synchronously before any
+ *    launch; a bounded-wait timeout inside a kernel is recorded in a device
+ *    error word that ta_sync_status() reads.
+ */
+#ifndef TATTN_H_
+#define TATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TA_OK = 0,
+  TA_ERR_INVALID_ARG = 1, /* null pointer, negative size, B*H overflow, ... */
+  TA_ERR_UNSUPPORTED = 2, /* D or dtype outside the supported set */
+  TA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
+  TA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+  TA_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (ta_sync_status) */
+} ta_status;
+
+typedef enum { TA_F16 = 0, TA_BF16 = 1, TA_F32 = 2 } ta_dtype;
+
+/* Forward: O = softmax(sm_scale * Q K^T) V with per-row LSE.
+ * [FA-JVP] _attn_fwd (+ _attn_fwd_inner stages), [PW] _fwd_kernel.
+ * In: q [B,H,M,D], k,v [B,H,N,D].  Out: o [B,H,M,D] (dt), lse [B,H,M] fp32. */
+ta_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int M,
+                   int N, int D, ta_dtype dt, int causal, float sm_scale, void* stream);
+
+/* Bytes of workspace attn_bwd needs: delta [B,H,M] fp32 (16-byte padded). */
+size_t attn_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt);
+
+/* Backward of attn_fwd for the loss <dO, O>.
+ * [FA-JVP] _attn_bwd_preprocess (delta = rowsum(dO o O)), _attn_bwd_dkdv,
+ * _attn_bwd_dq and JVPAttn.backward, with the thread's non-causal fix;
+ * [PW] _bwd_preprocess / _bwd_kv_kernel / _bwd_q_kernel.
+ * In: q,k,v, o and lse from attn_fwd, dO [B,H,M,D].  Out: dq [B,H,M,D],
+ * dk, dv [B,H,N,D] (dt).  ws: >= attn_bwd_workspace_bytes(...) bytes of
+ * device memory, 16-byte aligned, contents need not be initialised.
+ * Returns TA_ERR_INVALID_ARG if ws is null or too small. */
+ta_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H,
+                   int M, int N, int D, ta_dtype dt, int causal, float sm_scale, void* stream);
+
+/* Forward with fused forward-mode JVP: also returns
+ * tO = d/de attention(q + e tq, k + e tk, v + e tv) at e = 0.
+ * [FA-JVP] _attn_fwd_inner ENABLE_JVP branch and the _attn_fwd JVP epilogue:
+ * with T = sm_scale (tq K^T + Q tk^T) (zero where masked), mu_i = sum_j P_ij T_ij,
+ * tO = (P o T) V - mu o O + P tV.
+ * In: q,tq [B,H,M,D], k,v,tk,tv [B,H,N,D].  Out: o, to [B,H,M,D] (dt), lse. */
+ta_status attn_fwd_jvp(const void* q, const void* k, const void* v, const void* tq, const void* tk,
+                       const void* tv, void* o, float* lse, void* to, int B, int H, int M, int N, int D,
+                       ta_dtype dt, int causal, float sm_scale, void* stream);
+
+/* Piecewise attention forward ([PW] attention(), _fwd_kernel): the score of
+ * (i, j) is sm_scale * q2_i . k2_j when the signed distance i + N - M - j >= w,
+ * else sm_scale * q1_i . k1_j (the page's code rule piecewise_mask).
+ * In: q1,q2 [B,H,M,D], k1,k2,v [B,H,N,D].  Out: o (dt), lse (fp32). */
+ta_status piecewise_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                        void* o, float* lse, int B, int H, int M, int N, int D, ta_dtype dt, int causal,
+                        float sm_scale, int w, void* stream);
+
+/* Bytes of workspace piecewise_bwd needs (same layout as attn_bwd's). */
+size_t piecewise_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt);
+
+/* Piecewise backward ([PW] _bwd_preprocess, _bwd_kv_kernel, _bwd_q_kernel):
+ * dS = P o (dP - delta) is routed to (dq1, dk1) where distance < w and to
+ * (dq2, dk2) where distance >= w; dv = P^T dO.
+ * Out: dq1, dq2 [B,H,M,D], dk1, dk2, dv [B,H,N,D] (dt).
+ * Supports D = 64 only (the key-stationary pass keeps dV, dK1 and dK2 of a
+ * 128-key tile in tensor memory); D = 128 returns TA_ERR_UNSUPPORTED. */
+ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                        const void* o, const float* lse, const void* dO, void* dq1, void* dk1, void* dq2,
+                        void* dk2, void* dv, void* ws, size_t ws_bytes, int B, int H, int M, int N, int D,
+                        ta_dtype dt, int causal, float sm_scale, int w, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device error word that
+ * the kernels set when a bounded wait runs out.  TA_OK, TA_ERR_TIMEOUT or
+ * TA_ERR_CUDA (an asynchronous CUDA error). */
+ta_status ta_sync_status(void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* ta_status_str(ta_status s);
+
+/* Self-test of the bounded-wait machinery: launches one block that waits on
+ * an mbarrier nothing ever arrives on, with a limit of `timeout_ms`.  The
+ * kernel gives up, records a timeout and exits; ta_sync_status() then returns
+ * TA_ERR_TIMEOUT and the context stays usable.  No counterpart on the pages. */
+ta_status ta_selftest_wait_timeout(int timeout_ms, void* stream);
+
+/* Per-kernel timing with CUDA events recorded on the launch stream around
+ * every kernel the library launches (no counterpart on the pages).
+ * ta_profile_enable(1) clears the counters and starts recording;
+ * ta_profile_read() synchronises and fills, for up to `cap` kernels, the
+ * name, launch count and total milliseconds; it returns the number of
+ * kernels seen.  ta_profile_enable(0) stops recording. */
+ta_status ta_profile_enable(int on);
+int ta_profile_read(const char** names, int* launches, double* total_ms, int cap);
+
+/* Per-launch wait limit in milliseconds used by every kernel (default 2000,
+ * or the TA_WAIT_TIMEOUT_MS environment variable at load time). */
+void ta_set_wait_timeout_ms(int ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TATTN_H_ */

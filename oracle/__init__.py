@@ -85,7 +85,13 @@ def _softmax(S: np.ndarray, keep: np.ndarray):
 
 
 def _f64(*xs):
-    return [np.asarray(x, dtype=np.float64) for x in xs]
+    """float64 copies of numpy arrays or (any-dtype, any-device) torch tensors."""
+    out = []
+    for x in xs:
+        if hasattr(x, "detach"):
+            x = x.detach().cpu().double().numpy()
+        out.append(np.asarray(x, dtype=np.float64))
+    return out
 
 
 # ----------------------------------------------------------------- standard
@@ -214,3 +220,29 @@ def piecewise_fwd_bhsd(q1, k1, q2, k2, v, causal, sm_scale=None, w=0, heads=None
 
 def piecewise_bwd_bhsd(q1, k1, q2, k2, v, do, causal, sm_scale=None, w=0, heads=None):
     return _run_bhsd(piecewise_bwd, (q1, k1, q2, k2, v, do), (causal, sm_scale, w), heads, 5)
+
+
+# ------------------------------------------------------- sampled query rows
+def attention_rows(q, k, v, do, rows, causal: bool, sm_scale=None):
+    """One head, only the listed query rows: (O[rows], L[rows], dQ[rows]).
+
+    The same definitions as above restricted to rows i in `rows` (the mask
+    uses the absolute index i); query rows are independent, so these are
+    exactly the corresponding rows of attention_fwd / attention_bwd.  `do`
+    may be None (then dQ is not computed)."""
+    q, k, v = _f64(q, k, v)
+    rows = np.asarray(rows, dtype=np.int64)
+    M, N = q.shape[0], k.shape[0]
+    s = default_scale(q.shape[1], sm_scale)
+    if causal:
+        keep = np.arange(N)[None, :] <= rows[:, None] + (N - M)
+    else:
+        keep = np.ones((len(rows), N), dtype=bool)
+    P, L = _softmax(s * (q[rows] @ k.T), keep)
+    O = P @ v
+    if do is None:
+        return O, L, None
+    dor = _f64(do)[0][rows]
+    delta = (dor * O).sum(axis=1)
+    dS = P * (dor @ v.T - delta[:, None])
+    return O, L, s * (dS @ k)

@@ -340,3 +340,24 @@ def test_bhsd_wrappers_fill_selected_heads_only():
     Oh, Lh = oracle.attention_fwd(q[1, 2].numpy(), k[1, 2].numpy(), v[1, 2].numpy(), True, None)
     np.testing.assert_array_equal(O[1, 2], Oh)
     assert np.all(O[0] == 0)
+
+
+@pytest.mark.parametrize("M,N,causal", [(9, 9, True), (7, 11, True), (11, 6, True), (8, 8, False)])
+def test_sampled_rows_match_brute_force_and_finite_differences(M, N, causal):
+    """Row-sampled O, L, dQ: rows of the textbook loops and of the FD gradient."""
+    D = 4
+    q, k, v, do = rand(M, D), rand(N, D), rand(N, D), rand(M, D)
+    s = 0.55
+    rows = [0, M // 2, M - 1]
+    O, L, dQ = oracle.attention_rows(q, k, v, do, rows, causal, s)
+    Ob, Lb = brute_fwd(q, k, v, causal, s)
+    np.testing.assert_allclose(O, Ob[rows], atol=1e-13)
+    fin = np.isfinite(Lb[rows])
+    np.testing.assert_allclose(L[fin], Lb[rows][fin], atol=1e-13)
+
+    def f():
+        Of, _ = brute_fwd(q, k, v, causal, s)
+        return float((Of * do).sum())
+
+    g = _fd_grad(f, q)
+    np.testing.assert_allclose(dQ, g[rows], atol=2e-8, rtol=1e-6)

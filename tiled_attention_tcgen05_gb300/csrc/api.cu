@@ -1,0 +1,450 @@
+// C ABI of libtattn.so: argument validation, TMA tensor-map encoding, kernel
+// dispatch, the device error word behind the bounded waits, and per-kernel
+// CUDA-event timing.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/tattn.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace ta {
+
+// ------------------------------------------------------------ error word
+static __device__ uint32_t g_err_word;
+
+static uint32_t* error_word_ptr() {
+  static uint32_t* cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<uint32_t*>(p);
+  }
+  return cache[dev];
+}
+
+static uint64_t g_timeout_ns = [] {
+  const char* e = std::getenv("TA_WAIT_TIMEOUT_MS");
+  long v = e ? std::strtol(e, nullptr, 10) : 0;
+  if (v <= 0) v = 2000;
+  return static_cast<uint64_t>(v) * 1000000ull;
+}();
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [BH, S, D] 16-bit tensor viewed as a 3-D map with 64 x 128 x 1 boxes and
+// 128-byte swizzle; rows past S read as zeros.
+static bool make_map(CUtensorMap* map, const void* ptr, long long BH, long long S, int D, bool bf16) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------- profiling
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<ProfRec> g_prof_recs;
+static std::vector<cudaEvent_t> g_prof_pool;
+static size_t g_prof_pool_next = 0;
+static const char* g_prof_pending = nullptr;
+static cudaEvent_t g_prof_pending_ev = nullptr;
+
+static cudaEvent_t prof_event() {
+  if (g_prof_pool_next == g_prof_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_prof_pool.push_back(e);
+  }
+  return g_prof_pool[g_prof_pool_next++];
+}
+
+void prof_begin(const char* name, cudaStream_t s) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_pending = name;
+  g_prof_pending_ev = prof_event();
+  if (g_prof_pending_ev) cudaEventRecord(g_prof_pending_ev, s);
+}
+
+void prof_end(cudaStream_t s) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_pending || !g_prof_pending_ev) return;
+  cudaEvent_t e = prof_event();
+  if (!e) return;
+  cudaEventRecord(e, s);
+  g_prof_recs.push_back({g_prof_pending, g_prof_pending_ev, e});
+  g_prof_pending = nullptr;
+}
+
+// --------------------------------------------------------------- checks
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Problem {
+  long long BH;
+  int M, N, D;
+  bool bf16;
+  float sm_scale;
+};
+
+static ta_status check_common(int B, int H, int M, int N, int D, ta_dtype dt, float sm_scale, Problem* pr) {
+  if (B < 0 || H < 0 || M < 0 || N < 0) return TA_ERR_INVALID_ARG;
+  if (dt != TA_F16 && dt != TA_BF16) return TA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return TA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffll) return TA_ERR_INVALID_ARG;
+  if ((M + kBM - 1) / kBM > 65535 || (N + kBN - 1) / kBN > 65535) return TA_ERR_UNSUPPORTED;
+  pr->BH = BH;
+  pr->M = M;
+  pr->N = N;
+  pr->D = D;
+  pr->bf16 = (dt == TA_BF16);
+  pr->sm_scale = (std::isfinite(sm_scale) && sm_scale > 0.f) ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return TA_OK;
+}
+
+static ta_status check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p) return TA_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return TA_ERR_ALIGNMENT;
+  return TA_OK;
+}
+
+static ta_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TA_OK : TA_ERR_CUDA; }
+
+static FwdArgs fwd_args(const Problem& p, int causal, int w, void* o, float* lse, void* to) {
+  FwdArgs a;
+  a.o = o;
+  a.lse = lse;
+  a.to = to;
+  a.BH = static_cast<int>(p.BH);
+  a.M = p.M;
+  a.N = p.N;
+  a.P_SEQ = p.N - p.M;
+  a.num_q_tiles = (p.M + kBM - 1) / kBM;
+  a.causal = causal ? 1 : 0;
+  a.w = w;
+  a.sm_scale = p.sm_scale;
+  a.scale_log2 = p.sm_scale * kLog2e;
+  a.err = error_word_ptr();
+  a.timeout_ns = g_timeout_ns;
+  return a;
+}
+
+static BwdArgs bwd_args(const Problem& p, int causal, int w, const float* lse, const float* delta) {
+  BwdArgs a{};
+  a.lse = lse;
+  a.delta = delta;
+  a.BH = static_cast<int>(p.BH);
+  a.M = p.M;
+  a.N = p.N;
+  a.P_SEQ = p.N - p.M;
+  a.causal = causal ? 1 : 0;
+  a.w = w;
+  a.sm_scale = p.sm_scale;
+  a.scale_log2 = p.sm_scale * kLog2e;
+  a.err = error_word_ptr();
+  a.timeout_ns = g_timeout_ns;
+  return a;
+}
+
+static size_t delta_bytes(long long BH, int M) {
+  return (static_cast<size_t>(BH) * static_cast<size_t>(M) * sizeof(float) + 255) & ~size_t(255);
+}
+
+static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* k, const void* v,
+                         const void* q2, const void* k2, const void* v2, void* o, float* lse, void* to,
+                         int causal, int w, cudaStream_t s) {
+  if (p.BH == 0 || p.M == 0) return TA_OK;
+  if (p.N == 0) {
+    prof_begin("empty_rows", s);
+    cudaError_t e = launch_empty_rows(p.bf16, p.D, o, lse, to, p.BH * p.M, s);
+    prof_end(s);
+    return cuda_status(e);
+  }
+  FwdMaps maps;
+  bool ok = make_map(&maps.q, q, p.BH, p.M, p.D, p.bf16) && make_map(&maps.k, k, p.BH, p.N, p.D, p.bf16) &&
+            make_map(&maps.v, v, p.BH, p.N, p.D, p.bf16) &&
+            make_map(&maps.q2, q2 ? q2 : q, p.BH, p.M, p.D, p.bf16) &&
+            make_map(&maps.k2, k2 ? k2 : k, p.BH, p.N, p.D, p.bf16) &&
+            make_map(&maps.v2, v2 ? v2 : v, p.BH, p.N, p.D, p.bf16);
+  if (!ok) return TA_ERR_CUDA;
+  FwdArgs a = fwd_args(p, causal, w, o, lse, to);
+  static const char* names[3] = {"attn_fwd", "piecewise_fwd", "attn_fwd_jvp"};
+  prof_begin(names[mode], s);
+  cudaError_t e = launch_fwd(mode, p.bf16, p.D, maps, a, s);
+  prof_end(s);
+  return cuda_status(e);
+}
+
+static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* k, const void* v,
+                         const void* q2, const void* k2, const void* o, const float* lse, const void* dO,
+                         void* dq, void* dk, void* dq2, void* dk2, void* dv, void* ws, size_t ws_bytes,
+                         int causal, int w, cudaStream_t s) {
+  if (p.BH == 0) return TA_OK;
+  const bool pw = (mode == kPiecewise);
+  const size_t kv_bytes = static_cast<size_t>(p.BH) * p.N * p.D * 2;
+  if (p.M == 0) {  // no query: every key/value gradient is zero
+    cudaError_t e = launch_zero(dk, kv_bytes, s);
+    if (e == cudaSuccess) e = launch_zero(dv, kv_bytes, s);
+    if (e == cudaSuccess && pw) e = launch_zero(dk2, kv_bytes, s);
+    return cuda_status(e);
+  }
+  if (ws_bytes < delta_bytes(p.BH, p.M)) return TA_ERR_INVALID_ARG;
+  float* delta = static_cast<float*>(ws);
+  prof_begin("bwd_delta", s);
+  cudaError_t e = launch_delta(p.bf16, p.D, o, dO, delta, p.BH * p.M, s);
+  prof_end(s);
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  const size_t q_bytes = static_cast<size_t>(p.BH) * p.M * p.D * 2;
+  if (p.N == 0) {
+    e = launch_zero(dq, q_bytes, s);
+    if (e == cudaSuccess && pw) e = launch_zero(dq2, q_bytes, s);
+    return cuda_status(e);
+  }
+  BwdMaps maps;
+  bool ok = make_map(&maps.q, q, p.BH, p.M, p.D, p.bf16) && make_map(&maps.k, k, p.BH, p.N, p.D, p.bf16) &&
+            make_map(&maps.v, v, p.BH, p.N, p.D, p.bf16) && make_map(&maps.dO, dO, p.BH, p.M, p.D, p.bf16) &&
+            make_map(&maps.q2, q2 ? q2 : q, p.BH, p.M, p.D, p.bf16) &&
+            make_map(&maps.k2, k2 ? k2 : k, p.BH, p.N, p.D, p.bf16);
+  if (!ok) return TA_ERR_CUDA;
+  BwdArgs a = bwd_args(p, causal, w, lse, delta);
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dq2 = dq2;
+  a.dk2 = dk2;
+  prof_begin(pw ? "piecewise_bwd_dkdv" : "attn_bwd_dkdv", s);
+  e = launch_bwd_dkdv(mode, p.bf16, p.D, maps, a, s);
+  prof_end(s);
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  prof_begin(pw ? "piecewise_bwd_dq" : "attn_bwd_dq", s);
+  e = launch_bwd_dq(mode, p.bf16, p.D, maps, a, s);
+  prof_end(s);
+  return cuda_status(e);
+}
+
+}  // namespace ta
+
+using namespace ta;
+
+extern "C" {
+
+const char* ta_status_str(ta_status s) {
+  switch (s) {
+    case TA_OK: return "TA_OK";
+    case TA_ERR_INVALID_ARG: return "TA_ERR_INVALID_ARG";
+    case TA_ERR_UNSUPPORTED: return "TA_ERR_UNSUPPORTED";
+    case TA_ERR_ALIGNMENT: return "TA_ERR_ALIGNMENT";
+    case TA_ERR_CUDA: return "TA_ERR_CUDA";
+    case TA_ERR_TIMEOUT: return "TA_ERR_TIMEOUT";
+  }
+  return "TA_ERR_UNKNOWN";
+}
+
+void ta_set_wait_timeout_ms(int ms) { g_timeout_ns = static_cast<uint64_t>(ms > 0 ? ms : 2000) * 1000000ull; }
+
+ta_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int M, int N,
+                   int D, ta_dtype dt, int causal, float sm_scale, void* stream) {
+  Problem p;
+  ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
+  if (st != TA_OK) return st;
+  if (p.BH * M == 0) return TA_OK;
+  st = (N > 0) ? check_ptrs({q, k, v, o, lse}) : check_ptrs({o, lse});
+  if (st != TA_OK) return st;
+  return run_fwd(kStd, p, q, k, v, nullptr, nullptr, nullptr, o, lse, nullptr, causal, 0,
+                 static_cast<cudaStream_t>(stream));
+}
+
+ta_status attn_fwd_jvp(const void* q, const void* k, const void* v, const void* tq, const void* tk,
+                       const void* tv, void* o, float* lse, void* to, int B, int H, int M, int N, int D,
+                       ta_dtype dt, int causal, float sm_scale, void* stream) {
+  Problem p;
+  ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
+  if (st != TA_OK) return st;
+  if (p.BH * M == 0) return TA_OK;
+  st = (N > 0) ? check_ptrs({q, k, v, tq, tk, tv, o, lse, to}) : check_ptrs({o, lse, to});
+  if (st != TA_OK) return st;
+  return run_fwd(kJvp, p, q, k, v, tq, tk, tv, o, lse, to, causal, 0, static_cast<cudaStream_t>(stream));
+}
+
+ta_status piecewise_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, void* o,
+                        float* lse, int B, int H, int M, int N, int D, ta_dtype dt, int causal, float sm_scale,
+                        int w, void* stream) {
+  Problem p;
+  ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
+  if (st != TA_OK) return st;
+  if (p.BH * M == 0) return TA_OK;
+  st = (N > 0) ? check_ptrs({q1, k1, q2, k2, v, o, lse}) : check_ptrs({o, lse});
+  if (st != TA_OK) return st;
+  return run_fwd(kPiecewise, p, q1, k1, v, q2, k2, nullptr, o, lse, nullptr, causal, w,
+                 static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt) {
+  (void)N;
+  (void)D;
+  (void)dt;
+  if (B <= 0 || H <= 0 || M <= 0) return 0;
+  return delta_bytes(static_cast<long long>(B) * H, M);
+}
+
+size_t piecewise_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt) {
+  return attn_bwd_workspace_bytes(B, H, M, N, D, dt);
+}
+
+ta_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
+                   void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H, int M, int N, int D,
+                   ta_dtype dt, int causal, float sm_scale, void* stream) {
+  Problem p;
+  ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
+  if (st != TA_OK) return st;
+  if (p.BH == 0 || (M == 0 && N == 0)) return TA_OK;
+  if (M == 0) st = check_ptrs({dk, dv});
+  else if (N == 0) st = check_ptrs({o, dO, dq, ws});
+  else st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, ws});
+  if (st != TA_OK) return st;
+  return run_bwd(kStd, p, q, k, v, nullptr, nullptr, o, lse, dO, dq, dk, nullptr, nullptr, dv, ws, ws_bytes,
+                 causal, 0, static_cast<cudaStream_t>(stream));
+}
+
+ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                        const void* o, const float* lse, const void* dO, void* dq1, void* dk1, void* dq2,
+                        void* dk2, void* dv, void* ws, size_t ws_bytes, int B, int H, int M, int N, int D,
+                        ta_dtype dt, int causal, float sm_scale, int w, void* stream) {
+  Problem p;
+  ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
+  if (st != TA_OK) return st;
+  // TMEM holds S, dP, dV, dK1 and dK2 of a 128-key tile only for D <= 64.
+  if (D != 64) return TA_ERR_UNSUPPORTED;
+  if (p.BH == 0 || (M == 0 && N == 0)) return TA_OK;
+  if (M == 0) st = check_ptrs({dk1, dk2, dv});
+  else if (N == 0) st = check_ptrs({o, dO, dq1, dq2, ws});
+  else st = check_ptrs({q1, k1, q2, k2, v, o, lse, dO, dq1, dk1, dq2, dk2, dv, ws});
+  if (st != TA_OK) return st;
+  return run_bwd(kPiecewise, p, q1, k1, v, q2, k2, o, lse, dO, dq1, dk1, dq2, dk2, dv, ws, ws_bytes, causal, w,
+                 static_cast<cudaStream_t>(stream));
+}
+
+ta_status ta_sync_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  uint32_t* w = error_word_ptr();
+  if (!w) return TA_ERR_CUDA;
+  uint32_t h = 0;
+  if (cudaMemcpy(&h, w, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return TA_ERR_CUDA;
+  if (h) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return TA_ERR_CUDA;
+    return TA_ERR_TIMEOUT;
+  }
+  return TA_OK;
+}
+
+ta_status ta_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (on) {
+    g_prof_recs.clear();
+    g_prof_pool_next = 0;
+    g_prof_pending = nullptr;
+  }
+  g_prof_on = on != 0;
+  return TA_OK;
+}
+
+int ta_profile_read(const char** names, int* launches, double* total_ms, int cap) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  std::vector<std::string> keys;
+  std::vector<int> cnt;
+  std::vector<double> ms;
+  for (const ProfRec& r : g_prof_recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return -1;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return -1;
+    size_t i = 0;
+    while (i < keys.size() && keys[i] != r.name) ++i;
+    if (i == keys.size()) {
+      keys.push_back(r.name);
+      cnt.push_back(0);
+      ms.push_back(0.0);
+    }
+    cnt[i] += 1;
+    ms[i] += t;
+  }
+  for (size_t i = 0; i < keys.size() && static_cast<int>(i) < cap; ++i) {
+    // names point at the static strings passed to prof_begin
+    for (const ProfRec& r : g_prof_recs)
+      if (keys[i] == r.name) {
+        names[i] = r.name;
+        break;
+      }
+    launches[i] = cnt[i];
+    total_ms[i] = ms[i];
+  }
+  return static_cast<int>(keys.size());
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------ wait self-test
+namespace ta {
+__global__ void wait_selftest_kernel(uint32_t* err, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  WaitCtl ctl{err, timeout_ns, &abort_flag};
+  // Nothing ever arrives on `bar`: the bounded wait must give up.
+  mbar_wait(&bar, 0, ctl, kErrTimeoutOther);
+}
+}  // namespace ta
+
+extern "C" ta_status ta_selftest_wait_timeout(int timeout_ms, void* stream) {
+  if (timeout_ms <= 0 || timeout_ms > 10000) return TA_ERR_INVALID_ARG;
+  uint32_t* w = error_word_ptr();
+  if (!w) return TA_ERR_CUDA;
+  ta::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      w, static_cast<uint64_t>(timeout_ms) * 1000000ull);
+  return cudaGetLastError() == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}

@@ -1,0 +1,706 @@
+// Backward attention kernels for sm_103a (tcgen05 + TMA), standard and
+// piecewise.
+//
+// Two kernels, each one CTA per 128-row tile, same warp roles as the forward
+// (warps 0-3: one thread per TMEM lane; warp 4: producer; warp 5: MMA):
+//
+//  * attn_bwd_dkdv_kernel: key-stationary.  The CTA keeps a 128-key tile of K
+//    and V in shared memory and walks the query tiles that see it.  Per query
+//    tile: S^T = K Q^T and dP^T = V dO^T (tcgen05, into TMEM); thread j (key
+//    row j) recomputes P^T = exp2(S^T * c - L * log2 e) and
+//    dS^T = P^T o (dP^T - delta), writes both back into TMEM as 16-bit
+//    operands; then dV += P^T dO and dK += dS^T Q read them straight from
+//    TMEM.  dK is scaled by sm_scale at the end.
+//  * attn_bwd_dq_kernel: query-stationary.  Per key tile: S = Q K^T,
+//    dP = dO V^T, dS = P o (dP - delta), dQ += dS K; dQ * sm_scale at the end.
+//
+// Page sources: "Triton fused attention tutorial, updated with JVP support",
+// _attn_bwd / _attn_bwd_dkdv / _attn_bwd_dq (pT = exp2(qkT - m), dv += pT do,
+// dpT = v do^T, dsT = pT (dpT - Di), dk += dsT q, dq += ds k, dk *= sm_scale)
+// with the comment thread's fix (non-causal tiles run over the full range);
+// "FlagAttention piecewise.py", _bwd_kv_kernel / _bwd_q_kernel (p = exp2(s *
+// qk_scale - L * log2e), ds split by piecewise_mask into ds1 -> (dq1, dk1),
+// ds2 -> (dq2, dk2), both scaled by sm_scale).
+//
+// Departures from the pages, all result-preserving: P^T and dS^T stay in
+// TMEM as MMA operands; piecewise tiles that are entirely near or entirely
+// far run one score MMA and one gradient MMA instead of two.
+#include "common.cuh"
+#include "launch.h"
+
+namespace ta {
+
+enum : int { kNearB = 1, kFarB = 2 };
+
+__device__ __forceinline__ int pw_class_b(int q0, int k0, int P_SEQ, int w) {
+  const long long lo = (long long)q0 + P_SEQ - k0 - w;  // min over (i, j) of i + P_SEQ - j - w
+  // i in [q0, q0 + kBM), j in [k0, k0 + kBN): far iff i + P_SEQ - j - w >= 0
+  if (lo - (kBN - 1) >= 0) return kFarB;
+  if (lo + (kBM - 1) < 0) return kNearB;
+  return kNearB | kFarB;
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile_b(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh) {
+#pragma unroll
+  for (int kb = 0; kb < D / 64; ++kb) tma_load_3d(dst + kb * (kBM * 128), map, bar, kb * 64, row0, bh);
+}
+
+// d = A B^T over D: A, B are 128-row x D K-major swizzled tiles in smem.
+template <int D>
+__device__ __forceinline__ void mma_abT(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+    mma_ss(d_tmem, sdesc_sw128(a_smem + off, 16, 1024), sdesc_sw128(b_smem + off, 16, 1024), idesc,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// d (+)= X Y: X is 128 x 128 16-bit in TMEM (K = the 128 columns), Y is a
+// 128-row x D tile in smem read as an MN-major B operand (rows = K).
+template <int D>
+__device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
+                                       bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk) {
+    mma_ts(d_tmem, x_tmem + kk * 8, sdesc_sw128(y_smem + kk * 16 * 128, kBM * 128, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store_chunk32(T* dst, const uint32_t* v, float scale) {
+  constexpr bool BF = DT<T>::bf16;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack2<BF>(__uint_as_float(v[8 * q + 0]) * scale, __uint_as_float(v[8 * q + 1]) * scale);
+    u.y = pack2<BF>(__uint_as_float(v[8 * q + 2]) * scale, __uint_as_float(v[8 * q + 3]) * scale);
+    u.z = pack2<BF>(__uint_as_float(v[8 * q + 4]) * scale, __uint_as_float(v[8 * q + 5]) * scale);
+    u.w = pack2<BF>(__uint_as_float(v[8 * q + 6]) * scale, __uint_as_float(v[8 * q + 7]) * scale);
+    d4[q] = u;
+  }
+}
+
+// Reads a D-column fp32 accumulator row from TMEM and stores it (x scale) as
+// one row of T; `touched` false writes zeros.  Warp-collective.
+template <typename T, int D>
+__device__ __forceinline__ void epilogue_row(uint32_t taddr, T* dst, bool store, bool touched, float scale) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld_x32(taddr + 32 * c, v);
+    tmem_ld_wait(v);
+    if (store) store_chunk32<T>(dst + 32 * c, v, touched ? scale : 0.f);
+  }
+}
+
+#define TB_CHUNK(arr, c) (*reinterpret_cast<uint32_t(*)[32]>(&(arr)[32 * (c)]))
+
+// ======================================================================
+//                        dK, dV (key-stationary)
+// ======================================================================
+template <int MODE, int D>
+struct DkdvCfg {
+  static constexpr int BLK = kBM * 128;
+  static constexpr int TILE = (D / 64) * BLK;
+  static constexpr int NRES = (MODE == kStd) ? 2 : 3;  // K, V | K1, K2, V
+  static constexpr int NQT = (MODE == kStd) ? 2 : 3;   // Q, dO | Q1, Q2, dO
+  static constexpr int STAGE = NQT * TILE;
+  static constexpr int RESERVE = 2048 + 4 * 1024;      // alignment + static (barriers, L, delta)
+  static constexpr int ST_FIT = (kSmemMax - RESERVE - NRES * TILE) / STAGE;
+  static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
+  static constexpr int SMEM = NRES * TILE + STAGES * STAGE + 1024;
+  static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D, COL_DK2 = 256 + 2 * D;
+  static_assert(STAGES >= 1, "tile does not fit in shared memory");
+  static_assert(COL_DK2 + (MODE == kPiecewise ? D : 0) <= 512, "TMEM overflow");
+};
+
+template <typename T, int MODE, int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
+                         const BwdArgs args) {
+  using C = DkdvCfg<MODE, D>;
+  constexpr bool BF = DT<T>::bf16;
+  constexpr int STAGES = C::STAGES;
+  constexpr bool PW = (MODE == kPiecewise);
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_kv, bar_q[STAGES], bar_qempty[STAGES];
+  __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_consumed, bar_ds, bar_done;
+  __shared__ __align__(16) float sL[STAGES][kBM];      // L * log2(e) of the tile's queries
+  __shared__ __align__(16) float sDelta[STAGES][kBM];  // delta of the tile's queries
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int kt = blockIdx.y;
+  const int k0 = kt * kBN;
+  const int num_q_tiles = (args.M + kBM - 1) / kBM;
+  const int i0 = first_q_tile_for(k0, args.P_SEQ, args.causal);
+  const int nq = num_q_tiles > i0 ? num_q_tiles - i0 : 0;
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = base;                       // K | K1
+  uint8_t* sK2 = base + C::TILE;            // piecewise K2
+  uint8_t* sV = base + (C::NRES - 1) * C::TILE;
+  uint8_t* sStages = base + C::NRES * C::TILE;
+  auto sQ = [&](int st) { return sStages + st * C::STAGE; };                 // Q | Q1
+  auto sQ2 = [&](int st) { return sStages + st * C::STAGE + C::TILE; };      // Q2
+  auto sDO = [&](int st) { return sStages + st * C::STAGE + (C::NQT - 1) * C::TILE; };
+
+  WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_kv, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bar_q[s], 1);
+      mbar_init(&bar_qempty[s], 1);
+    }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_consumed, 4);
+    mbar_init(&bar_ds, 4);
+    mbar_init(&bar_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (nq > 0) {
+      if (lane == 0) {
+        mbar_expect_tx(&bar_kv, C::NRES * C::TILE);
+        load_tile_b<D>(sK, &tm_k, &bar_kv, k0, bh);
+        if constexpr (PW) load_tile_b<D>(sK2, &tm_k2, &bar_kv, k0, bh);
+        load_tile_b<D>(sV, &tm_v, &bar_kv, k0, bh);
+      }
+      int issued = 0;
+      for (int u = 0; u < nq; ++u) {
+        const int st = u % STAGES;
+        if (u >= STAGES) {
+          if (!warp_wait(&bar_qempty[st], ((u / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
+        }
+        const int q0 = (i0 + u) * kBM;
+#pragma unroll
+        for (int e = lane; e < kBM; e += 32) {
+          const int q = q0 + e;
+          const size_t g = static_cast<size_t>(bh) * args.M + q;
+          sL[st][e] = (q < args.M) ? args.lse[g] * kLog2e : INFINITY;
+          sDelta[st][e] = (q < args.M) ? args.delta[g] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mbar_expect_tx(&bar_q[st], C::NQT * C::TILE);
+          load_tile_b<D>(sQ(st), &tm_q, &bar_q[st], q0, bh);
+          if constexpr (PW) load_tile_b<D>(sQ2(st), &tm_q2, &bar_q[st], q0, bh);
+          load_tile_b<D>(sDO(st), &tm_do, &bar_q[st], q0, bh);
+        }
+        issued = u + 1;
+      }
+      if (lane == 0) {  // never leave a TMA write in flight behind an early exit
+        int zero = 0;
+        WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
+        mbar_wait(&bar_kv, 0, drain, kErrTimeoutTma);
+        for (int u = issued - STAGES > 0 ? issued - STAGES : 0; u < issued; ++u)
+          mbar_wait(&bar_q[u % STAGES], (u / STAGES) & 1, drain, kErrTimeoutTma);
+      }
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0 && nq > 0) {
+      constexpr uint32_t idesc_s = idesc_f16(kBN, kBM, BF, false, false);  // M = keys, N = queries
+      constexpr uint32_t idesc_g = idesc_f16(kBN, D, BF, false, true);     // M = keys, N = D
+      bool ok = mbar_wait(&bar_kv, 0, ctl, kErrTimeoutTma);
+      bool acc1 = false, acc2 = false;
+      int nstr = 0;
+      for (int u = 0; ok && u < nq; ++u) {
+        const int st = u % STAGES;
+        const int q0 = (i0 + u) * kBM;
+        if (!(ok = mbar_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+        tc_fence_after();
+        int cls = kNearB;
+        if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
+        if (cls == kNearB) {
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(st)), idesc_s);
+        } else if (cls == kFarB) {
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
+        } else {
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(st)), idesc_s);
+          mma_abT<D>(tmem + C::COL_B, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
+        }
+        mma_commit(&bar_s);
+        if (cls == (kNearB | kFarB)) {
+          if (!(ok = mbar_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
+          tc_fence_after();
+          ++nstr;
+        }
+        mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(st)), idesc_s);  // dP^T = V dO^T
+        mma_commit(&bar_dp);
+        if (!(ok = mbar_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        mma_tY<D>(tmem + C::COL_DV, tmem + C::COL_A, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
+        if constexpr (!PW) {
+          mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, u > 0);  // dK += dS^T Q
+        } else {
+          if (cls == kNearB) {
+            mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
+            acc1 = true;
+          } else if (cls == kFarB) {
+            mma_tY<D>(tmem + C::COL_DK2, tmem + C::COL_B, smem_u32(sQ2(st)), idesc_g, acc2);
+            acc2 = true;
+          } else {
+            mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
+            mma_tY<D>(tmem + C::COL_DK2, tmem + C::COL_A + 64, smem_u32(sQ2(st)), idesc_g, acc2);
+            acc1 = acc2 = true;
+          }
+        }
+        mma_commit(&bar_qempty[st]);
+      }
+      if (ok) mma_commit(&bar_done);
+    }
+  } else {
+    // ------------------------------------------- key-row softmax gradient
+    const int r = threadIdx.x;
+    const int j = k0 + r;  // this thread's key
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    bool ok = true;
+    bool touched1 = false, touched2 = false;
+    int nstr = 0;
+    for (int u = 0; u < nq; ++u) {
+      const int st = u % STAGES;
+      const int q0 = (i0 + u) * kBM;
+      if (!(ok = warp_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+      if (!(ok = warp_wait(&bar_s, u & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+      int cls = kNearB;
+      if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
+      touched1 |= (cls & kNearB) != 0;
+      touched2 |= (cls & kFarB) != 0;
+      uint32_t s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + C::COL_A + 32 * c, TB_CHUNK(s, c));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(TB_CHUNK(s, c));
+      // far iff column c >= fl (query q0 + c, key j: q0 + c + P_SEQ - j >= w)
+      const long long fl = (long long)j + args.w - args.P_SEQ - q0;
+      if (cls == (kNearB | kFarB)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t s2[32];
+          tmem_ld_x32(lane_addr + C::COL_B + 32 * c, s2);
+          tmem_ld_wait(s2);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e >= fl) s[32 * c + e] = s2[e];
+        }
+      }
+      // visible iff j <= q + P_SEQ, i.e. column c >= lo
+      const int lo = args.causal ? j - args.P_SEQ - q0 : -1;
+      float p[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float x = ex2(__uint_as_float(s[c]) * args.scale_log2 - sL[st][c]);
+        p[c] = (c >= lo) ? x : 0.f;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack2<BF>(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
+        tmem_st_x16(lane_addr + C::COL_A + 16 * c, pk);
+      }
+      if (cls == (kNearB | kFarB)) {
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_consumed);
+        ++nstr;
+      }
+      if (!(ok = warp_wait(&bar_dp, u & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32];
+        tmem_ld_x32(lane_addr + C::COL_B + 32 * c, dp);
+        tmem_ld_wait(dp);
+        uint32_t pk1[16], pk2[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = 32 * c + 2 * e;
+          const float ds0 = p[c0] * (__uint_as_float(dp[2 * e]) - sDelta[st][c0]);
+          const float ds1 = p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - sDelta[st][c0 + 1]);
+          if (cls == (kNearB | kFarB)) {
+            const bool f0 = c0 >= fl, f1 = c0 + 1 >= fl;
+            pk1[e] = pack2<BF>(f0 ? 0.f : ds0, f1 ? 0.f : ds1);
+            pk2[e] = pack2<BF>(f0 ? ds0 : 0.f, f1 ? ds1 : 0.f);
+          } else {
+            pk1[e] = pack2<BF>(ds0, ds1);
+          }
+        }
+        tmem_st_x16(lane_addr + C::COL_B + 16 * c, pk1);
+        if (cls == (kNearB | kFarB)) tmem_st_x16(lane_addr + C::COL_A + 64 + 16 * c, pk2);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ds);
+    }
+    (void)nstr;
+    // ------------------------------------------------------------ epilogue
+    if (nq > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
+    tc_fence_after();
+    const bool live = ok && nq > 0;
+    const bool st_row = j < args.N;
+    const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * D;
+    T* dv = reinterpret_cast<T*>(args.dv) + off;
+    T* dk = reinterpret_cast<T*>(args.dk) + off;
+    if (live) {
+      epilogue_row<T, D>(lane_addr + C::COL_DV, dv, st_row, true, 1.f);
+      if constexpr (!PW) {
+        epilogue_row<T, D>(lane_addr + C::COL_DK, dk, st_row, true, args.sm_scale);
+      } else {
+        T* dk2 = reinterpret_cast<T*>(args.dk2) + off;
+        epilogue_row<T, D>(lane_addr + C::COL_DK, dk, st_row, touched1, args.sm_scale);
+        epilogue_row<T, D>(lane_addr + C::COL_DK2, dk2, st_row, touched2, args.sm_scale);
+      }
+    } else if (st_row) {
+      uint32_t z[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) z[e] = 0;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        store_chunk32<T>(dv + 32 * c, z, 0.f);
+        store_chunk32<T>(dk + 32 * c, z, 0.f);
+        if constexpr (PW) store_chunk32<T>(reinterpret_cast<T*>(args.dk2) + off + 32 * c, z, 0.f);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// ======================================================================
+//                         dQ (query-stationary)
+// ======================================================================
+template <int MODE, int D>
+struct DqCfg {
+  static constexpr int BLK = kBM * 128;
+  static constexpr int TILE = (D / 64) * BLK;
+  static constexpr int NRES = (MODE == kStd) ? 2 : 3;  // Q, dO | Q1, Q2, dO
+  static constexpr int NKT = (MODE == kStd) ? 2 : 3;   // K, V | K1, K2, V
+  static constexpr int STAGE = NKT * TILE;
+  static constexpr int RESERVE = 2048;
+  static constexpr int ST_FIT = (kSmemMax - RESERVE - NRES * TILE) / STAGE;
+  static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
+  static constexpr int SMEM = NRES * TILE + STAGES * STAGE + 1024;
+  static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DQ = 256, COL_DQ2 = 256 + D;
+  static_assert(STAGES >= 1, "tile does not fit in shared memory");
+  static_assert(COL_DQ2 + (MODE == kPiecewise ? D : 0) <= 512, "TMEM overflow");
+};
+
+template <typename T, int MODE, int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
+                       const BwdArgs args) {
+  using C = DqCfg<MODE, D>;
+  constexpr bool BF = DT<T>::bf16;
+  constexpr int STAGES = C::STAGES;
+  constexpr bool PW = (MODE == kPiecewise);
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q, bar_kv[STAGES], bar_kvempty[STAGES];
+  __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_consumed, bar_ds, bar_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int num_q_tiles = (args.M + kBM - 1) / kBM;
+  const int qt = num_q_tiles - 1 - blockIdx.y;  // heaviest causal tiles first
+  const int q0 = qt * kBM;
+  const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;
+  uint8_t* sQ2 = base + C::TILE;
+  uint8_t* sDO = base + (C::NRES - 1) * C::TILE;
+  uint8_t* sStages = base + C::NRES * C::TILE;
+  auto sK = [&](int st) { return sStages + st * C::STAGE; };
+  auto sK2 = [&](int st) { return sStages + st * C::STAGE + C::TILE; };
+  auto sV = [&](int st) { return sStages + st * C::STAGE + (C::NKT - 1) * C::TILE; };
+
+  WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bar_kv[s], 1);
+      mbar_init(&bar_kvempty[s], 1);
+    }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_consumed, 4);
+    mbar_init(&bar_ds, 4);
+    mbar_init(&bar_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nkv > 0) {
+      mbar_expect_tx(&bar_q, C::NRES * C::TILE);
+      load_tile_b<D>(sQ, &tm_q, &bar_q, q0, bh);
+      if constexpr (PW) load_tile_b<D>(sQ2, &tm_q2, &bar_q, q0, bh);
+      load_tile_b<D>(sDO, &tm_do, &bar_q, q0, bh);
+      int issued = 0;
+      for (int t = 0; t < nkv; ++t) {
+        const int st = t % STAGES;
+        if (t >= STAGES && !mbar_wait(&bar_kvempty[st], ((t / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
+        const int k0 = t * kBN;
+        int cls = kNearB;
+        if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
+        const int nk = ((cls & kNearB) ? 1 : 0) + ((cls & kFarB) ? 1 : 0);
+        mbar_expect_tx(&bar_kv[st], (nk + 1) * C::TILE);
+        if (cls & kNearB) load_tile_b<D>(sK(st), &tm_k, &bar_kv[st], k0, bh);
+        if (cls & kFarB) load_tile_b<D>(sK2(st), &tm_k2, &bar_kv[st], k0, bh);
+        load_tile_b<D>(sV(st), &tm_v, &bar_kv[st], k0, bh);
+        issued = t + 1;
+      }
+      int zero = 0;
+      WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
+      mbar_wait(&bar_q, 0, drain, kErrTimeoutTma);
+      for (int t = issued - STAGES > 0 ? issued - STAGES : 0; t < issued; ++t)
+        mbar_wait(&bar_kv[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
+    }
+  } else if (warp == 5) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0 && nkv > 0) {
+      constexpr uint32_t idesc_s = idesc_f16(kBM, kBN, BF, false, false);
+      constexpr uint32_t idesc_g = idesc_f16(kBM, D, BF, false, true);
+      bool ok = mbar_wait(&bar_q, 0, ctl, kErrTimeoutTma);
+      bool acc1 = false, acc2 = false;
+      int nstr = 0;
+      for (int t = 0; ok && t < nkv; ++t) {
+        const int st = t % STAGES;
+        if (!(ok = mbar_wait(&bar_kv[st], (t / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+        tc_fence_after();
+        int cls = kNearB;
+        if constexpr (PW) cls = pw_class_b(q0, t * kBN, args.P_SEQ, args.w);
+        if (cls == kNearB) {
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sQ), smem_u32(sK(st)), idesc_s);
+        } else if (cls == kFarB) {
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sQ2), smem_u32(sK2(st)), idesc_s);
+        } else {
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sQ), smem_u32(sK(st)), idesc_s);
+          mma_abT<D>(tmem + C::COL_B, smem_u32(sQ2), smem_u32(sK2(st)), idesc_s);
+        }
+        mma_commit(&bar_s);
+        if (cls == (kNearB | kFarB)) {
+          if (!(ok = mbar_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
+          tc_fence_after();
+          ++nstr;
+        }
+        mma_abT<D>(tmem + C::COL_B, smem_u32(sDO), smem_u32(sV(st)), idesc_s);  // dP = dO V^T
+        mma_commit(&bar_dp);
+        if (!(ok = mbar_wait(&bar_ds, t & 1, ctl, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        if constexpr (!PW) {
+          mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, t > 0);  // dQ += dS K
+        } else {
+          if (cls == kNearB) {
+            mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, acc1);
+            acc1 = true;
+          } else if (cls == kFarB) {
+            mma_tY<D>(tmem + C::COL_DQ2, tmem + C::COL_B, smem_u32(sK2(st)), idesc_g, acc2);
+            acc2 = true;
+          } else {
+            mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, acc1);
+            mma_tY<D>(tmem + C::COL_DQ2, tmem + C::COL_A + 64, smem_u32(sK2(st)), idesc_g, acc2);
+            acc1 = acc2 = true;
+          }
+        }
+        mma_commit(&bar_kvempty[st]);
+      }
+      if (ok) mma_commit(&bar_done);
+    }
+  } else {
+    // --------------------------------------------- query-row softmax gradient
+    const int r = threadIdx.x;
+    const int row = q0 + r;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool in_m = row < args.M;
+    const size_t g = static_cast<size_t>(bh) * args.M + (in_m ? row : 0);
+    const float L2 = in_m ? args.lse[g] * kLog2e : INFINITY;
+    const float dlt = in_m ? args.delta[g] : 0.f;
+    bool ok = true;
+    bool touched1 = false, touched2 = false;
+    for (int t = 0; t < nkv; ++t) {
+      const int k0 = t * kBN;
+      if (!(ok = warp_wait(&bar_s, t & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+      int cls = kNearB;
+      if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
+      touched1 |= (cls & kNearB) != 0;
+      touched2 |= (cls & kFarB) != 0;
+      uint32_t s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + C::COL_A + 32 * c, TB_CHUNK(s, c));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(TB_CHUNK(s, c));
+      // far iff key k0 + c satisfies row + P_SEQ - (k0 + c) >= w, i.e. c <= pwl
+      const long long pwl = (long long)row + args.P_SEQ - k0 - args.w;
+      if (cls == (kNearB | kFarB)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t s2[32];
+          tmem_ld_x32(lane_addr + C::COL_B + 32 * c, s2);
+          tmem_ld_wait(s2);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (32 * c + e <= pwl) s[32 * c + e] = s2[e];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_consumed);
+      }
+      int lim = args.N - 1 - k0;  // keys past N are padding
+      if (args.causal) lim = min(lim, row + args.P_SEQ - k0);
+      float p[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float x = ex2(__uint_as_float(s[c]) * args.scale_log2 - L2);
+        p[c] = (c <= lim) ? x : 0.f;
+      }
+      if (!(ok = warp_wait(&bar_dp, t & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dp[32];
+        tmem_ld_x32(lane_addr + C::COL_B + 32 * c, dp);
+        tmem_ld_wait(dp);
+        uint32_t pk1[16], pk2[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = 32 * c + 2 * e;
+          const float ds0 = p[c0] * (__uint_as_float(dp[2 * e]) - dlt);
+          const float ds1 = p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - dlt);
+          if (cls == (kNearB | kFarB)) {
+            const bool f0 = c0 <= pwl, f1 = c0 + 1 <= pwl;
+            pk1[e] = pack2<BF>(f0 ? 0.f : ds0, f1 ? 0.f : ds1);
+            pk2[e] = pack2<BF>(f0 ? ds0 : 0.f, f1 ? ds1 : 0.f);
+          } else {
+            pk1[e] = pack2<BF>(ds0, ds1);
+          }
+        }
+        tmem_st_x16(lane_addr + C::COL_B + 16 * c, pk1);
+        if (cls == (kNearB | kFarB)) tmem_st_x16(lane_addr + C::COL_A + 64 + 16 * c, pk2);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ds);
+    }
+    if (nkv > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
+    tc_fence_after();
+    const bool live = ok && nkv > 0;
+    T* dq = reinterpret_cast<T*>(args.dq) + g * D;
+    if (live) {
+      if constexpr (!PW) {
+        epilogue_row<T, D>(lane_addr + C::COL_DQ, dq, in_m, true, args.sm_scale);
+      } else {
+        T* dq2 = reinterpret_cast<T*>(args.dq2) + g * D;
+        epilogue_row<T, D>(lane_addr + C::COL_DQ, dq, in_m, touched1, args.sm_scale);
+        epilogue_row<T, D>(lane_addr + C::COL_DQ2, dq2, in_m, touched2, args.sm_scale);
+      }
+    } else if (in_m) {
+      uint32_t z[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) z[e] = 0;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        store_chunk32<T>(dq + 32 * c, z, 0.f);
+        if constexpr (PW) store_chunk32<T>(reinterpret_cast<T*>(args.dq2) + g * D + 32 * c, z, 0.f);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- host side
+template <typename T, int MODE, int D>
+static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
+  using C = DkdvCfg<MODE, D>;
+  auto kern = attn_bwd_dkdv_kernel<T, MODE, D>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(a.BH, (a.N + kBN - 1) / kBN);
+  kern<<<grid, 192, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
+  return cudaGetLastError();
+}
+
+template <typename T, int MODE, int D>
+static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
+  using C = DqCfg<MODE, D>;
+  auto kern = attn_bwd_dq_kernel<T, MODE, D>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(a.BH, (a.M + kBM - 1) / kBM);
+  kern<<<grid, 192, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
+  if (mode == kStd && D == 64) return bf16 ? launch_dkdv_t<__nv_bfloat16, kStd, 64>(m, a, s) : launch_dkdv_t<__half, kStd, 64>(m, a, s);
+  if (mode == kStd && D == 128) return bf16 ? launch_dkdv_t<__nv_bfloat16, kStd, 128>(m, a, s) : launch_dkdv_t<__half, kStd, 128>(m, a, s);
+  if (mode == kPiecewise && D == 64) return bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dkdv_t<__half, kPiecewise, 64>(m, a, s);
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
+  if (mode == kStd && D == 64) return bf16 ? launch_dq_t<__nv_bfloat16, kStd, 64>(m, a, s) : launch_dq_t<__half, kStd, 64>(m, a, s);
+  if (mode == kStd && D == 128) return bf16 ? launch_dq_t<__nv_bfloat16, kStd, 128>(m, a, s) : launch_dq_t<__half, kStd, 128>(m, a, s);
+  if (mode == kPiecewise && D == 64) return bf16 ? launch_dq_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dq_t<__half, kPiecewise, 64>(m, a, s);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace ta

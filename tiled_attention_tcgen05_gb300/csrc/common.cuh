@@ -1,0 +1,85 @@
+// Shared definitions for the attention kernels: problem parameters, tile
+// constants and the mode tags.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace ta {
+
+constexpr int kBM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;  // keys per tile
+constexpr int kSmemMax = 232448;  // opt-in dynamic shared memory per block
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+// The running row maximum is only raised (and O rescaled) when a new score
+// exceeds it by more than this many powers of two; below that the stale
+// maximum is kept, which is exact because O and l share it.
+constexpr float kRescaleThreshold = 8.0f;
+
+enum Mode : int { kStd = 0, kPiecewise = 1, kJvp = 2 };
+
+struct FwdArgs {
+  void* o;
+  float* lse;
+  void* to;       // JVP tangent output (kJvp only)
+  int BH, M, N, P_SEQ;
+  int num_q_tiles;
+  int causal;
+  int w;          // piecewise threshold
+  float scale_log2;  // sm_scale * log2(e)
+  float sm_scale;
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+struct BwdArgs {
+  void* dq;   // dq  (dq1 in piecewise)
+  void* dq2;  // piecewise only
+  void* dk;   // dk  (dk1 in piecewise)
+  void* dk2;  // piecewise only
+  void* dv;
+  const float* lse;
+  const float* delta;
+  int BH, M, N, P_SEQ;
+  int causal;
+  int w;
+  float scale_log2;
+  float sm_scale;
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+// Number of key tiles that query tile [q0, q0 + kBM) visits.
+__host__ __device__ inline int kv_tiles_for(int q0, int M, int N, int P_SEQ, int causal) {
+  int n_all = (N + kBN - 1) / kBN;
+  if (!causal) return n_all;
+  int last = q0 + kBM - 1 + P_SEQ;  // largest visible key of the tile
+  if (last < 0) return 0;
+  if (last > N - 1) last = N - 1;
+  return last / kBN + 1;
+}
+
+// First query tile that key tile [k0, k0 + kBN) is visible from.
+__host__ __device__ inline int first_q_tile_for(int k0, int P_SEQ, int causal) {
+  if (!causal) return 0;
+  int first_row = k0 - P_SEQ;  // smallest i with k0 <= i + P_SEQ
+  if (first_row < 0) first_row = 0;
+  return first_row / kBM;
+}
+
+template <typename T>
+struct DT;
+template <>
+struct DT<__nv_bfloat16> {
+  static constexpr bool bf16 = true;
+};
+template <>
+struct DT<__half> {
+  static constexpr bool bf16 = false;
+};
+
+}  // namespace ta

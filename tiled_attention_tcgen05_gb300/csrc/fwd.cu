@@ -1,0 +1,505 @@
+// Forward attention kernels for sm_103a: TMA-fed K/V ring, tcgen05 MMAs with
+// TMEM accumulators, one softmax thread per query row.
+//
+// One CTA owns one 128-row query tile of one (batch, head) and walks the key
+// tiles the causal / ragged schedule allows.  Warp roles (192 threads):
+//   warps 0-3  softmax + correction + epilogue; thread r owns query row r,
+//              which is TMEM lane r (tcgen05.ld 32x32b shape), so row max and
+//              row sum need no shuffles;
+//   warp 4     TMA producer (Q once, then a STAGES-deep ring of K/V tiles);
+//   warp 5     TMEM allocator and MMA issuer (one thread).
+// Per key tile t:  S = Q K_t^T (tcgen05.mma, A and B from shared memory) ->
+// softmax writes P (16-bit, packed two per TMEM column) over S -> O += P V_t
+// with P read straight from TMEM.  Standard mode double-buffers S so the
+// next QK^T overlaps the current softmax.
+//
+// Page sources: "Triton fused attention tutorial, updated with JVP support",
+// _attn_fwd / _attn_fwd_inner (online exp2 softmax with running max and sum,
+// acc = acc * alpha + P V, epilogue M = m + log2 l, O = acc / l; JVP branch:
+// t_qk = t_q k^T + q t_k^T, p_tqk = p * t_qk * sm_scale, mu, g_acc, p_tv_acc
+// and t_O = g_acc / l - (mu / l) O + p_tv_acc / l); "FlagAttention
+// piecewise.py", _fwd_kernel (piecewise_mask choosing q2 k2^T or q1 k1^T,
+// causal mask P_SEQ + i >= j, empty rows O = 0, L = -inf, natural-log L).
+//
+// Departures from the pages' design, all result-preserving: P lives in TMEM
+// instead of registers/shared memory; the running maximum is raised lazily
+// (only when it grows by more than 2^8), so O is rescaled rarely; the
+// tangent accumulators g_acc and p_tv_acc are one TMEM accumulator U; and
+// piecewise tiles whose keys are all near (or all far) run one QK^T MMA
+// instead of two.
+#include <cstdio>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace ta {
+
+template <int MODE, int D>
+struct FwdCfg {
+  static constexpr int KB = D / 64;       // 64-column (128-byte) swizzle blocks per row
+  static constexpr int BLK = kBM * 128;   // bytes of one 128-row x 64-column block
+  static constexpr int TILE = KB * BLK;   // bytes of one 128 x D tile
+  static constexpr int NQ = (MODE == kStd) ? 1 : 2;   // resident query-like tiles
+  static constexpr int NKT = (MODE == kStd) ? 1 : 2;  // key-like tiles per stage
+  static constexpr int NVT = (MODE == kJvp) ? 2 : 1;  // value-like tiles per stage
+  static constexpr int STAGE = (NKT + NVT) * TILE;
+  static constexpr int RESERVE = 2048;    // alignment slack + static shared memory
+  static constexpr int ST_FIT = (kSmemMax - RESERVE - NQ * TILE) / STAGE;
+  static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
+  static constexpr int NBUF = (MODE == kStd) ? 2 : 1;
+  static constexpr int SMEM = NQ * TILE + STAGES * STAGE + 1024;
+  static constexpr uint32_t COL_S0 = 0;    // S (buffer 0) | piecewise S(q1,k1) | jvp S
+  static constexpr uint32_t COL_S1 = 128;  // S (buffer 1) | piecewise S(q2,k2) | jvp T
+  static constexpr uint32_t COL_O = 256;
+  static constexpr uint32_t COL_U = 256 + D;  // jvp tangent accumulator
+  static_assert(STAGES >= 1, "tile does not fit in shared memory");
+  static_assert(COL_U + (MODE == kJvp ? D : 0) <= 512, "TMEM overflow");
+};
+
+enum : int { kNear = 1, kFar = 2 };
+
+// Which score products a piecewise tile needs: far iff i + P_SEQ - j >= w.
+__device__ __forceinline__ int pw_class(int q0, int k0, int P_SEQ, int w) {
+  const long long lo = (long long)q0 + P_SEQ - k0 - w;  // smallest i - j + P_SEQ - w
+  const long long hi = lo + (kBM - 1);                  // largest
+  if (lo >= kBN - 1) return kFar;   // every column c <= i + P_SEQ - k0 - w
+  if (hi < 0) return kNear;
+  return kNear | kFar;
+}
+
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh) {
+#pragma unroll
+  for (int kb = 0; kb < D / 64; ++kb) tma_load_3d(dst + kb * (kBM * 128), map, bar, kb * 64, row0, bh);
+}
+
+// d = A B^T over the head dimension: A, B are 128 x D K-major swizzled tiles.
+template <int D>
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc,
+                                       bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
+    mma_ss(d_tmem, sdesc_sw128(a_smem + off, 16, 1024), sdesc_sw128(b_smem + off, 16, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// d (+)= P V: P is 128 x 128 (16-bit, TMEM), V is 128 keys x D stored with D
+// contiguous (MN-major B operand; 64-column blocks kBM*128 bytes apart).
+template <int D>
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t idesc,
+                                       bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 16 * 128, kBM * 128, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void store_row_chunk(T* dst, const float* v32, float scale) {
+  constexpr bool BF = DT<T>::bf16;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack2<BF>(v32[8 * q + 0] * scale, v32[8 * q + 1] * scale);
+    u.y = pack2<BF>(v32[8 * q + 2] * scale, v32[8 * q + 3] * scale);
+    u.z = pack2<BF>(v32[8 * q + 4] * scale, v32[8 * q + 5] * scale);
+    u.w = pack2<BF>(v32[8 * q + 6] * scale, v32[8 * q + 7] * scale);
+    d4[q] = u;
+  }
+}
+
+#define TA_CHUNK(arr, c) (*reinterpret_cast<uint32_t(*)[32]>(&(arr)[32 * (c)]))
+
+template <typename T, int MODE, int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q2,
+                    const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2,
+                    const FwdArgs args) {
+  using C = FwdCfg<MODE, D>;
+  constexpr bool BF = DT<T>::bf16;
+  constexpr int STAGES = C::STAGES;
+  constexpr int NBUF = C::NBUF;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q;
+  __shared__ __align__(8) uint64_t bar_k[STAGES], bar_v[STAGES], bar_empty[STAGES];
+  __shared__ __align__(8) uint64_t bar_s[NBUF], bar_p[NBUF];
+  __shared__ __align__(8) uint64_t bar_o, bar_ofinal;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int qt = args.num_q_tiles - 1 - blockIdx.y;  // heaviest causal tiles first
+  const int q0 = qt * kBM;
+  const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;                                  // Q | Q1 | Q  (+ Q2 | TQ)
+  uint8_t* sStages = base + C::NQ * C::TILE;
+  auto sKt = [&](int st, int i) { return sStages + st * C::STAGE + i * C::TILE; };
+  auto sVt = [&](int st, int i) { return sStages + st * C::STAGE + (C::NKT + i) * C::TILE; };
+
+  WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bar_k[s], 1);
+      mbar_init(&bar_v[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&bar_s[b], 1);
+      mbar_init(&bar_p[b], 4);
+    }
+    mbar_init(&bar_o, 1);
+    mbar_init(&bar_ofinal, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 4) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0 && nkv > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int qrow = q0;
+      mbar_expect_tx(&bar_q, C::NQ * C::TILE);
+      load_tile<D>(sQ, &tm_q, &bar_q, qrow, bh);
+      if constexpr (C::NQ == 2) load_tile<D>(sQ + C::TILE, &tm_q2, &bar_q, qrow, bh);
+      uint32_t last_phase[STAGES];
+      int used = 0;
+      for (int t = 0; t < nkv; ++t) {
+        const int st = t % STAGES;
+        if (t >= STAGES) {
+          if (!mbar_wait(&bar_empty[st], ((t / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
+        }
+        const int k0 = t * kBN;
+        if constexpr (MODE == kStd) {
+          mbar_expect_tx(&bar_k[st], C::TILE);
+          load_tile<D>(sKt(st, 0), &tm_k, &bar_k[st], k0, bh);
+          mbar_expect_tx(&bar_v[st], C::TILE);
+          load_tile<D>(sVt(st, 0), &tm_v, &bar_v[st], k0, bh);
+        } else if constexpr (MODE == kPiecewise) {
+          const int cls = pw_class(q0, k0, args.P_SEQ, args.w);
+          const int nk = ((cls & kNear) ? 1 : 0) + ((cls & kFar) ? 1 : 0);
+          mbar_expect_tx(&bar_k[st], nk * C::TILE);
+          if (cls & kNear) load_tile<D>(sKt(st, 0), &tm_k, &bar_k[st], k0, bh);
+          if (cls & kFar) load_tile<D>(sKt(st, 1), &tm_k2, &bar_k[st], k0, bh);
+          mbar_expect_tx(&bar_v[st], C::TILE);
+          load_tile<D>(sVt(st, 0), &tm_v, &bar_v[st], k0, bh);
+        } else {
+          mbar_expect_tx(&bar_k[st], 2 * C::TILE);
+          load_tile<D>(sKt(st, 0), &tm_k, &bar_k[st], k0, bh);
+          load_tile<D>(sKt(st, 1), &tm_k2, &bar_k[st], k0, bh);
+          mbar_expect_tx(&bar_v[st], 2 * C::TILE);
+          load_tile<D>(sVt(st, 0), &tm_v, &bar_v[st], k0, bh);
+          load_tile<D>(sVt(st, 1), &tm_v2, &bar_v[st], k0, bh);
+        }
+        last_phase[st] = (t / STAGES) & 1;
+        used = t + 1 < STAGES ? t + 1 : STAGES;
+      }
+      // Never leave a TMA write in flight behind an early exit.
+      WaitCtl drain{args.err, args.timeout_ns, &abort_flag};
+      int zero = 0;
+      drain.abort = reinterpret_cast<volatile int*>(&zero);
+      mbar_wait(&bar_q, 0, drain, kErrTimeoutTma);
+      for (int s = 0; s < used; ++s) {
+        mbar_wait(&bar_k[s], last_phase[s], drain, kErrTimeoutTma);
+        mbar_wait(&bar_v[s], last_phase[s], drain, kErrTimeoutTma);
+      }
+    }
+  } else if (warp == 5) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0 && nkv > 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(kBM, kBN, BF, false, false);
+      constexpr uint32_t idesc_pv = idesc_f16(kBM, D, BF, false, true);
+      const uint32_t aQ = smem_u32(sQ);
+      const uint32_t aQ2 = aQ + C::TILE;
+      auto issue_pv = [&](int u, uint64_t* done_bar) -> bool {
+        const int b = u % NBUF;
+        const int st = u % STAGES;
+        if (!mbar_wait(&bar_p[b], (u / NBUF) & 1, ctl, kErrTimeoutSoftmax)) return false;
+        if (!mbar_wait(&bar_v[st], (u / STAGES) & 1, ctl, kErrTimeoutTma)) return false;
+        tc_fence_after();
+        const uint32_t p_col = (NBUF == 2) ? (b ? C::COL_S1 : C::COL_S0) : C::COL_S0;
+        mma_pv<D>(tmem + C::COL_O, tmem + p_col, smem_u32(sVt(st, 0)), idesc_pv, u > 0);
+        if constexpr (MODE == kJvp) {
+          mma_pv<D>(tmem + C::COL_U, tmem + C::COL_S1, smem_u32(sVt(st, 0)), idesc_pv, u > 0);
+          mma_pv<D>(tmem + C::COL_U, tmem + C::COL_S0, smem_u32(sVt(st, 1)), idesc_pv, true);
+        }
+        mma_commit(&bar_empty[st]);
+        mma_commit(done_bar);
+        return true;
+      };
+      bool ok = mbar_wait(&bar_q, 0, ctl, kErrTimeoutTma);
+      for (int t = 0; ok && t < nkv; ++t) {
+        const int st = t % STAGES;
+        if (NBUF == 1 && t > 0) {
+          ok = issue_pv(t - 1, &bar_o);
+          if (!ok) break;
+        }
+        if (!mbar_wait(&bar_k[st], (t / STAGES) & 1, ctl, kErrTimeoutTma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int b = t % NBUF;
+        const uint32_t aK = smem_u32(sKt(st, 0));
+        if constexpr (MODE == kStd) {
+          mma_qk<D>(tmem + (b ? C::COL_S1 : C::COL_S0), aQ, aK, idesc_qk, false);
+        } else if constexpr (MODE == kPiecewise) {
+          const int cls = pw_class(q0, t * kBN, args.P_SEQ, args.w);
+          if (cls & kNear) mma_qk<D>(tmem + C::COL_S0, aQ, aK, idesc_qk, false);
+          if (cls & kFar) mma_qk<D>(tmem + C::COL_S1, aQ2, smem_u32(sKt(st, 1)), idesc_qk, false);
+        } else {
+          mma_qk<D>(tmem + C::COL_S0, aQ, aK, idesc_qk, false);
+          // T = tq K^T + q tk^T (the sm_scale factor is applied by the softmax)
+          mma_qk<D>(tmem + C::COL_S1, aQ2, aK, idesc_qk, false);
+          mma_qk<D>(tmem + C::COL_S1, aQ, smem_u32(sKt(st, 1)), idesc_qk, true);
+        }
+        mma_commit(&bar_s[b]);
+        if (NBUF == 2 && t > 0) {
+          ok = issue_pv(t - 1, &bar_o);
+        }
+      }
+      if (ok) issue_pv(nkv - 1, &bar_ofinal);
+    }
+  } else {
+    // ------------------------------------------- softmax / correction / epilogue
+    const int r = threadIdx.x;  // 0..127: query row within the tile, TMEM lane
+    const int row = q0 + r;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float m_ref = -INFINITY;  // running (lazily raised) row max, log2 domain
+    float l = 0.f;
+    float mu = 0.f;
+    bool ok = true;
+    for (int t = 0; t < nkv; ++t) {
+      const int b = t % NBUF;
+      if (!warp_wait(&bar_s[b], (t / NBUF) & 1, ctl, kErrTimeoutMma)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = t * kBN;
+      uint32_t s[128];
+      const uint32_t s_col = (NBUF == 2 && b) ? C::COL_S1 : C::COL_S0;
+      int cls = kNear;
+      if constexpr (MODE == kPiecewise) cls = pw_class(q0, k0, args.P_SEQ, args.w);
+      const uint32_t first_col = (MODE == kPiecewise && cls == kFar) ? C::COL_S1 : s_col;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + first_col + 32 * c, TA_CHUNK(s, c));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(TA_CHUNK(s, c));
+      float x[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(s[j]) * args.scale_log2;
+      if constexpr (MODE == kPiecewise) {
+        if (cls == (kNear | kFar)) {
+          // far iff c <= row + P_SEQ - k0 - w: take the (q2, k2) score there
+          const long long pwl = (long long)row + args.P_SEQ - k0 - args.w;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t s2[32];
+            tmem_ld_x32(lane_addr + C::COL_S1 + 32 * c, s2);
+            tmem_ld_wait(s2);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (32 * c + j <= pwl) x[32 * c + j] = __uint_as_float(s2[j]) * args.scale_log2;
+          }
+        }
+      }
+      const bool need_mask =
+          (args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) || (k0 + kBN > args.N);
+      if (need_mask) {
+        int lim = args.N - 1 - k0;
+        if (args.causal) lim = min(lim, row + args.P_SEQ - k0);
+#pragma unroll
+        for (int j = 0; j < 128; ++j)
+          if (j > lim) x[j] = -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int j = 1; j < 128; ++j) mx = fmaxf(mx, x[j]);
+      const float m_new = fmaxf(m_ref, mx);
+      bool resc = false;
+      float alpha = 1.f;
+      if (t == 0) {
+        m_ref = m_new;
+      } else if (m_new > m_ref + kRescaleThreshold) {
+        resc = true;
+        alpha = ex2(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float rs = 0.f;
+#pragma unroll
+      for (int j = 0; j < 128; ++j) {
+        x[j] = ex2(x[j] - m_use);
+        rs += x[j];
+      }
+      l = l * alpha + rs;
+      // P (16-bit, two per column) over the first 64 columns of the S buffer
+      const uint32_t p_col = (MODE == kStd) ? s_col : C::COL_S0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pk[j] = pack2<BF>(x[32 * c + 2 * j], x[32 * c + 2 * j + 1]);
+        tmem_st_x16(lane_addr + p_col + 16 * c, pk);
+      }
+      if constexpr (MODE == kJvp) {
+        // P o T (T = sm_scale * (tq k^T + q tk^T)) over the first 64 columns of T
+        float mpart = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t tr[32];
+          tmem_ld_x32(lane_addr + C::COL_S1 + 32 * c, tr);
+          tmem_ld_wait(tr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a0 = x[32 * c + 2 * j] * __uint_as_float(tr[2 * j]) * args.sm_scale;
+            const float a1 = x[32 * c + 2 * j + 1] * __uint_as_float(tr[2 * j + 1]) * args.sm_scale;
+            mpart += a0 + a1;
+            pk[j] = pack2<BF>(a0, a1);
+          }
+          tmem_st_x16(lane_addr + C::COL_S1 + 16 * c, pk);
+        }
+        mu = mu * alpha + mpart;
+      }
+      // Correction: rescale the O (and U) rows once the previous P V landed.
+      if (t > 0 && __any_sync(0xffffffffu, resc)) {
+        if (!warp_wait(&bar_o, (t - 1) & 1, ctl, kErrTimeoutMma)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        constexpr int NACC = (MODE == kJvp) ? 2 : 1;
+#pragma unroll
+        for (int a = 0; a < NACC; ++a) {
+          const uint32_t col0 = a ? C::COL_U : C::COL_O;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld_x32(lane_addr + col0 + 32 * c, ov);
+            tmem_ld_wait(ov);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+            tmem_st_x32(lane_addr + col0 + 32 * c, ov);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[b]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (nkv > 0) ok = warp_wait(&bar_ofinal, 0, ctl, kErrTimeoutMma) && __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const bool live = ok && nkv > 0;
+    const float inv_l = (live && l > 0.f) ? 1.f / l : 0.f;
+    if (row < args.M) {
+      T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * D;
+      T* trow = nullptr;
+      if constexpr (MODE == kJvp) trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * D;
+      args.lse[static_cast<size_t>(bh) * args.M + row] =
+          (live && l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+      (void)trow;
+      if (!live) {
+        float z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          store_row_chunk<T>(orow + 32 * c, z, 0.f);
+          if constexpr (MODE == kJvp) store_row_chunk<T>(trow + 32 * c, z, 0.f);
+        }
+      }
+    }
+    if (live) {
+      // tcgen05.ld is warp-collective: every lane loads, rows >= M skip the store.
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld_x32(lane_addr + C::COL_O + 32 * c, ov);
+        tmem_ld_wait(ov);
+        float of[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) of[j] = __uint_as_float(ov[j]) * inv_l;
+        if (row < args.M) {
+          T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * D;
+          store_row_chunk<T>(orow + 32 * c, of, 1.f);
+        }
+        if constexpr (MODE == kJvp) {
+          uint32_t uv[32];
+          tmem_ld_x32(lane_addr + C::COL_U + 32 * c, uv);
+          tmem_ld_wait(uv);
+          const float mu_l = mu * inv_l;
+          float tv[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tv[j] = __uint_as_float(uv[j]) * inv_l - mu_l * of[j];
+          if (row < args.M) {
+            T* trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * D;
+            store_row_chunk<T>(trow + 32 * c, tv, 1.f);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------- host side
+template <typename T, int MODE, int D>
+static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<MODE, D>;
+  auto kern = attn_fwd_kernel<T, MODE, D>;
+  static bool attr_set = false;  // per instantiation; the attribute is per device-function
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(a.BH, a.num_q_tiles);
+  kern<<<grid, 192, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, maps.v2, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s) {
+#define TA_FWD_CASE(MODE_, D_)                                                          \
+  if (mode == MODE_ && D == D_)                                                         \
+    return bf16 ? launch_fwd_t<__nv_bfloat16, MODE_, D_>(maps, a, s)                    \
+                : launch_fwd_t<__half, MODE_, D_>(maps, a, s);
+  TA_FWD_CASE(kStd, 64)
+  TA_FWD_CASE(kStd, 128)
+  TA_FWD_CASE(kPiecewise, 64)
+  TA_FWD_CASE(kPiecewise, 128)
+  TA_FWD_CASE(kJvp, 64)
+  TA_FWD_CASE(kJvp, 128)
+#undef TA_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ta

@@ -1,0 +1,39 @@
+// Host-side declarations shared by the kernel translation units and the
+// C-ABI layer.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace ta {
+
+struct FwdMaps {
+  CUtensorMap q, k, v;     // standard: q, k, v
+  CUtensorMap q2, k2, v2;  // piecewise: q2, k2 (v2 unused); jvp: tq, tk, tv
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dO;  // piecewise: q1, k1, v, dO
+  CUtensorMap q2, k2;       // piecewise only
+};
+
+cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s);
+
+// delta_i = sum_d O_id dO_id for BH*M rows.
+cudaError_t launch_delta(bool bf16, int D, const void* o, const void* dO, float* delta, long long rows,
+                         cudaStream_t s);
+cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& maps, const BwdArgs& a,
+                            cudaStream_t s);
+cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& maps, const BwdArgs& a, cudaStream_t s);
+
+// Fills O = 0, L = -inf (rows that see no key) for BH*M rows.
+cudaError_t launch_empty_rows(bool bf16, int D, void* o, float* lse, void* to, long long rows, cudaStream_t s);
+// Zero-fills n bytes (gradients of keys no query sees).
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
+
+// Profiling hooks (no-ops unless ta_profile_enable(1)).
+void prof_begin(const char* name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+
+}  // namespace ta
