@@ -1,0 +1,417 @@
+"""Benchmark: attention forward + backward, bf16, causal, B=1 H=32 M=N=8192 D=128.
+
+One step = one pass of the whole hot path over one batch: attn_fwd (O, L)
+then attn_bwd (delta, dK/dV, dQ) on inputs resident in HBM.  The metric is
+throughput in TFLOPS with the FLOP count 4*B*H*M*N*D for the forward, 2.5x
+that for the backward, halved for causal (the benchmark harness of "Triton
+fused attention tutorial, updated with JVP support", bench_flash_attention).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}]
+For N > 1 launch one process per GPU with torch.distributed.run; every rank
+runs the same workload on its own GPU (independent heads: weak scaling, no
+collective on the data path; one barrier and a max-reduction of the timing).
+--impl reference times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd+bwd TFLOPS/GPU (bf16, causal) and % of GB300 dense tensor peak"
+WORKLOAD = dict(B=1, H=32, M=8192, N=8192, D=128, dtype="bf16", causal=True)
+WORKLOAD_NAME = "attention fwd+bwd bf16 causal B1 H32 M=N=8192 D128 (synthetic N(0,1), seeded)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def flops_fwd(B, H, M, N, D, causal):
+    f = 4.0 * B * H * M * N * D
+    return f * 0.5 if causal else f
+
+
+def step_flops(w=WORKLOAD):
+    f = flops_fwd(w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"])
+    return f * (1.0 + 2.5)
+
+
+def kernel_algorithmic(name, w=WORKLOAD):
+    """(bound, per-launch algorithmic FLOPs or bytes) of each library kernel.
+
+    attn_fwd: the forward's two matmuls.  attn_bwd_dkdv: four of the
+    backward's five algorithmic matmuls (S^T recompute, dP^T, dV, dK).
+    attn_bwd_dq: the dQ matmul (its S and dP recomputes are extra work, not
+    counted).  bwd_delta: bytes of O and dO read plus delta written."""
+    f = flops_fwd(w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"])
+    rows = w["B"] * w["H"] * w["M"]
+    table = {
+        "attn_fwd": ("tensor", f),
+        "attn_bwd_dkdv": ("tensor", 2.0 * f),
+        "attn_bwd_dq": ("tensor", 0.5 * f),
+        "bwd_delta": ("hbm", rows * w["D"] * 2 * 2 + rows * 4),
+    }
+    return table.get(name)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(peaks, key):
+    for k in (key, key.replace("_sustained", "")):
+        v = peaks.get(k)
+        if isinstance(v, (int, float)):
+            return float(v)
+        if isinstance(v, dict):
+            for kk in ("value", "peak", "median"):
+                if isinstance(v.get(kk), (int, float)):
+                    return float(v[kk])
+    return FALLBACK_PEAKS.get(key)
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tiled_attention_tcgen05_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
+    when the summary was taken on different kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    ent = d.get("kernels", {}).get(kernel)
+    return ent.get("dram_bytes_per_launch") if ent else None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not getattr(self, "out", ""):
+            return None
+        sm, mx, reasons, pw = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "power_w_median": statistics.median(pw) if pw else None, "samples": len(sm)}
+
+
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise maximum of per-rank timings (no-op for one rank)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_tflops(flops_per_rank_step, world, ms):
+    """Whole-job throughput: every rank runs the full workload (weak scaling)."""
+    return flops_per_rank_step * world / (ms * 1e-3) / 1e12
+
+
+# --------------------------------------------------------------- CPU oracle
+def cpu_oracle_sample(heads: int, threads: int):
+    """Runs the oracle's forward + backward on `heads` whole heads of the
+    workload in a fresh process with `threads` BLAS threads.  Returns
+    (seconds, flops of the sample)."""
+    code = f"""
+import os, sys, time, json
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import synth_inputs as si, oracle
+w = {WORKLOAD!r}
+names = ("q", "k", "v", "do")
+x = si.attention_inputs(1, {heads}, w["M"], w["N"], w["D"], w["dtype"], 3, names=names)
+t0 = time.perf_counter()
+for h in range({heads}):
+    oracle.attention_fwd(x["q"][0, h], x["k"][0, h], x["v"][0, h], w["causal"])
+    oracle.attention_bwd(x["q"][0, h], x["k"][0, h], x["v"][0, h], x["do"][0, h], w["causal"])
+print(json.dumps({{"s": time.perf_counter() - t0}}))
+"""
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(threads)
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    secs = json.loads(r.stdout.strip().splitlines()[-1])["s"]
+    w = WORKLOAD
+    f = flops_fwd(1, heads, w["M"], w["N"], w["D"], w["causal"]) * 3.5
+    return secs, f
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    heads = 1
+    times = []
+    for _ in range(args.warmup):
+        cpu_oracle_sample(heads, threads)
+    for _ in range(args.steps):
+        s, f = cpu_oracle_sample(heads, threads)
+        times.append(s)
+    secs = statistics.mean(times)
+    tflops = f / secs / 1e12
+    sample = f"{heads} of 32 heads (b=0,h=0) of the workload per step, fwd+bwd in fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, **WORKLOAD, "sample_heads": heads},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOPS", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import synth_inputs as si
+    import tiled_attention_tcgen05_gb300 as ta
+
+    ta.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOAD
+    B, H, M, N, D, causal = w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"]
+    names = ("q", "k", "v", "do")
+    cpu = si.attention_inputs(B, H, M, N, D, w["dtype"], 3, names=names)
+    host = {n: t.pin_memory() for n, t in cpu.items()}
+    g = {n: t.to(dev) for n, t in host.items()}
+    o = torch.empty_like(g["q"])
+    lse = torch.empty(B, H, M, device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])
+    ws = torch.empty(max(16, ta.attn_bwd_workspace_bytes(B, H, M, N, D, torch.bfloat16)), device=dev,
+                     dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ta.attn_fwd(g["q"], g["k"], g["v"], causal, None, o=o, lse=lse, stream=stream)
+        ta.attn_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal, None, dq=dq, dk=dk, dv=dv, ws=ws,
+                    stream=stream)
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    if ta.sync_status(stream) != "TA_OK":
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- device-resident timed region (with per-kernel events)
+    barrier()
+    ta.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    prof = ta.profile_read()
+    ta.profile_enable(False)
+    barrier()
+    status = ta.sync_status(stream)
+    if status != "TA_OK":
+        raise RuntimeError(f"device error word: {status}")
+    ms = ev0.elapsed_time(ev1) / args.steps
+
+    # ---- end-to-end: pinned host inputs -> device -> results back to host
+    out_host = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+    def e2e_step():
+        for n in names:
+            g[n].copy_(host[n], non_blocking=True)
+        step()
+        for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            out_host[n].copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    f_step = step_flops()
+    value = job_tflops(f_step, world, ms)
+    e2e_value = job_tflops(f_step, world, e2e_ms)
+    peaks, src = load_peaks()
+    bf16_peak = peak_value(peaks, "bf16_tflops")
+    hbm_peak = peak_value(peaks, "hbm_gbs")
+
+    kernels = {}
+    for name, (n, tot) in prof.items():
+        kernels[name] = {"launches": n, "total_ms": tot, "avg_ms": tot / max(1, n)}
+    dom = max(kernels, key=lambda k: kernels[k]["total_ms"])
+    bound, algo = kernel_algorithmic(dom)
+    avg_s = kernels[dom]["avg_ms"] * 1e-3
+    if bound == "tensor":
+        achieved = algo / avg_s / 1e12
+        peak, unit = bf16_peak, "TFLOP/s"
+    else:
+        achieved = algo / avg_s / 1e9
+        peak, unit = hbm_peak, "GB/s"
+    for name, k in kernels.items():
+        ka = kernel_algorithmic(name)
+        if ka:
+            b, a = ka
+            rate = a / (k["avg_ms"] * 1e-3)
+            k["achieved"] = rate / 1e12 if b == "tensor" else rate / 1e9
+            k["unit"] = "TFLOP/s" if b == "tensor" else "GB/s"
+            k["frac_of_" + src] = k["achieved"] / (bf16_peak if b == "tensor" else hbm_peak)
+
+    cpu_heads = 6
+    cpu_secs, cpu_f = cpu_oracle_sample(cpu_heads, os.cpu_count() or 1)
+    launches = sum(k["launches"] for k in kernels.values())
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, **w, "l2": "inputs (q,k,v,dO 268 MB) larger than L2 (129 MB)",
+                   "flops_per_step": f_step},
+        "pct_of_peak": value / world / bf16_peak,
+        "peak_source": src,
+        "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "peak_source": src + (" (burst)" if bound == "tensor" else ""),
+                     "traffic": ncu_traffic(dom), "algorithmic_per_launch": algo},
+        "kernels": kernels,
+        "cpu_baseline": {"value": cpu_f / cpu_secs / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": "%d of 32 heads (b=0, h<%d), fwd+bwd, fp64 numpy, %.1f s"
+                                   % (cpu_heads, cpu_heads, cpu_secs)},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if "RANK" not in os.environ:
+        world = 1  # a single process drives one GPU; N > 1 needs one process per GPU
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,94 @@
+"""The C ABI without a GPU: libtattn.so builds, loads, exports every function
+include/tattn.h declares, and rejects bad arguments with the documented
+status codes before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tattn.h")
+
+OK, INVALID, UNSUPPORTED, ALIGNMENT = 0, 1, 2, 3
+F16, BF16, F32 = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tiled_attention_tcgen05_gb300 import build
+    path = build.build()
+    import tiled_attention_tcgen05_gb300 as ta
+    return ta.load(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "extern")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_bwd", "attn_bwd_workspace_bytes", "attn_fwd_jvp", "piecewise_fwd",
+              "piecewise_bwd", "ta_sync_status", "ta_status_str"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in tattn.h but not exported"
+
+
+def test_status_strings(lib):
+    assert lib.ta_status_str(0) == b"TA_OK"
+    assert lib.ta_status_str(5) == b"TA_ERR_TIMEOUT"
+
+
+def _fwd(lib, q=16, k=32, v=48, o=64, lse=80, B=1, H=1, M=128, N=128, D=64, dt=BF16):
+    vp = ctypes.c_void_p
+    return lib.attn_fwd(vp(q), vp(k), vp(v), vp(o), vp(lse), B, H, M, N, D, dt, 0, -1.0, vp(0))
+
+
+def test_validation_codes(lib):
+    assert _fwd(lib, D=96) == UNSUPPORTED
+    assert _fwd(lib, D=256) == UNSUPPORTED
+    assert _fwd(lib, dt=F32) == UNSUPPORTED
+    assert _fwd(lib, dt=7) == UNSUPPORTED
+    assert _fwd(lib, B=-1) == INVALID
+    assert _fwd(lib, M=-5) == INVALID
+    assert _fwd(lib, q=0) == INVALID
+    assert _fwd(lib, lse=0) == INVALID
+    assert _fwd(lib, k=0x1008) == ALIGNMENT
+    assert _fwd(lib, o=0x1004) == ALIGNMENT
+    assert _fwd(lib, B=0) == OK          # empty: no work, no launch
+    assert _fwd(lib, M=0) == OK
+    assert _fwd(lib, M=128 * 65536) == UNSUPPORTED  # more query tiles than the grid allows
+
+
+def test_backward_workspace_and_validation(lib):
+    vp = ctypes.c_void_p
+    assert lib.attn_bwd_workspace_bytes(1, 32, 8192, 8192, 128, BF16) == 32 * 8192 * 4
+    assert lib.attn_bwd_workspace_bytes(1, 1, 3, 3, 64, F16) == 256
+    assert lib.attn_bwd_workspace_bytes(0, 1, 3, 3, 64, F16) == 0
+    p = [vp(16 * (i + 1)) for i in range(10)]
+    st = lib.attn_bwd(*p[:9], vp(0), 1024, 1, 1, 128, 128, 64, BF16, 1, -1.0, vp(0))
+    assert st == INVALID  # null workspace
+    st = lib.attn_bwd(*p[:9], vp(0x2008), 1024, 1, 1, 128, 128, 64, BF16, 1, -1.0, vp(0))
+    assert st == ALIGNMENT
+    # piecewise backward keeps three D-wide accumulators in TMEM: D = 64 only
+    q = [vp(16 * (i + 1)) for i in range(14)]
+    st = lib.piecewise_bwd(*q, 1 << 20, 1, 1, 128, 128, 128, BF16, 1, -1.0, 64, vp(0))
+    assert st == UNSUPPORTED
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import tiled_attention_tcgen05_gb300 as ta
+    saved = ta._lib
+    try:
+        ta._lib = None
+        with pytest.raises(RuntimeError, match="not built"):
+            ta.load(str(tmp_path / "missing.so"))
+    finally:
+        ta._lib = saved

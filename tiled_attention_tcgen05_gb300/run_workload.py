@@ -1,0 +1,73 @@
+"""Runs the library's entry points on one of the synthetic workloads for a
+number of steps: the command line used for profiling (ncu) and timing runs.
+
+  python -m tiled_attention_tcgen05_gb300.run_workload --workload 3 --steps 2 --warmup 1
+
+Workloads (synth_inputs.WORKLOADS): 1 fwd+bwd fp16 B1 H2 S128 D64 non-causal;
+2 fwd+bwd bf16 causal B4 H16 S2048 D128; 3 fwd+bwd bf16 causal B1 H32 S8192
+D128; 4 fwd+JVP fp16 B2 H8 S1024 D64 (--causal 0/1); 5 piecewise fwd+bwd bf16
+causal B2 H16 S4096 D64 w=512.  Prints the mean milliseconds per step.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import torch  # noqa: E402
+
+import synth_inputs as si  # noqa: E402
+import tiled_attention_tcgen05_gb300 as ta  # noqa: E402
+
+
+def make_step(wid: int, causal_override=None):
+    w = si.WORKLOADS[wid]
+    B, H, M, N, D, dt = w["B"], w["H"], w["M"], w["N"], w["D"], w["dtype"]
+    causal = w["causal"] if causal_override is None else bool(causal_override)
+    if w["mode"] == "jvp":
+        names = ("q", "k", "v", "tq", "tk", "tv")
+    elif w["mode"] == "piecewise":
+        names = ("q1", "k1", "q2", "k2", "v", "do")
+    else:
+        names = ("q", "k", "v", "do")
+    x = {n: t.cuda() for n, t in si.attention_inputs(B, H, M, N, D, dt, wid, names=names).items()}
+    if w["mode"] == "jvp":
+        return lambda: ta.attn_fwd_jvp(*(x[n] for n in names), causal=bool(causal))
+    if w["mode"] == "piecewise":
+        def step():
+            o, lse = ta.piecewise_fwd(x["q1"], x["k1"], x["q2"], x["k2"], x["v"], w["w"], causal)
+            ta.piecewise_bwd(x["q1"], x["k1"], x["q2"], x["k2"], x["v"], o, lse, x["do"], w["w"], causal)
+        return step
+
+    def step():
+        o, lse = ta.attn_fwd(x["q"], x["k"], x["v"], causal)
+        ta.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal)
+    return step
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=2)
+    ap.add_argument("--warmup", type=int, default=1)
+    ap.add_argument("--causal", type=int, default=None)
+    a = ap.parse_args()
+    ta.load()
+    step = make_step(a.workload, a.causal)
+    for _ in range(a.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.steps):
+        step()
+    e1.record()
+    status = ta.sync_status()
+    print(f"workload {a.workload}: {e0.elapsed_time(e1) / max(1, a.steps):.3f} ms/step, status {status}")
+    return 0 if status == "TA_OK" else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())
