@@ -75,6 +75,25 @@ ta_status attn_bwd(const void* q, const void* k, const void* v, const void* o, c
                    const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H,
                    int M, int N, int D, ta_dtype dt, int causal, float sm_scale, void* stream);
 
+/* attn_bwd for callers that cannot allocate device memory or pass a
+ * workspace (for example a host framework that has reserved all device memory
+ * for its own pool, or a step loop that must not call cudaMalloc because it
+ * synchronises the device).  The pages have no counterpart: this is a
+ * packaging variant of attn_bwd, with the same arguments minus `ws`.
+ *  - Scratch (delta, one float per query row) lives in a fixed array inside
+ *    the library's device image: at most 2^21 rows, i.e. B*H*M <= 2097152
+ *    (8 MiB, held on every GPU that loads the library until the process
+ *    exits).  Larger problems return TA_ERR_UNSUPPORTED without launching.
+ *  - The call allocates nothing.  Its first call on a device looks up the
+ *    array's device address (cudaGetSymbolAddress) with that device current;
+ *    make that first call before any stream capture.
+ *  - Every call shares the one array and fully rewrites the rows it uses, so
+ *    nothing needs clearing between calls; calls that may run at the same
+ *    time on the GPU (other streams, other host threads) race on it. */
+ta_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                           const void* dO, void* dq, void* dk, void* dv, int B, int H, int M, int N, int D,
+                           ta_dtype dt, int causal, float sm_scale, void* stream);
+
 /* Forward with fused forward-mode JVP: also returns
  * tO = d/de attention(q + e tq, k + e tk, v + e tv) at e = 0.
  * [FA-JVP] _attn_fwd_inner ENABLE_JVP branch and the _attn_fwd JVP epilogue:
