@@ -54,8 +54,9 @@ def _fwd(lib, q=16, k=32, v=48, o=64, lse=80, B=1, H=1, M=128, N=128, D=64, dt=B
 def test_validation_codes(lib):
     assert _fwd(lib, D=96) == UNSUPPORTED
     assert _fwd(lib, D=256) == UNSUPPORTED
-    assert _fwd(lib, dt=F32) == UNSUPPORTED
+    assert _fwd(lib, dt=F32, D=96) == UNSUPPORTED
     assert _fwd(lib, dt=7) == UNSUPPORTED
+    assert _fwd(lib, dt=F32, k=0x1004) == ALIGNMENT
     assert _fwd(lib, B=-1) == INVALID
     assert _fwd(lib, M=-5) == INVALID
     assert _fwd(lib, q=0) == INVALID

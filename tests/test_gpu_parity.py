@@ -218,3 +218,50 @@ def test_bounded_wait_times_out_and_context_survives(gpu_lib):
     assert ta.selftest_wait_timeout(20) == "TA_ERR_TIMEOUT"
     assert ta.sync_status() == "TA_OK"  # the word was cleared; the context still works
     _fwd_check(1, 1, 128, 128, 64, "f16", False, workload=31)
+
+
+# ---------------------------------------------------------------- fp32 mode
+F32_TOL = 1e-4
+
+
+@pytest.mark.parametrize("B,H,M,N,D,causal", [(1, 2, 128, 128, 64, False), (1, 2, 200, 333, 128, True),
+                                              (1, 1, 333, 200, 64, True), (2, 1, 96, 96, 128, False)])
+def test_fp32_mode_fwd_bwd_jvp(gpu_lib, B, H, M, N, D, causal):
+    ta = gpu_lib
+    names = ("q", "k", "v", "do", "tq", "tk", "tv")
+    cpu = {}
+    for idx, n in enumerate(names):
+        import synth_inputs as si
+        rows = M if n in ("q", "do", "tq") else N
+        cpu[n] = si.randn((B, H, rows, D), "f32", si.seed_for(15, idx))
+    g = {n: t.cuda() for n, t in cpu.items()}
+    o, lse = ta.attn_fwd(g["q"], g["k"], g["v"], causal)
+    dq, dk, dv = ta.attn_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal)
+    o2, lse2, to = ta.attn_fwd_jvp(g["q"], g["k"], g["v"], g["tq"], g["tk"], g["tv"], causal=causal)
+    assert ta.sync_status() == "TA_OK"
+    O, L = oracle.attention_fwd_bhsd(cpu["q"], cpu["k"], cpu["v"], causal)
+    dQ, dK, dV = oracle.attention_bwd_bhsd(cpu["q"], cpu["k"], cpu["v"], cpu["do"], causal)
+    _, _, tO = oracle.attention_jvp_bhsd(cpu["q"], cpu["k"], cpu["v"], cpu["tq"], cpu["tk"], cpu["tv"], causal)
+    for name, got, ref in (("O", o, O), ("L", lse, L), ("dQ", dq, dQ), ("dK", dk, dK), ("dV", dv, dV),
+                           ("O(jvp)", o2, O), ("tO", to, tO)):
+        compare(name, got, ref, F32_TOL)
+
+
+@pytest.mark.parametrize("D,w", [(64, 100), (128, 40), (64, -20)])
+def test_fp32_mode_piecewise(gpu_lib, D, w):
+    import synth_inputs as si
+    ta = gpu_lib
+    B, H, M, N = 1, 2, 256, 256
+    names = ("q1", "k1", "q2", "k2", "v", "do")
+    cpu = {n: si.randn((B, H, M if n in ("q1", "q2", "do") else N, D), "f32", si.seed_for(16, i))
+           for i, n in enumerate(names)}
+    g = {n: t.cuda() for n, t in cpu.items()}
+    o, lse = ta.piecewise_fwd(g["q1"], g["k1"], g["q2"], g["k2"], g["v"], w, True)
+    grads = ta.piecewise_bwd(g["q1"], g["k1"], g["q2"], g["k2"], g["v"], o, lse, g["do"], w, True)
+    assert ta.sync_status() == "TA_OK"
+    O, L = oracle.piecewise_fwd_bhsd(*(cpu[n] for n in names[:5]), True, None, w)
+    ref = oracle.piecewise_bwd_bhsd(*(cpu[n] for n in names), True, None, w)
+    compare("O", o, O, F32_TOL)
+    compare("L", lse, L, F32_TOL)
+    for name, got, r in zip(("dq1", "dk1", "dq2", "dk2", "dv"), grads, ref):
+        compare(name, got, r, F32_TOL)

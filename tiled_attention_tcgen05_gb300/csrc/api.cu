@@ -120,12 +120,14 @@ struct Problem {
   long long BH;
   int M, N, D;
   bool bf16;
+  bool f32;   // fp32 mode: SIMT kernels
+  int esize;  // bytes per element
   float sm_scale;
 };
 
 static ta_status check_common(int B, int H, int M, int N, int D, ta_dtype dt, float sm_scale, Problem* pr) {
   if (B < 0 || H < 0 || M < 0 || N < 0) return TA_ERR_INVALID_ARG;
-  if (dt != TA_F16 && dt != TA_BF16) return TA_ERR_UNSUPPORTED;
+  if (dt != TA_F16 && dt != TA_BF16 && dt != TA_F32) return TA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return TA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffll) return TA_ERR_INVALID_ARG;
@@ -135,6 +137,8 @@ static ta_status check_common(int B, int H, int M, int N, int D, ta_dtype dt, fl
   pr->N = N;
   pr->D = D;
   pr->bf16 = (dt == TA_BF16);
+  pr->f32 = (dt == TA_F32);
+  pr->esize = pr->f32 ? 4 : 2;
   pr->sm_scale = (std::isfinite(sm_scale) && sm_scale > 0.f) ? sm_scale : 1.0f / std::sqrt(static_cast<float>(D));
   return TA_OK;
 }
@@ -195,7 +199,18 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
   if (p.BH == 0 || p.M == 0) return TA_OK;
   if (p.N == 0) {
     prof_begin("empty_rows", s);
-    cudaError_t e = launch_empty_rows(p.bf16, p.D, o, lse, to, p.BH * p.M, s);
+    cudaError_t e = launch_empty_rows(p.esize, p.D, o, lse, to, p.BH * p.M, s);
+    prof_end(s);
+    return cuda_status(e);
+  }
+  static const char* f32_names[3] = {"attn_fwd_f32", "piecewise_fwd_f32", "attn_fwd_jvp_f32"};
+  if (p.f32) {
+    F32Ptrs fp{static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+               static_cast<const float*>(q2), static_cast<const float*>(k2), static_cast<const float*>(v2),
+               nullptr};
+    FwdArgs a = fwd_args(p, causal, w, o, lse, to);
+    prof_begin(f32_names[mode], s);
+    cudaError_t e = launch_f32_fwd(mode, p.D, fp, a, s);
     prof_end(s);
     return cuda_status(e);
   }
@@ -220,7 +235,7 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
                          int causal, int w, cudaStream_t s) {
   if (p.BH == 0) return TA_OK;
   const bool pw = (mode == kPiecewise);
-  const size_t kv_bytes = static_cast<size_t>(p.BH) * p.N * p.D * 2;
+  const size_t kv_bytes = static_cast<size_t>(p.BH) * p.N * p.D * p.esize;
   if (p.M == 0) {  // no query: every key/value gradient is zero
     cudaError_t e = launch_zero(dk, kv_bytes, s);
     if (e == cudaSuccess) e = launch_zero(dv, kv_bytes, s);
@@ -230,13 +245,30 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
   if (ws_bytes < delta_bytes(p.BH, p.M)) return TA_ERR_INVALID_ARG;
   float* delta = static_cast<float*>(ws);
   prof_begin("bwd_delta", s);
-  cudaError_t e = launch_delta(p.bf16, p.D, o, dO, delta, p.BH * p.M, s);
+  cudaError_t e = p.f32 ? launch_f32_delta(p.D, static_cast<const float*>(o), static_cast<const float*>(dO),
+                                           delta, p.BH * p.M, s)
+                        : launch_delta(p.bf16, p.D, o, dO, delta, p.BH * p.M, s);
   prof_end(s);
   if (e != cudaSuccess) return TA_ERR_CUDA;
-  const size_t q_bytes = static_cast<size_t>(p.BH) * p.M * p.D * 2;
+  const size_t q_bytes = static_cast<size_t>(p.BH) * p.M * p.D * p.esize;
   if (p.N == 0) {
     e = launch_zero(dq, q_bytes, s);
     if (e == cudaSuccess && pw) e = launch_zero(dq2, q_bytes, s);
+    return cuda_status(e);
+  }
+  if (p.f32) {
+    F32Ptrs fp{static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+               static_cast<const float*>(q2), static_cast<const float*>(k2), nullptr,
+               static_cast<const float*>(dO)};
+    BwdArgs a = bwd_args(p, causal, w, lse, delta);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dq2 = dq2;
+    a.dk2 = dk2;
+    prof_begin(pw ? "piecewise_bwd_f32" : "attn_bwd_f32", s);
+    e = launch_f32_bwd(mode, p.D, fp, a, s);
+    prof_end(s);
     return cuda_status(e);
   }
   BwdMaps maps;
@@ -352,8 +384,9 @@ ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const vo
   Problem p;
   ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
   if (st != TA_OK) return st;
-  // TMEM holds S, dP, dV, dK1 and dK2 of a 128-key tile only for D <= 64.
-  if (D != 64) return TA_ERR_UNSUPPORTED;
+  // TMEM holds S, dP, dV, dK1 and dK2 of a 128-key tile only for D <= 64
+  // (the fp32 mode has no such limit).
+  if (D != 64 && dt != TA_F32) return TA_ERR_UNSUPPORTED;
   if (p.BH == 0 || (M == 0 && N == 0)) return TA_OK;
   if (M == 0) st = check_ptrs({dk1, dk2, dv});
   else if (N == 0) st = check_ptrs({o, dO, dq1, dq2, ws});

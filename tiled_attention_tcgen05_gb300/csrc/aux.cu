@@ -72,10 +72,9 @@ __global__ void empty_rows_kernel(uint4* o, float* lse, uint4* to, long long row
   for (long long i = blockIdx.x * 256ll + threadIdx.x; i < rows; i += 256ll * gridDim.x) lse[i] = -INFINITY;
 }
 
-cudaError_t launch_empty_rows(bool bf16, int D, void* o, float* lse, void* to, long long rows, cudaStream_t s) {
-  (void)bf16;
+cudaError_t launch_empty_rows(int esize, int D, void* o, float* lse, void* to, long long rows, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  const int vpr = D * 2 / 16;
+  const int vpr = D * esize / 16;
   long long blocks = (rows * vpr + 255) / 256;
   if (blocks > sm_count() * 8) blocks = sm_count() * 8;
   empty_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<uint4*>(o), lse, static_cast<uint4*>(to), rows, vpr);

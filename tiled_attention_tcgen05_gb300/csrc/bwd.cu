@@ -1,8 +1,11 @@
 // Backward attention kernels for sm_103a (tcgen05 + TMA), standard and
 // piecewise.
 //
-// Two kernels, each one CTA per 128-row tile, same warp roles as the forward
-// (warps 0-3: one thread per TMEM lane; warp 4: producer; warp 5: MMA):
+// Two kernels, each one CTA per 128-row tile, 320 threads:
+//   warps 0-7  element-wise softmax gradient; TMEM lane = row (warp % 4
+//              selects the 32-lane quarter), and warp / 4 selects which half
+//              of the tile's 128 columns the thread handles;
+//   warp 8     TMA producer;  warp 9  TMEM allocator and MMA issuer.
 //
 //  * attn_bwd_dkdv_kernel: key-stationary.  The CTA keeps a 128-key tile of K
 //    and V in shared memory and walks the query tiles that see it.  Per query
@@ -25,15 +28,25 @@
 // Departures from the pages, all result-preserving: P^T and dS^T stay in
 // TMEM as MMA operands; piecewise tiles that are entirely near or entirely
 // far run one score MMA and one gradient MMA instead of two.
+//
+// TMEM operand placement: a thread of column half h (h = warp / 4) owns the
+// score columns [64h, 64h + 64) of its 128-column buffer; it writes its
+// 16-bit results (64 values = 32 packed columns) at [64h, 64h + 32) and, for
+// the far half of a straddling piecewise tile, at [64h + 32, 64h + 64).  The
+// gradient MMAs read the packed operand's 8-column K-steps from both halves.
 #include "common.cuh"
 #include "launch.h"
 
 namespace ta {
 
 enum : int { kNearB = 1, kFarB = 2 };
+constexpr int kBwdThreads = 320;
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
+constexpr int kRowWarps = 8;  // arrivals on the per-tile softmax barriers
 
 __device__ __forceinline__ int pw_class_b(int q0, int k0, int P_SEQ, int w) {
-  const long long lo = (long long)q0 + P_SEQ - k0 - w;  // min over (i, j) of i + P_SEQ - j - w
+  const long long lo = (long long)q0 + P_SEQ - k0 - w;  // min over (i, j) of i + P_SEQ - j - w is lo - (kBN-1)
   // i in [q0, q0 + kBM), j in [k0, k0 + kBN): far iff i + P_SEQ - j - w >= 0
   if (lo - (kBN - 1) >= 0) return kFarB;
   if (lo + (kBM - 1) < 0) return kNearB;
@@ -57,14 +70,16 @@ __device__ __forceinline__ void mma_abT(uint32_t d_tmem, uint32_t a_smem, uint32
   }
 }
 
-// d (+)= X Y: X is 128 x 128 16-bit in TMEM (K = the 128 columns), Y is a
+// d (+)= X Y: X is 128 x 128 16-bit in TMEM whose K-steps 0-3 sit at columns
+// x + [0, 32) and K-steps 4-7 at x + [64, 96) (the two column halves); Y is a
 // 128-row x D tile in smem read as an MN-major B operand (rows = K).
 template <int D>
 __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
                                        bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk) {
-    mma_ts(d_tmem, x_tmem + kk * 8, sdesc_sw128(y_smem + kk * 16 * 128, kBM * 128, 1024), idesc,
+    const uint32_t xc = x_tmem + (kk & 3) * 8 + (kk >> 2) * 64;
+    mma_ts(d_tmem, xc, sdesc_sw128(y_smem + kk * 16 * 128, kBM * 128, 1024), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -84,17 +99,28 @@ __device__ __forceinline__ void store_chunk32(T* dst, const uint32_t* v, float s
   }
 }
 
-// Reads a D-column fp32 accumulator row from TMEM and stores it (x scale) as
-// one row of T; `touched` false writes zeros.  Warp-collective.
+// Reads columns [c0, c0 + D/2) of a D-column fp32 accumulator row from TMEM
+// and stores them (x scale) into the matching half of one row of T;
+// `touched` false writes zeros.  Warp-collective.
 template <typename T, int D>
-__device__ __forceinline__ void epilogue_row(uint32_t taddr, T* dst, bool store, bool touched, float scale) {
+__device__ __forceinline__ void epilogue_half(uint32_t taddr, T* row, int c0, bool store, bool touched,
+                                              float scale) {
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
+  for (int c = 0; c < D / 64; ++c) {
     uint32_t v[32];
-    tmem_ld_x32(taddr + 32 * c, v);
+    tmem_ld_x32(taddr + c0 + 32 * c, v);
     tmem_ld_wait(v);
-    if (store) store_chunk32<T>(dst + 32 * c, v, touched ? scale : 0.f);
+    if (store) store_chunk32<T>(row + c0 + 32 * c, v, touched ? scale : 0.f);
   }
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void zero_half(T* row, int c0) {
+  uint32_t z[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) z[e] = 0;
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) store_chunk32<T>(row + c0 + 32 * c, z, 0.f);
 }
 
 #define TB_CHUNK(arr, c) (*reinterpret_cast<uint32_t(*)[32]>(&(arr)[32 * (c)]))
@@ -119,7 +145,7 @@ struct DkdvCfg {
 };
 
 template <typename T, int MODE, int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
@@ -165,12 +191,12 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(&bar_s, 1);
     mbar_init(&bar_dp, 1);
-    mbar_init(&bar_consumed, 4);
-    mbar_init(&bar_ds, 4);
+    mbar_init(&bar_consumed, kRowWarps);
+    mbar_init(&bar_ds, kRowWarps);
     mbar_init(&bar_done, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(&tmem_slot, 512);
     tmem_relinquish();
   }
@@ -179,7 +205,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (nq > 0) {
       if (lane == 0) {
@@ -219,7 +245,7 @@ __global__ void __launch_bounds__(192, 1)
           mbar_wait(&bar_q[u % STAGES], (u / STAGES) & 1, drain, kErrTimeoutTma);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && nq > 0) {
       constexpr uint32_t idesc_s = idesc_f16(kBN, kBM, BF, false, false);  // M = keys, N = queries
@@ -264,7 +290,7 @@ __global__ void __launch_bounds__(192, 1)
             acc2 = true;
           } else {
             mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
-            mma_tY<D>(tmem + C::COL_DK2, tmem + C::COL_A + 64, smem_u32(sQ2(st)), idesc_g, acc2);
+            mma_tY<D>(tmem + C::COL_DK2, tmem + C::COL_A + 32, smem_u32(sQ2(st)), idesc_g, acc2);
             acc1 = acc2 = true;
           }
         }
@@ -274,12 +300,12 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // ------------------------------------------- key-row softmax gradient
-    const int r = threadIdx.x;
-    const int j = k0 + r;  // this thread's key
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int hc = warp >> 2;      // column half of the tile this thread handles
+    const int cb = 64 * hc;        // first column of that half
+    const int j = k0 + (threadIdx.x & 127);  // this thread's key
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     bool ok = true;
     bool touched1 = false, touched2 = false;
-    int nstr = 0;
     for (int u = 0; u < nq; ++u) {
       const int st = u % STAGES;
       const int q0 = (i0 + u) * kBM;
@@ -290,76 +316,93 @@ __global__ void __launch_bounds__(192, 1)
       if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
       touched1 |= (cls & kNearB) != 0;
       touched2 |= (cls & kFarB) != 0;
-      uint32_t s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + C::COL_A + 32 * c, TB_CHUNK(s, c));
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(TB_CHUNK(s, c));
+      uint32_t s[64];
+      tmem_ld_x32(lane_addr + C::COL_A + cb, TB_CHUNK(s, 0));
+      tmem_ld_x32(lane_addr + C::COL_A + cb + 32, TB_CHUNK(s, 1));
+      tmem_ld_wait(TB_CHUNK(s, 0));
+      tmem_ld_wait(TB_CHUNK(s, 1));
       // far iff column c >= fl (query q0 + c, key j: q0 + c + P_SEQ - j >= w)
       const long long fl = (long long)j + args.w - args.P_SEQ - q0;
       if (cls == (kNearB | kFarB)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t s2[32];
-          tmem_ld_x32(lane_addr + C::COL_B + 32 * c, s2);
+          tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, s2);
           tmem_ld_wait(s2);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (32 * c + e >= fl) s[32 * c + e] = s2[e];
+            if (cb + 32 * c + e >= fl) s[32 * c + e] = s2[e];
         }
       }
-      // visible iff j <= q + P_SEQ, i.e. column c >= lo
-      const int lo = args.causal ? j - args.P_SEQ - q0 : -1;
-      float p[128];
+      // L * log2(e) of the 64 queries, four per vector load
+      const float4* L4 = reinterpret_cast<const float4*>(&sL[st][cb]);
+      float p[64];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float x = ex2(__uint_as_float(s[c]) * args.scale_log2 - sL[st][c]);
-        p[c] = (c >= lo) ? x : 0.f;
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = L4[c4];
+        p[4 * c4 + 0] = ex2(fmaf(__uint_as_float(s[4 * c4 + 0]), args.scale_log2, -l4.x));
+        p[4 * c4 + 1] = ex2(fmaf(__uint_as_float(s[4 * c4 + 1]), args.scale_log2, -l4.y));
+        p[4 * c4 + 2] = ex2(fmaf(__uint_as_float(s[4 * c4 + 2]), args.scale_log2, -l4.z));
+        p[4 * c4 + 3] = ex2(fmaf(__uint_as_float(s[4 * c4 + 3]), args.scale_log2, -l4.w));
+      }
+      // causal: key j visible from query q0 + c iff c >= j - P_SEQ - q0
+      if (args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) {
+        const int lo = j - args.P_SEQ - q0 - cb;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < lo) p[c] = 0.f;
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack2<BF>(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
-        tmem_st_x16(lane_addr + C::COL_A + 16 * c, pk);
+        tmem_st_x16(lane_addr + C::COL_A + cb + 16 * c, pk);
       }
       if (cls == (kNearB | kFarB)) {
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_consumed);
-        ++nstr;
       }
       if (!(ok = warp_wait(&bar_dp, u & 1, ctl, kErrTimeoutMma))) break;
       tc_fence_after();
+      const float4* D4 = reinterpret_cast<const float4*>(&sDelta[st][cb]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t dp[32];
-        tmem_ld_x32(lane_addr + C::COL_B + 32 * c, dp);
+        tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, dp);
         tmem_ld_wait(dp);
-        uint32_t pk1[16], pk2[16];
+        float ds[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = 32 * c + 2 * e;
-          const float ds0 = p[c0] * (__uint_as_float(dp[2 * e]) - sDelta[st][c0]);
-          const float ds1 = p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - sDelta[st][c0 + 1]);
-          if (cls == (kNearB | kFarB)) {
-            const bool f0 = c0 >= fl, f1 = c0 + 1 >= fl;
-            pk1[e] = pack2<BF>(f0 ? 0.f : ds0, f1 ? 0.f : ds1);
-            pk2[e] = pack2<BF>(f0 ? ds0 : 0.f, f1 ? ds1 : 0.f);
-          } else {
-            pk1[e] = pack2<BF>(ds0, ds1);
-          }
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 d4 = D4[8 * c + e4];
+          ds[4 * e4 + 0] = p[32 * c + 4 * e4 + 0] * (__uint_as_float(dp[4 * e4 + 0]) - d4.x);
+          ds[4 * e4 + 1] = p[32 * c + 4 * e4 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d4.y);
+          ds[4 * e4 + 2] = p[32 * c + 4 * e4 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d4.z);
+          ds[4 * e4 + 3] = p[32 * c + 4 * e4 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d4.w);
         }
-        tmem_st_x16(lane_addr + C::COL_B + 16 * c, pk1);
-        if (cls == (kNearB | kFarB)) tmem_st_x16(lane_addr + C::COL_A + 64 + 16 * c, pk2);
+        uint32_t pk1[16];
+        if (cls == (kNearB | kFarB)) {
+          uint32_t pk2[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const bool f0 = cb + 32 * c + 2 * e >= fl, f1 = cb + 32 * c + 2 * e + 1 >= fl;
+            pk1[e] = pack2<BF>(f0 ? 0.f : ds[2 * e], f1 ? 0.f : ds[2 * e + 1]);
+            pk2[e] = pack2<BF>(f0 ? ds[2 * e] : 0.f, f1 ? ds[2 * e + 1] : 0.f);
+          }
+          tmem_st_x16(lane_addr + C::COL_A + cb + 32 + 16 * c, pk2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk1[e] = pack2<BF>(ds[2 * e], ds[2 * e + 1]);
+        }
+        tmem_st_x16(lane_addr + C::COL_B + cb + 16 * c, pk1);
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_ds);
     }
-    (void)nstr;
     // ------------------------------------------------------------ epilogue
     if (nq > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
@@ -368,32 +411,27 @@ __global__ void __launch_bounds__(192, 1)
     const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * D;
     T* dv = reinterpret_cast<T*>(args.dv) + off;
     T* dk = reinterpret_cast<T*>(args.dk) + off;
+    const int dc = hc * (D / 2);  // this thread's half of the D columns
     if (live) {
-      epilogue_row<T, D>(lane_addr + C::COL_DV, dv, st_row, true, 1.f);
+      epilogue_half<T, D>(lane_addr + C::COL_DV, dv, dc, st_row, true, 1.f);
       if constexpr (!PW) {
-        epilogue_row<T, D>(lane_addr + C::COL_DK, dk, st_row, true, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, true, args.sm_scale);
       } else {
         T* dk2 = reinterpret_cast<T*>(args.dk2) + off;
-        epilogue_row<T, D>(lane_addr + C::COL_DK, dk, st_row, touched1, args.sm_scale);
-        epilogue_row<T, D>(lane_addr + C::COL_DK2, dk2, st_row, touched2, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, touched1, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DK2, dk2, dc, st_row, touched2, args.sm_scale);
       }
     } else if (st_row) {
-      uint32_t z[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) z[e] = 0;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        store_chunk32<T>(dv + 32 * c, z, 0.f);
-        store_chunk32<T>(dk + 32 * c, z, 0.f);
-        if constexpr (PW) store_chunk32<T>(reinterpret_cast<T*>(args.dk2) + off + 32 * c, z, 0.f);
-      }
+      zero_half<T, D>(dv, dc);
+      zero_half<T, D>(dk, dc);
+      if constexpr (PW) zero_half<T, D>(reinterpret_cast<T*>(args.dk2) + off, dc);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
 // ======================================================================
@@ -416,7 +454,7 @@ struct DqCfg {
 };
 
 template <typename T, int MODE, int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
@@ -459,12 +497,12 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(&bar_s, 1);
     mbar_init(&bar_dp, 1);
-    mbar_init(&bar_consumed, 4);
-    mbar_init(&bar_ds, 4);
+    mbar_init(&bar_consumed, kRowWarps);
+    mbar_init(&bar_ds, kRowWarps);
     mbar_init(&bar_done, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(&tmem_slot, 512);
     tmem_relinquish();
   }
@@ -473,7 +511,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && nkv > 0) {
       mbar_expect_tx(&bar_q, C::NRES * C::TILE);
@@ -500,7 +538,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int t = issued - STAGES > 0 ? issued - STAGES : 0; t < issued; ++t)
         mbar_wait(&bar_kv[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
     }
-  } else if (warp == 5) {
+  } else if (warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0 && nkv > 0) {
       constexpr uint32_t idesc_s = idesc_f16(kBM, kBN, BF, false, false);
@@ -543,7 +581,7 @@ __global__ void __launch_bounds__(192, 1)
             acc2 = true;
           } else {
             mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, acc1);
-            mma_tY<D>(tmem + C::COL_DQ2, tmem + C::COL_A + 64, smem_u32(sK2(st)), idesc_g, acc2);
+            mma_tY<D>(tmem + C::COL_DQ2, tmem + C::COL_A + 32, smem_u32(sK2(st)), idesc_g, acc2);
             acc1 = acc2 = true;
           }
         }
@@ -553,12 +591,13 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else {
     // --------------------------------------------- query-row softmax gradient
-    const int r = threadIdx.x;
-    const int row = q0 + r;
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int hc = warp >> 2;
+    const int cb = 64 * hc;
+    const int row = q0 + (threadIdx.x & 127);
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     const bool in_m = row < args.M;
     const size_t g = static_cast<size_t>(bh) * args.M + (in_m ? row : 0);
-    const float L2 = in_m ? args.lse[g] * kLog2e : INFINITY;
+    const float neg_L2 = in_m ? -args.lse[g] * kLog2e : -INFINITY;
     const float dlt = in_m ? args.delta[g] : 0.f;
     bool ok = true;
     bool touched1 = false, touched2 = false;
@@ -570,58 +609,67 @@ __global__ void __launch_bounds__(192, 1)
       if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
       touched1 |= (cls & kNearB) != 0;
       touched2 |= (cls & kFarB) != 0;
-      uint32_t s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + C::COL_A + 32 * c, TB_CHUNK(s, c));
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(TB_CHUNK(s, c));
+      uint32_t s[64];
+      tmem_ld_x32(lane_addr + C::COL_A + cb, TB_CHUNK(s, 0));
+      tmem_ld_x32(lane_addr + C::COL_A + cb + 32, TB_CHUNK(s, 1));
+      tmem_ld_wait(TB_CHUNK(s, 0));
+      tmem_ld_wait(TB_CHUNK(s, 1));
       // far iff key k0 + c satisfies row + P_SEQ - (k0 + c) >= w, i.e. c <= pwl
       const long long pwl = (long long)row + args.P_SEQ - k0 - args.w;
       if (cls == (kNearB | kFarB)) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t s2[32];
-          tmem_ld_x32(lane_addr + C::COL_B + 32 * c, s2);
+          tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, s2);
           tmem_ld_wait(s2);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (32 * c + e <= pwl) s[32 * c + e] = s2[e];
+            if (cb + 32 * c + e <= pwl) s[32 * c + e] = s2[e];
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_consumed);
       }
-      int lim = args.N - 1 - k0;  // keys past N are padding
-      if (args.causal) lim = min(lim, row + args.P_SEQ - k0);
-      float p[128];
+      float p[64];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float x = ex2(__uint_as_float(s[c]) * args.scale_log2 - L2);
-        p[c] = (c <= lim) ? x : 0.f;
+      for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(__uint_as_float(s[c]), args.scale_log2, neg_L2));
+      if ((args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) || k0 + kBN > args.N) {
+        int lim = args.N - 1 - k0;  // keys past N are padding
+        if (args.causal) lim = min(lim, row + args.P_SEQ - k0);
+        lim -= cb;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c > lim) p[c] = 0.f;
       }
       if (!(ok = warp_wait(&bar_dp, t & 1, ctl, kErrTimeoutMma))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t dp[32];
-        tmem_ld_x32(lane_addr + C::COL_B + 32 * c, dp);
+        tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, dp);
         tmem_ld_wait(dp);
-        uint32_t pk1[16], pk2[16];
+        uint32_t pk1[16];
+        if (cls == (kNearB | kFarB)) {
+          uint32_t pk2[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = 32 * c + 2 * e;
-          const float ds0 = p[c0] * (__uint_as_float(dp[2 * e]) - dlt);
-          const float ds1 = p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - dlt);
-          if (cls == (kNearB | kFarB)) {
-            const bool f0 = c0 <= pwl, f1 = c0 + 1 <= pwl;
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = 32 * c + 2 * e;
+            const float ds0 = p[c0] * (__uint_as_float(dp[2 * e]) - dlt);
+            const float ds1 = p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - dlt);
+            const bool f0 = cb + c0 <= pwl, f1 = cb + c0 + 1 <= pwl;
             pk1[e] = pack2<BF>(f0 ? 0.f : ds0, f1 ? 0.f : ds1);
             pk2[e] = pack2<BF>(f0 ? ds0 : 0.f, f1 ? ds1 : 0.f);
-          } else {
-            pk1[e] = pack2<BF>(ds0, ds1);
+          }
+          tmem_st_x16(lane_addr + C::COL_A + cb + 32 + 16 * c, pk2);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = 32 * c + 2 * e;
+            pk1[e] = pack2<BF>(p[c0] * (__uint_as_float(dp[2 * e]) - dlt),
+                               p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - dlt));
           }
         }
-        tmem_st_x16(lane_addr + C::COL_B + 16 * c, pk1);
-        if (cls == (kNearB | kFarB)) tmem_st_x16(lane_addr + C::COL_A + 64 + 16 * c, pk2);
+        tmem_st_x16(lane_addr + C::COL_B + cb + 16 * c, pk1);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -632,30 +680,25 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     const bool live = ok && nkv > 0;
     T* dq = reinterpret_cast<T*>(args.dq) + g * D;
+    const int dc = hc * (D / 2);
     if (live) {
       if constexpr (!PW) {
-        epilogue_row<T, D>(lane_addr + C::COL_DQ, dq, in_m, true, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, true, args.sm_scale);
       } else {
         T* dq2 = reinterpret_cast<T*>(args.dq2) + g * D;
-        epilogue_row<T, D>(lane_addr + C::COL_DQ, dq, in_m, touched1, args.sm_scale);
-        epilogue_row<T, D>(lane_addr + C::COL_DQ2, dq2, in_m, touched2, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, touched1, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DQ2, dq2, dc, in_m, touched2, args.sm_scale);
       }
     } else if (in_m) {
-      uint32_t z[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) z[e] = 0;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        store_chunk32<T>(dq + 32 * c, z, 0.f);
-        if constexpr (PW) store_chunk32<T>(reinterpret_cast<T*>(args.dq2) + g * D + 32 * c, z, 0.f);
-      }
+      zero_half<T, D>(dq, dc);
+      if constexpr (PW) zero_half<T, D>(reinterpret_cast<T*>(args.dq2) + g * D, dc);
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------- host side
@@ -670,7 +713,7 @@ static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_
     attr = true;
   }
   dim3 grid(a.BH, (a.N + kBN - 1) / kBN);
-  kern<<<grid, 192, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
+  kern<<<grid, kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
   return cudaGetLastError();
 }
 
@@ -685,7 +728,7 @@ static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t 
     attr = true;
   }
   dim3 grid(a.BH, (a.M + kBM - 1) / kBM);
-  kern<<<grid, 192, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
+  kern<<<grid, kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
   return cudaGetLastError();
 }
 

@@ -307,9 +307,10 @@ __global__ void __launch_bounds__(192, 1)
       for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + first_col + 32 * c, TA_CHUNK(s, c));
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(TA_CHUNK(s, c));
+      // raw scores; sm_scale * log2(e) > 0 is applied inside the exponent FMA
       float x[128];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(s[j]) * args.scale_log2;
+      for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(s[j]);
       if constexpr (MODE == kPiecewise) {
         if (cls == (kNear | kFar)) {
           // far iff c <= row + P_SEQ - k0 - w: take the (q2, k2) score there
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(192, 1)
             tmem_ld_wait(s2);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (32 * c + j <= pwl) x[32 * c + j] = __uint_as_float(s2[j]) * args.scale_log2;
+              if (32 * c + j <= pwl) x[32 * c + j] = __uint_as_float(s2[j]);
           }
         }
       }
@@ -334,10 +335,17 @@ __global__ void __launch_bounds__(192, 1)
         for (int j = 0; j < 128; ++j)
           if (j > lim) x[j] = -INFINITY;
       }
-      float mx = x[0];
+      // tree reductions: eight independent chains instead of one 128-long chain
+      float mx8[8];
 #pragma unroll
-      for (int j = 1; j < 128; ++j) mx = fmaxf(mx, x[j]);
-      const float m_new = fmaxf(m_ref, mx);
+      for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+      for (int j = 8; j < 128; j += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], x[j + k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_new = fmaxf(m_ref, mx * args.scale_log2);
       bool resc = false;
       float alpha = 1.f;
       if (t == 0) {
@@ -347,13 +355,14 @@ __global__ void __launch_bounds__(192, 1)
         alpha = ex2(m_ref - m_new);
         m_ref = m_new;
       }
-      const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs = 0.f;
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 128; ++j) {
-        x[j] = ex2(x[j] - m_use);
-        rs += x[j];
+        x[j] = ex2(fmaf(x[j], args.scale_log2, neg_m));
+        rs8[j & 7] += x[j];
       }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       l = l * alpha + rs;
       // P (16-bit, two per column) over the first 64 columns of the S buffer
       const uint32_t p_col = (MODE == kStd) ? s_col : C::COL_S0;
@@ -366,7 +375,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       if constexpr (MODE == kJvp) {
         // P o T (T = sm_scale * (tq k^T + q tk^T)) over the first 64 columns of T
-        float mpart = 0.f;
+        float mp4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t tr[32];
@@ -377,12 +386,12 @@ __global__ void __launch_bounds__(192, 1)
           for (int j = 0; j < 16; ++j) {
             const float a0 = x[32 * c + 2 * j] * __uint_as_float(tr[2 * j]) * args.sm_scale;
             const float a1 = x[32 * c + 2 * j + 1] * __uint_as_float(tr[2 * j + 1]) * args.sm_scale;
-            mpart += a0 + a1;
+            mp4[j & 3] += a0 + a1;
             pk[j] = pack2<BF>(a0, a1);
           }
           tmem_st_x16(lane_addr + C::COL_S1 + 16 * c, pk);
         }
-        mu = mu * alpha + mpart;
+        mu = mu * alpha + ((mp4[0] + mp4[1]) + (mp4[2] + mp4[3]));
       }
       // Correction: rescale the O (and U) rows once the previous P V landed.
       if (t > 0 && __any_sync(0xffffffffu, resc)) {
@@ -471,6 +480,278 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 5) tmem_dealloc(tmem, 512);
 }
 
+// ======================================================================
+//   Standard forward, two query tiles per CTA (ping-pong softmax groups)
+// ======================================================================
+// One CTA owns query rows [q0, q0 + 256) of one head as two 128-row tiles
+// that share every K/V tile.  Warps 0-3 run the softmax of tile 0, warps 4-7
+// that of tile 1, warp 8 is the TMA producer and warp 9 the MMA issuer, which
+// alternates between the tiles so one group's softmax overlaps the other
+// group's MMAs:  S0(t) S1(t) | PV0(t) S0(t+1) | PV1(t) S1(t+1) | ...
+template <int D>
+struct Fwd2Cfg {
+  static constexpr int BLK = kBM * 128;
+  static constexpr int TILE = (D / 64) * BLK;
+  static constexpr int STAGE = 2 * TILE;  // K, V
+  static constexpr int ST_FIT = (kSmemMax - 2048 - 2 * TILE) / STAGE;
+  static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
+  static constexpr int SMEM = 2 * TILE + STAGES * STAGE + 1024;
+  static constexpr int GROUP_HEADS = 8;  // heads whose tiles are scheduled together (L2 reuse of K/V)
+  static_assert(STAGES >= 2, "two K/V stages needed");
+  static_assert(256 + 2 * D <= 512, "TMEM overflow");
+};
+
+// Linear block index -> (head, pair of query tiles): groups of GROUP_HEADS
+// heads, and within a group the heaviest (last) causal tile pairs first.
+__device__ __forceinline__ void fwd2_decode(int id, int BH, int pairs, int G, int* bh, int* pair) {
+  const int per_group = G * pairs;
+  const int grp = id / per_group;
+  const int h0 = grp * G;
+  const int gh = min(G, BH - h0);  // heads in this (possibly last, smaller) group
+  const int within = id - grp * per_group;
+  *pair = pairs - 1 - within / gh;
+  *bh = h0 + within % gh;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+  using C = Fwd2Cfg<D>;
+  constexpr bool BF = DT<T>::bf16;
+  constexpr int STAGES = C::STAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q;
+  __shared__ __align__(8) uint64_t bar_k[STAGES], bar_v[STAGES], bar_empty[STAGES];
+  __shared__ __align__(8) uint64_t bar_s[2], bar_p[2], bar_o[2], bar_ofinal;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int pairs = (args.M + 2 * kBM - 1) / (2 * kBM);
+  int bh, pair;
+  fwd2_decode(blockIdx.x, args.BH, pairs, C::GROUP_HEADS, &bh, &pair);
+  const int q0 = pair * 2 * kBM;
+  int n_t[2];
+  n_t[0] = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
+  n_t[1] = kv_tiles_for(q0 + kBM, args.M, args.N, args.P_SEQ, args.causal);
+  const int nt = n_t[1] > n_t[0] ? n_t[1] : n_t[0];
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = base;  // tile 0 at sQ, tile 1 at sQ + TILE
+  uint8_t* sStages = base + 2 * C::TILE;
+  auto sK = [&](int st) { return sStages + st * C::STAGE; };
+  auto sV = [&](int st) { return sStages + st * C::STAGE + C::TILE; };
+
+  WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bar_k[s], 1);
+      mbar_init(&bar_v[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(&bar_s[w], 1);
+      mbar_init(&bar_p[w], 4);
+      mbar_init(&bar_o[w], 1);
+    }
+    mbar_init(&bar_ofinal, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t col_s[2] = {0u, 128u};
+  const uint32_t col_o[2] = {256u, 256u + D};
+
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_expect_tx(&bar_q, 2 * C::TILE);
+      load_tile<D>(sQ, &tm_q, &bar_q, q0, bh);
+      load_tile<D>(sQ + C::TILE, &tm_q, &bar_q, q0 + kBM, bh);
+      int issued = 0;
+      for (int t = 0; t < nt; ++t) {
+        const int st = t % STAGES;
+        if (t >= STAGES && !mbar_wait(&bar_empty[st], ((t / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
+        mbar_expect_tx(&bar_k[st], C::TILE);
+        load_tile<D>(sK(st), &tm_k, &bar_k[st], t * kBN, bh);
+        mbar_expect_tx(&bar_v[st], C::TILE);
+        load_tile<D>(sV(st), &tm_v, &bar_v[st], t * kBN, bh);
+        issued = t + 1;
+      }
+      int zero = 0;
+      WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
+      mbar_wait(&bar_q, 0, drain, kErrTimeoutTma);
+      for (int t = issued - STAGES > 0 ? issued - STAGES : 0; t < issued; ++t) {
+        mbar_wait(&bar_k[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
+        mbar_wait(&bar_v[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
+      }
+    }
+  } else if (warp == 9) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idesc_qk = idesc_f16(kBM, kBN, BF, false, false);
+      constexpr uint32_t idesc_pv = idesc_f16(kBM, D, BF, false, true);
+      const uint32_t aQ[2] = {smem_u32(sQ), smem_u32(sQ) + C::TILE};
+      bool ok = mbar_wait(&bar_q, 0, ctl, kErrTimeoutTma) && mbar_wait(&bar_k[0], 0, ctl, kErrTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        for (int w = 0; w < 2; ++w)
+          if (n_t[w] > 0) {
+            mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(0)), idesc_qk, false);
+            mma_commit(&bar_s[w]);
+          }
+      }
+      for (int t = 0; ok && t < nt; ++t) {
+        const int st = t % STAGES;
+        const int st1 = (t + 1) % STAGES;
+        if (!(ok = mbar_wait(&bar_v[st], (t / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+        const bool next = t + 1 < nt;
+        if (next && !(ok = mbar_wait(&bar_k[st1], ((t + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+        for (int w = 0; w < 2; ++w) {
+          if (t < n_t[w]) {
+            if (!(ok = mbar_wait(&bar_p[w], t & 1, ctl, kErrTimeoutSoftmax))) break;
+            tc_fence_after();
+            mma_pv<D>(tmem + col_o[w], tmem + col_s[w], smem_u32(sV(st)), idesc_pv, t > 0);
+            mma_commit(&bar_o[w]);
+          }
+          if (next && t + 1 < n_t[w]) {
+            mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(st1)), idesc_qk, false);
+            mma_commit(&bar_s[w]);
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bar_empty[st]);
+      }
+      if (ok) mma_commit(&bar_ofinal);
+    }
+  } else {
+    // ------------------------------- softmax / correction / epilogue (tile w)
+    const int w = warp >> 2;
+    const int r = threadIdx.x & 127;
+    const int row = q0 + w * kBM + r;
+    const int tq0 = q0 + w * kBM;  // first row of this group's tile
+    const int n = n_t[w];
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      if (!(ok = warp_wait(&bar_s[w], t & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+      const int k0 = t * kBN;
+      uint32_t s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + col_s[w] + 32 * c, TA_CHUNK(s, c));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_wait(TA_CHUNK(s, c));
+      float x[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(s[j]);
+      if ((args.causal && k0 + kBN - 1 > tq0 + args.P_SEQ) || (k0 + kBN > args.N)) {
+        int lim = args.N - 1 - k0;
+        if (args.causal) lim = min(lim, row + args.P_SEQ - k0);
+#pragma unroll
+        for (int j = 0; j < 128; ++j)
+          if (j > lim) x[j] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+      for (int j = 8; j < 128; j += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], x[j + k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float m_new = fmaxf(m_ref, mx * args.scale_log2);
+      bool resc = false;
+      float alpha = 1.f;
+      if (t == 0) {
+        m_ref = m_new;
+      } else if (m_new > m_ref + kRescaleThreshold) {
+        resc = true;
+        alpha = ex2(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(fmaf(x[32 * c + 2 * e], args.scale_log2, neg_m));
+          const float p1 = ex2(fmaf(x[32 * c + 2 * e + 1], args.scale_log2, neg_m));
+          rs8[(2 * e) & 7] += p0;
+          rs8[(2 * e + 1) & 7] += p1;
+          pk[e] = pack2<BF>(p0, p1);
+        }
+        tmem_st_x16(lane_addr + col_s[w] + 16 * c, pk);
+      }
+      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      l = l * alpha + rs;
+      if (t > 0 && __any_sync(0xffffffffu, resc)) {
+        if (!(ok = warp_wait(&bar_o[w], (t - 1) & 1, ctl, kErrTimeoutMma))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld_x32(lane_addr + col_o[w] + 32 * c, ov);
+          tmem_ld_wait(ov);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+          tmem_st_x32(lane_addr + col_o[w] + 32 * c, ov);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[w]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (nt > 0) ok = warp_wait(&bar_ofinal, 0, ctl, kErrTimeoutMma) && __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const bool live = ok && n > 0;
+    const float inv_l = (live && l > 0.f) ? 1.f / l : 0.f;
+    T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + (row < args.M ? row : 0)) * D;
+    if (row < args.M)
+      args.lse[static_cast<size_t>(bh) * args.M + row] = (live && l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      float of[32];
+      if (live) {
+        uint32_t ov[32];
+        tmem_ld_x32(lane_addr + col_o[w] + 32 * c, ov);
+        tmem_ld_wait(ov);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) of[j] = __uint_as_float(ov[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) of[j] = 0.f;
+      }
+      if (row < args.M) store_row_chunk<T>(orow + 32 * c, of, inv_l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
 // ---------------------------------------------------------------- host side
 template <typename T, int MODE, int D>
 static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
@@ -487,13 +768,32 @@ static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStrea
   return cudaGetLastError();
 }
 
+template <typename T, int D>
+static cudaError_t launch_fwd2_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
+  using C = Fwd2Cfg<D>;
+  auto kern = attn_fwd2_kernel<T, D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const long long pairs = (a.M + 2 * kBM - 1) / (2 * kBM);
+  const long long blocks = pairs * a.BH;
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s) {
+  if (mode == kStd) {
+    if (D == 64) return bf16 ? launch_fwd2_t<__nv_bfloat16, 64>(maps, a, s) : launch_fwd2_t<__half, 64>(maps, a, s);
+    if (D == 128) return bf16 ? launch_fwd2_t<__nv_bfloat16, 128>(maps, a, s) : launch_fwd2_t<__half, 128>(maps, a, s);
+  }
 #define TA_FWD_CASE(MODE_, D_)                                                          \
   if (mode == MODE_ && D == D_)                                                         \
     return bf16 ? launch_fwd_t<__nv_bfloat16, MODE_, D_>(maps, a, s)                    \
                 : launch_fwd_t<__half, MODE_, D_>(maps, a, s);
-  TA_FWD_CASE(kStd, 64)
-  TA_FWD_CASE(kStd, 128)
   TA_FWD_CASE(kPiecewise, 64)
   TA_FWD_CASE(kPiecewise, 128)
   TA_FWD_CASE(kJvp, 64)

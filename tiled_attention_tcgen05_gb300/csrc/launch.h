@@ -27,10 +27,20 @@ cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& maps, con
                             cudaStream_t s);
 cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& maps, const BwdArgs& a, cudaStream_t s);
 
-// Fills O = 0, L = -inf (rows that see no key) for BH*M rows.
-cudaError_t launch_empty_rows(bool bf16, int D, void* o, float* lse, void* to, long long rows, cudaStream_t s);
+// Fills O = 0, L = -inf (rows that see no key) for BH*M rows of D elements
+// of `esize` bytes.
+cudaError_t launch_empty_rows(int esize, int D, void* o, float* lse, void* to, long long rows, cudaStream_t s);
 // Zero-fills n bytes (gradients of keys no query sees).
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
+
+// fp32 mode (SIMT kernels, no TMA): plain float pointers.
+struct F32Ptrs {
+  const float *q, *k, *v, *q2, *k2, *v2, *dO;
+};
+cudaError_t launch_f32_fwd(int mode, int D, const F32Ptrs& p, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_f32_delta(int D, const float* o, const float* dO, float* delta, long long rows,
+                             cudaStream_t s);
+cudaError_t launch_f32_bwd(int mode, int D, const F32Ptrs& p, const BwdArgs& a, cudaStream_t s);
 
 // Profiling hooks (no-ops unless ta_profile_enable(1)).
 void prof_begin(const char* name, cudaStream_t s);
