@@ -9,7 +9,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/tattn.h"
+#include "tattn.h"
 #include "common.cuh"
 #include "launch.h"
 

@@ -62,11 +62,12 @@ __device__ __forceinline__ void load_tile_b(uint8_t* dst, const CUtensorMap* map
 // d = A B^T over D: A, B are 128-row x D K-major swizzled tiles in smem.
 template <int D>
 __device__ __forceinline__ void mma_abT(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
+  const uint64_t da = sdesc_sw128(a_smem, 16, 1024);
+  const uint64_t db = sdesc_sw128(b_smem, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(a_smem + off, 16, 1024), sdesc_sw128(b_smem + off, 16, 1024), idesc,
-           kk > 0 ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, da + off, db + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -76,10 +77,11 @@ __device__ __forceinline__ void mma_abT(uint32_t d_tmem, uint32_t a_smem, uint32
 template <int D>
 __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
                                        bool accumulate) {
+  const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk) {
     const uint32_t xc = x_tmem + (kk & 3) * 8 + (kk >> 2) * 64;
-    mma_ts(d_tmem, xc, sdesc_sw128(y_smem + kk * 16 * 128, kBM * 128, 1024), idesc,
+    mma_ts(d_tmem, xc, dy + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
   }
 }

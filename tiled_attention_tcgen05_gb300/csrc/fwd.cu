@@ -74,14 +74,18 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
 }
 
 // d = A B^T over the head dimension: A, B are 128 x D K-major swizzled tiles.
+// The descriptors are built once; each K-step adds its byte offset / 16 to
+// the 14-bit start-address field (shared addresses stay below 256 KB, so the
+// add never carries out of the field).
 template <int D>
 __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc,
                                        bool accumulate) {
+  const uint64_t da = sdesc_sw128(a_smem, 16, 1024);
+  const uint64_t db = sdesc_sw128(b_smem, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(a_smem + off, 16, 1024), sdesc_sw128(b_smem + off, 16, 1024), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, da + off, db + off, idesc, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -90,9 +94,10 @@ __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t a_smem, uint32_
 template <int D>
 __device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t idesc,
                                        bool accumulate) {
+  const uint64_t dv = sdesc_sw128(v_smem, kBM * 128, 1024);
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
-    mma_ts(d_tmem, p_tmem + kk * 8, sdesc_sw128(v_smem + kk * 16 * 128, kBM * 128, 1024), idesc,
+    mma_ts(d_tmem, p_tmem + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
            (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -488,16 +493,18 @@ __global__ void __launch_bounds__(192, 1)
 // that of tile 1, warp 8 is the TMA producer and warp 9 the MMA issuer, which
 // alternates between the tiles so one group's softmax overlaps the other
 // group's MMAs:  S0(t) S1(t) | PV0(t) S0(t+1) | PV1(t) S1(t+1) | ...
+// K and V have separate rings: a K tile is released as soon as both score
+// MMAs that read it have finished, so the K ring runs further ahead of the
+// MMAs than a joint K/V ring of the same size could.
 template <int D>
 struct Fwd2Cfg {
   static constexpr int BLK = kBM * 128;
   static constexpr int TILE = (D / 64) * BLK;
-  static constexpr int STAGE = 2 * TILE;  // K, V
-  static constexpr int ST_FIT = (kSmemMax - 2048 - 2 * TILE) / STAGE;
-  static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
-  static constexpr int SMEM = 2 * TILE + STAGES * STAGE + 1024;
+  static constexpr int KST = (D == 128) ? 3 : 4;  // K ring depth
+  static constexpr int VST = (D == 128) ? 2 : 4;  // V ring depth
+  static constexpr int SMEM = (2 + KST + VST) * TILE + 1024;
   static constexpr int GROUP_HEADS = 8;  // heads whose tiles are scheduled together (L2 reuse of K/V)
-  static_assert(STAGES >= 2, "two K/V stages needed");
+  static_assert(SMEM + 2048 <= kSmemMax, "tiles do not fit in shared memory");
   static_assert(256 + 2 * D <= 512, "TMEM overflow");
 };
 
@@ -519,11 +526,11 @@ __global__ void __launch_bounds__(320, 1)
                      const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
   using C = Fwd2Cfg<D>;
   constexpr bool BF = DT<T>::bf16;
-  constexpr int STAGES = C::STAGES;
+  constexpr int KST = C::KST, VST = C::VST;
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q;
-  __shared__ __align__(8) uint64_t bar_k[STAGES], bar_v[STAGES], bar_empty[STAGES];
+  __shared__ __align__(8) uint64_t bar_k[KST], bar_kempty[KST], bar_v[VST], bar_vempty[VST];
   __shared__ __align__(8) uint64_t bar_s[2], bar_p[2], bar_o[2], bar_ofinal;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -541,18 +548,20 @@ __global__ void __launch_bounds__(320, 1)
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;  // tile 0 at sQ, tile 1 at sQ + TILE
-  uint8_t* sStages = base + 2 * C::TILE;
-  auto sK = [&](int st) { return sStages + st * C::STAGE; };
-  auto sV = [&](int st) { return sStages + st * C::STAGE + C::TILE; };
+  auto sK = [&](int st) { return base + (2 + st) * C::TILE; };
+  auto sV = [&](int st) { return base + (2 + KST + st) * C::TILE; };
 
   WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(&bar_k[s], 1);
+      mbar_init(&bar_kempty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(&bar_v[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_vempty[s], 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&bar_s[w], 1);
@@ -575,30 +584,35 @@ __global__ void __launch_bounds__(320, 1)
 
   if (warp == 8) {
     // ------------------------------------------------------ TMA producer
-    if (lane == 0 && nt > 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      mbar_expect_tx(&bar_q, 2 * C::TILE);
-      load_tile<D>(sQ, &tm_q, &bar_q, q0, bh);
-      load_tile<D>(sQ + C::TILE, &tm_q, &bar_q, q0 + kBM, bh);
+    // lane 0 feeds Q and the K ring, lane 1 the V ring, independently
+    if (lane < 2 && nt > 0) {
+      const bool is_k = (lane == 0);
+      const int depth = is_k ? KST : VST;
+      uint64_t* full = is_k ? bar_k : bar_v;
+      uint64_t* empty = is_k ? bar_kempty : bar_vempty;
+      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        mbar_expect_tx(&bar_q, 2 * C::TILE);
+        load_tile<D>(sQ, &tm_q, &bar_q, q0, bh);
+        load_tile<D>(sQ + C::TILE, &tm_q, &bar_q, q0 + kBM, bh);
+      } else {
+        tma_prefetch_desc(&tm_v);
+      }
       int issued = 0;
       for (int t = 0; t < nt; ++t) {
-        const int st = t % STAGES;
-        if (t >= STAGES && !mbar_wait(&bar_empty[st], ((t / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
-        mbar_expect_tx(&bar_k[st], C::TILE);
-        load_tile<D>(sK(st), &tm_k, &bar_k[st], t * kBN, bh);
-        mbar_expect_tx(&bar_v[st], C::TILE);
-        load_tile<D>(sV(st), &tm_v, &bar_v[st], t * kBN, bh);
+        const int st = t % depth;
+        if (t >= depth && !mbar_wait(&empty[st], ((t / depth) - 1) & 1, ctl, kErrTimeoutMma)) break;
+        mbar_expect_tx(&full[st], C::TILE);
+        load_tile<D>(is_k ? sK(st) : sV(st), map, &full[st], t * kBN, bh);
         issued = t + 1;
       }
       int zero = 0;
       WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
-      mbar_wait(&bar_q, 0, drain, kErrTimeoutTma);
-      for (int t = issued - STAGES > 0 ? issued - STAGES : 0; t < issued; ++t) {
-        mbar_wait(&bar_k[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
-        mbar_wait(&bar_v[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
-      }
+      if (is_k) mbar_wait(&bar_q, 0, drain, kErrTimeoutTma);
+      for (int t = issued - depth > 0 ? issued - depth : 0; t < issued; ++t)
+        mbar_wait(&full[t % depth], (t / depth) & 1, drain, kErrTimeoutTma);
     }
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
@@ -615,26 +629,28 @@ __global__ void __launch_bounds__(320, 1)
             mma_commit(&bar_s[w]);
           }
       }
+      if (ok) mma_commit(&bar_kempty[0]);  // K tile 0 is consumed once both score MMAs finish
       for (int t = 0; ok && t < nt; ++t) {
-        const int st = t % STAGES;
-        const int st1 = (t + 1) % STAGES;
-        if (!(ok = mbar_wait(&bar_v[st], (t / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+        const int sv = t % VST;
+        const int sk1 = (t + 1) % KST;
+        if (!(ok = mbar_wait(&bar_v[sv], (t / VST) & 1, ctl, kErrTimeoutTma))) break;
         const bool next = t + 1 < nt;
-        if (next && !(ok = mbar_wait(&bar_k[st1], ((t + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+        if (next && !(ok = mbar_wait(&bar_k[sk1], ((t + 1) / KST) & 1, ctl, kErrTimeoutTma))) break;
         for (int w = 0; w < 2; ++w) {
           if (t < n_t[w]) {
             if (!(ok = mbar_wait(&bar_p[w], t & 1, ctl, kErrTimeoutSoftmax))) break;
             tc_fence_after();
-            mma_pv<D>(tmem + col_o[w], tmem + col_s[w], smem_u32(sV(st)), idesc_pv, t > 0);
+            mma_pv<D>(tmem + col_o[w], tmem + col_s[w], smem_u32(sV(sv)), idesc_pv, t > 0);
             mma_commit(&bar_o[w]);
           }
           if (next && t + 1 < n_t[w]) {
-            mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(st1)), idesc_qk, false);
+            mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(sk1)), idesc_qk, false);
             mma_commit(&bar_s[w]);
           }
         }
         if (!ok) break;
-        mma_commit(&bar_empty[st]);
+        mma_commit(&bar_vempty[sv]);
+        if (next) mma_commit(&bar_kempty[sk1]);
       }
       if (ok) mma_commit(&bar_ofinal);
     }

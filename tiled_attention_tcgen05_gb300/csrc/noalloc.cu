@@ -11,7 +11,7 @@
 // the call itself allocates nothing.
 #include <mutex>
 
-#include "../../include/tattn.h"
+#include "tattn.h"
 #include "common.cuh"
 
 namespace ta {
