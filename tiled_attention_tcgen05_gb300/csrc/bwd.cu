@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int kt = blockIdx.y;
+  int bh, kt;  // key tiles with the most query tiles (the first ones, causal) first
+  grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt);
   const int k0 = kt * kBN;
   const int num_q_tiles = (args.M + kBM - 1) / kBM;
   const int i0 = first_q_tile_for(k0, args.P_SEQ, args.causal);
@@ -474,9 +474,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
   const int num_q_tiles = (args.M + kBM - 1) / kBM;
-  const int qt = num_q_tiles - 1 - blockIdx.y;  // heaviest causal tiles first
+  int bh, rank;
+  grouped_tile(blockIdx.x, args.BH, num_q_tiles, kGroupHeads, &bh, &rank);
+  const int qt = num_q_tiles - 1 - rank;  // heaviest causal tiles first
   const int q0 = qt * kBM;
   const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
 
@@ -703,6 +704,261 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
+// ======================================================================
+//      dQ, standard mode: Q and dO in TMEM, three-or-more-deep K/V ring
+// ======================================================================
+// Q and dO are the A operands of S = Q K^T and dP = dO V^T for every key
+// tile, so they live in TMEM (two 16-bit elements per column) and those MMAs
+// read only K or V from shared memory.  Q and dO arrive by TMA in the last
+// slot of the K/V ring; the softmax warps copy them into TMEM, after which the
+// slot joins the ring.  The softmax warps also release the S buffer as soon
+// as they have loaded S(t), so S(t + 1) is computed while they work on t:
+//   S(0) dP(0) | S(t+1) | dQ(t) dP(t+1) | ...
+template <int D>
+struct DqStdCfg {
+  static constexpr int BLK = kBM * 128;
+  static constexpr int TILE = (D / 64) * BLK;
+  static constexpr int STAGE = 2 * TILE;  // K, V
+  static constexpr int ST_FIT = (kSmemMax - 2048) / STAGE;
+  static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
+  static constexpr int SMEM = STAGES * STAGE + 1024;
+  static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DQ = 256;
+  static constexpr uint32_t COL_QT = 256 + D, COL_DOT = 256 + D + D / 2;
+  static_assert(STAGES >= 3, "K/V ring too shallow");
+  static_assert(COL_DOT + D / 2 <= 512, "TMEM overflow");
+};
+
+// d = A B^T over D with A (128 rows x D, 16-bit) in TMEM, 8 packed columns
+// per K-step from a_tmem, and B a 128-row x D K-major swizzled tile in smem.
+template <int D>
+__device__ __forceinline__ void mma_tB(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc) {
+  const uint64_t db = sdesc_sw128(b_smem, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+    mma_ts(d_tmem, a_tmem + kk * 8, db + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Copies row r of a 128 x D 16-bit K-major 128-byte-swizzled tile from shared
+// memory into TMEM lane r, columns taddr .. taddr + D/2 (two elements per
+// column, lower index in the low half): the layout an A operand is read in.
+// Warp-collective.
+template <int D>
+__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uint32_t taddr) {
+#pragma unroll
+  for (int kb = 0; kb < D / 64; ++kb) {
+    uint32_t v[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 c = *reinterpret_cast<const uint4*>(tile + kb * (kBM * 128) + r * 128 + ((j ^ (r & 7)) * 16));
+      v[4 * j + 0] = c.x;
+      v[4 * j + 1] = c.y;
+      v[4 * j + 2] = c.z;
+      v[4 * j + 3] = c.w;
+    }
+    tmem_st_x32(taddr + 32 * kb, v);
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dq_std_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                           const BwdArgs args) {
+  using C = DqStdCfg<D>;
+  constexpr bool BF = DT<T>::bf16;
+  constexpr int STAGES = C::STAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q, bar_qfree, bar_kv[STAGES], bar_kvempty[STAGES];
+  __shared__ __align__(8) uint64_t bar_s, bar_consumed, bar_dp, bar_ds, bar_done;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_q_tiles = (args.M + kBM - 1) / kBM;
+  int bh, rank;
+  grouped_tile(blockIdx.x, args.BH, num_q_tiles, kGroupHeads, &bh, &rank);
+  const int qt = num_q_tiles - 1 - rank;  // heaviest causal tiles first
+  const int q0 = qt * kBM;
+  const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
+
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  auto sK = [&](int st) { return base + st * C::STAGE; };
+  auto sV = [&](int st) { return base + st * C::STAGE + C::TILE; };
+  uint8_t* sQ = sK(STAGES - 1);  // Q and dO transit through the last ring slot
+  uint8_t* sDO = sV(STAGES - 1);
+
+  WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_qfree, kRowWarps);
+    for (int st = 0; st < STAGES; ++st) {
+      mbar_init(&bar_kv[st], 1);
+      mbar_init(&bar_kvempty[st], 1);
+    }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_consumed, kRowWarps);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_ds, kRowWarps);
+    mbar_init(&bar_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nkv > 0) {
+      mbar_expect_tx(&bar_q, 2 * C::TILE);
+      load_tile_b<D>(sQ, &tm_q, &bar_q, q0, bh);
+      load_tile_b<D>(sDO, &tm_do, &bar_q, q0, bh);
+      int issued = 0;
+      for (int t = 0; t < nkv; ++t) {
+        const int st = t % STAGES;
+        if (t >= STAGES) {
+          if (!mbar_wait(&bar_kvempty[st], ((t / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
+        } else if (st == STAGES - 1) {  // the slot still holds Q and dO until they are in TMEM
+          if (!mbar_wait(&bar_qfree, 0, ctl, kErrTimeoutSoftmax)) break;
+        }
+        mbar_expect_tx(&bar_kv[st], 2 * C::TILE);
+        load_tile_b<D>(sK(st), &tm_k, &bar_kv[st], t * kBN, bh);
+        load_tile_b<D>(sV(st), &tm_v, &bar_kv[st], t * kBN, bh);
+        issued = t + 1;
+      }
+      int zero = 0;
+      WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
+      mbar_wait(&bar_q, 0, drain, kErrTimeoutTma);
+      for (int t = issued - STAGES > 0 ? issued - STAGES : 0; t < issued; ++t)
+        mbar_wait(&bar_kv[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
+    }
+  } else if (warp == kWarpMma) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0 && nkv > 0) {
+      constexpr uint32_t idesc_s = idesc_f16(kBM, kBN, BF, false, false);
+      constexpr uint32_t idesc_g = idesc_f16(kBM, D, BF, false, true);
+      bool ok = mbar_wait(&bar_qfree, 0, ctl, kErrTimeoutSoftmax) && mbar_wait(&bar_kv[0], 0, ctl, kErrTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        mma_tB<D>(tmem + C::COL_A, tmem + C::COL_QT, smem_u32(sK(0)), idesc_s);   // S = Q K^T
+        mma_commit(&bar_s);
+        mma_tB<D>(tmem + C::COL_B, tmem + C::COL_DOT, smem_u32(sV(0)), idesc_s);  // dP = dO V^T
+        mma_commit(&bar_dp);
+      }
+      for (int t = 0; ok && t < nkv; ++t) {
+        const int st = t % STAGES;
+        const int st1 = (t + 1) % STAGES;
+        const bool next = t + 1 < nkv;
+        if (next) {
+          if (!(ok = mbar_wait(&bar_consumed, t & 1, ctl, kErrTimeoutSoftmax))) break;
+          if (!(ok = mbar_wait(&bar_kv[st1], ((t + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+          tc_fence_after();
+          mma_tB<D>(tmem + C::COL_A, tmem + C::COL_QT, smem_u32(sK(st1)), idesc_s);
+          mma_commit(&bar_s);
+        }
+        if (!(ok = mbar_wait(&bar_ds, t & 1, ctl, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, t > 0);  // dQ += dS K
+        mma_commit(&bar_kvempty[st]);
+        if (next) {
+          mma_tB<D>(tmem + C::COL_B, tmem + C::COL_DOT, smem_u32(sV(st1)), idesc_s);
+          mma_commit(&bar_dp);
+        }
+      }
+      if (ok) mma_commit(&bar_done);
+    }
+  } else {
+    // --------------------------------------------- query-row softmax gradient
+    const int hc = warp >> 2;  // key half of the tile: columns [64 hc, 64 hc + 64)
+    const int cb = 64 * hc;
+    const int r = threadIdx.x & 127;
+    const int row = q0 + r;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const bool in_m = row < args.M;
+    const size_t g = static_cast<size_t>(bh) * args.M + (in_m ? row : 0);
+    const float neg_L2 = in_m ? -args.lse[g] * kLog2e : -INFINITY;
+    const float dlt = in_m ? args.delta[g] : 0.f;
+    bool ok = true;
+    if (nkv > 0) {  // group 0 copies Q, group 1 copies dO into TMEM
+      ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma);
+      if (ok) {
+        tile_row_to_tmem<D>(hc == 0 ? sQ : sDO, r, lane_addr + (hc == 0 ? C::COL_QT : C::COL_DOT));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_qfree);
+      }
+    }
+    for (int t = 0; ok && t < nkv; ++t) {
+      const int k0 = t * kBN;
+      if (!(ok = warp_wait(&bar_s, t & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld_x32(lane_addr + C::COL_A + cb, TB_CHUNK(sv, 0));
+      tmem_ld_x32(lane_addr + C::COL_A + cb + 32, TB_CHUNK(sv, 1));
+      tmem_ld_wait(TB_CHUNK(sv, 0));
+      tmem_ld_wait(TB_CHUNK(sv, 1));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_consumed);  // S buffer free for S(t + 1)
+      float p[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(__uint_as_float(sv[c]), args.scale_log2, neg_L2));
+      if ((args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) || k0 + kBN > args.N) {
+        int lim = args.N - 1 - k0;  // keys past N are padding
+        if (args.causal) lim = min(lim, row + args.P_SEQ - k0);
+        lim -= cb;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c > lim) p[c] = 0.f;
+      }
+      if (!(ok = warp_wait(&bar_dp, t & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dp[32];
+        tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, dp);
+        tmem_ld_wait(dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = 32 * c + 2 * e;
+          pk[e] = pack2<BF>(p[c0] * (__uint_as_float(dp[2 * e]) - dlt),
+                            p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - dlt));
+        }
+        tmem_st_x16(lane_addr + C::COL_B + cb + 16 * c, pk);  // dS (16-bit) over dP
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ds);
+    }
+    if (nkv > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
+    tc_fence_after();
+    T* dq = reinterpret_cast<T*>(args.dq) + g * D;
+    const int dc = hc * (D / 2);
+    if (ok && nkv > 0) {
+      epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, true, args.sm_scale);
+    } else if (in_m) {
+      zero_half<T, D>(dq, dc);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+}
+
 // ---------------------------------------------------------------- host side
 template <typename T, int MODE, int D>
 static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
@@ -714,8 +970,9 @@ static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(a.BH, (a.N + kBN - 1) / kBN);
-  kern<<<grid, kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
+  const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
   return cudaGetLastError();
 }
 
@@ -729,8 +986,9 @@ static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t 
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid(a.BH, (a.M + kBM - 1) / kBM);
-  kern<<<grid, kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
+  const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
   return cudaGetLastError();
 }
 
@@ -741,9 +999,25 @@ cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& m, const 
   return cudaErrorNotSupported;
 }
 
+template <typename T, int D>
+static cudaError_t launch_dq_std_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
+  using C = DqStdCfg<D>;
+  auto kern = attn_bwd_dq_std_kernel<T, D>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
-  if (mode == kStd && D == 64) return bf16 ? launch_dq_t<__nv_bfloat16, kStd, 64>(m, a, s) : launch_dq_t<__half, kStd, 64>(m, a, s);
-  if (mode == kStd && D == 128) return bf16 ? launch_dq_t<__nv_bfloat16, kStd, 128>(m, a, s) : launch_dq_t<__half, kStd, 128>(m, a, s);
+  if (mode == kStd && D == 64) return bf16 ? launch_dq_std_t<__nv_bfloat16, 64>(m, a, s) : launch_dq_std_t<__half, 64>(m, a, s);
+  if (mode == kStd && D == 128) return bf16 ? launch_dq_std_t<__nv_bfloat16, 128>(m, a, s) : launch_dq_std_t<__half, 128>(m, a, s);
   if (mode == kPiecewise && D == 64) return bf16 ? launch_dq_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dq_t<__half, kPiecewise, 64>(m, a, s);
   return cudaErrorNotSupported;
 }

@@ -71,6 +71,21 @@ __host__ __device__ inline int first_q_tile_for(int k0, int P_SEQ, int causal) {
   return first_row / kBM;
 }
 
+// Linear block index -> (head, rank of the tile within its head): heads are
+// taken in groups of G (so the resident CTAs of one wave share the K/V or
+// Q/dO of only G heads and reuse them through L2), and within a group rank 0
+// (the caller's heaviest tile) comes first for every head.
+__device__ __forceinline__ void grouped_tile(int id, int BH, int ntiles, int G, int* bh, int* rank) {
+  const int per_group = G * ntiles;
+  const int grp = id / per_group;
+  const int h0 = grp * G;
+  const int gh = min(G, BH - h0);  // heads in this (possibly last, smaller) group
+  const int within = id - grp * per_group;
+  *rank = within / gh;
+  *bh = h0 + within % gh;
+}
+constexpr int kGroupHeads = 8;
+
 template <typename T>
 struct DT;
 template <>

@@ -503,22 +503,9 @@ struct Fwd2Cfg {
   static constexpr int KST = (D == 128) ? 3 : 4;  // K ring depth
   static constexpr int VST = (D == 128) ? 2 : 4;  // V ring depth
   static constexpr int SMEM = (2 + KST + VST) * TILE + 1024;
-  static constexpr int GROUP_HEADS = 8;  // heads whose tiles are scheduled together (L2 reuse of K/V)
   static_assert(SMEM + 2048 <= kSmemMax, "tiles do not fit in shared memory");
   static_assert(256 + 2 * D <= 512, "TMEM overflow");
 };
-
-// Linear block index -> (head, pair of query tiles): groups of GROUP_HEADS
-// heads, and within a group the heaviest (last) causal tile pairs first.
-__device__ __forceinline__ void fwd2_decode(int id, int BH, int pairs, int G, int* bh, int* pair) {
-  const int per_group = G * pairs;
-  const int grp = id / per_group;
-  const int h0 = grp * G;
-  const int gh = min(G, BH - h0);  // heads in this (possibly last, smaller) group
-  const int within = id - grp * per_group;
-  *pair = pairs - 1 - within / gh;
-  *bh = h0 + within % gh;
-}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(320, 1)
@@ -538,8 +525,9 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int pairs = (args.M + 2 * kBM - 1) / (2 * kBM);
-  int bh, pair;
-  fwd2_decode(blockIdx.x, args.BH, pairs, C::GROUP_HEADS, &bh, &pair);
+  int bh, rank;
+  grouped_tile(blockIdx.x, args.BH, pairs, kGroupHeads, &bh, &rank);
+  const int pair = pairs - 1 - rank;  // heaviest causal pairs first
   const int q0 = pair * 2 * kBM;
   int n_t[2];
   n_t[0] = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
