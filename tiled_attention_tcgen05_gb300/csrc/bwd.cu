@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     abort_flag = 0;
     mbar_init(&bar_kv, 1);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bar_q[s], 1);
+      mbar_init(&bar_q[s], 2);  // TMA bytes + L/delta stores
       mbar_init(&bar_qempty[s], 1);
     }
     mbar_init(&bar_s, 1);
@@ -216,6 +216,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if constexpr (PW) load_tile_b<D>(sK2, &tm_k2, &bar_kv, k0, bh);
         load_tile_b<D>(sV, &tm_v, &bar_kv, k0, bh);
       }
+      // L * log2(e) and delta of a query tile are fetched into registers one
+      // tile ahead, so that when a stage frees the TMA is issued at once and
+      // the global-load latency stays off the critical path.  A stage's
+      // barrier takes two arrivals: the TMA byte count and the L/delta stores.
+      float lv[kBM / 32], dv[kBM / 32];
+      auto fetch = [&](int u) {
+        const int q0 = (i0 + u) * kBM;
+#pragma unroll
+        for (int e = 0; e < kBM / 32; ++e) {
+          const int q = q0 + lane + 32 * e;
+          const size_t g = static_cast<size_t>(bh) * args.M + q;
+          lv[e] = (q < args.M) ? args.lse[g] * kLog2e : INFINITY;
+          dv[e] = (q < args.M) ? args.delta[g] : 0.f;
+        }
+      };
+      fetch(0);
       int issued = 0;
       for (int u = 0; u < nq; ++u) {
         const int st = u % STAGES;
@@ -223,21 +239,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!warp_wait(&bar_qempty[st], ((u / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
         }
         const int q0 = (i0 + u) * kBM;
-#pragma unroll
-        for (int e = lane; e < kBM; e += 32) {
-          const int q = q0 + e;
-          const size_t g = static_cast<size_t>(bh) * args.M + q;
-          sL[st][e] = (q < args.M) ? args.lse[g] * kLog2e : INFINITY;
-          sDelta[st][e] = (q < args.M) ? args.delta[g] : 0.f;
-        }
-        __syncwarp();
         if (lane == 0) {
           mbar_expect_tx(&bar_q[st], C::NQT * C::TILE);
           load_tile_b<D>(sQ(st), &tm_q, &bar_q[st], q0, bh);
           if constexpr (PW) load_tile_b<D>(sQ2(st), &tm_q2, &bar_q[st], q0, bh);
           load_tile_b<D>(sDO(st), &tm_do, &bar_q[st], q0, bh);
         }
+#pragma unroll
+        for (int e = 0; e < kBM / 32; ++e) {
+          sL[st][lane + 32 * e] = lv[e];
+          sDelta[st][lane + 32 * e] = dv[e];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_q[st]);
         issued = u + 1;
+        if (u + 1 < nq) fetch(u + 1);
       }
       if (lane == 0) {  // never leave a TMA write in flight behind an early exit
         int zero = 0;
@@ -959,6 +975,313 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
+// ======================================================================
+//        dK, dV, standard mode: score MMA one query tile ahead
+// ======================================================================
+// The softmax warps load S^T(u) into registers and release the score buffer
+// at once (bar_consumed), so S^T(u + 1) is computed while they work on u;
+// they write P^T and dS^T (16-bit, interleaved 16 + 16 packed columns per
+// 32-column chunk) over dP^T, where dV and dK read them:
+//   S^T(0) dP^T(0) | S^T(u+1) | dV(u) dK(u) dP^T(u+1) | ...
+// That needs Q(u + 1) a whole tile earlier than a plain ring provides, so Q
+// has its own ring (3 deep at D = 128) and dO a separate one (2 deep), and the
+// per-query L and delta are loaded by the softmax warps themselves, a tile
+// ahead, into a small double buffer instead of riding with the Q stages.
+//
+// Every byte of shared memory the kernel uses lives in the dynamic region
+// (no static __shared__), in this order from the first 1024-byte boundary:
+// K, V, the Q ring, the dO ring (128-byte swizzled tiles), L and delta
+// (double-buffered, see below), then the mbarriers and flags.  The tiles
+// leave too little room for a full 1024-byte alignment allowance, so the
+// kernel checks the actual padding against PAD at run time and reports
+// kErrSmemLayout instead of running if it does not fit.
+template <int D>
+struct DkdvStdCfg {
+  static constexpr int BLK = kBM * 128;
+  static constexpr int TILE = (D / 64) * BLK;
+  static constexpr int QST = (D == 128) ? 3 : 4;  // Q ring depth
+  static constexpr int OST = (D == 128) ? 2 : 4;  // dO ring depth
+  static constexpr int LD_OFF = (2 + QST + OST) * TILE;  // L / delta: [buffer][half][L, delta][64] floats
+  static constexpr int LD_BYTES = 2 * 2 * 2 * 64 * 4;
+  static constexpr int BAR_OFF = LD_OFF + LD_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int USED = BAR_OFF + BAR_BYTES;
+  static constexpr int PAD = (kSmemMax - USED) < 1023 ? (kSmemMax - USED) : 1023;  // alignment allowance
+  static constexpr int SMEM = USED + PAD;
+  static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D;
+  static_assert(PAD >= 0 && SMEM <= kSmemMax, "tiles do not fit in shared memory");
+  static_assert(BAR_BYTES >= 8 * (1 + 2 * QST + 2 * OST + 5 + 4) + 8, "barrier area too small");
+  static_assert(COL_DK + D <= 512, "TMEM overflow");
+};
+
+// d (+)= X Y with X's K-steps interleaved: step kk at x + (kk / 2) * 32 +
+// (kk % 2) * 8 (16 packed columns in each 32-column chunk); Y as in mma_tY.
+template <int D>
+__device__ __forceinline__ void mma_tY_il(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
+                                          bool accumulate) {
+  const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
+#pragma unroll
+  for (int kk = 0; kk < 128 / 16; ++kk) {
+    mma_ts(d_tmem, x_tmem + (kk >> 1) * 32 + (kk & 1) * 8, dy + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_dkdv_std_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                             const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                             const BwdArgs args) {
+  using C = DkdvStdCfg<D>;
+  constexpr bool BF = DT<T>::bf16;
+  constexpr int QST = C::QST, OST = C::OST;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (base - smem_raw > C::PAD) {  // uniform across the CTA: nothing has been touched yet
+    if (threadIdx.x == 0 && args.err) atomicOr(args.err, kErrSmemLayout);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + C::BAR_OFF);
+  uint64_t& bar_kv = bars[0];
+  uint64_t* bar_qf = bars + 1;
+  uint64_t* bar_qe = bar_qf + QST;
+  uint64_t* bar_of = bar_qe + QST;
+  uint64_t* bar_oe = bar_of + OST;
+  uint64_t& bar_s = bar_oe[OST];
+  uint64_t& bar_consumed = bar_oe[OST + 1];
+  uint64_t& bar_dp = bar_oe[OST + 2];
+  uint64_t& bar_ds = bar_oe[OST + 3];
+  uint64_t& bar_done = bar_oe[OST + 4];
+  uint64_t* bar_pub = bar_oe + OST + 5;  // [buffer * 2 + half]: L / delta of a tile stored
+  uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(bar_pub + 4);
+  int& abort_flag = *(reinterpret_cast<int*>(bar_pub + 4) + 1);
+  float* sLD = reinterpret_cast<float*>(base + C::LD_OFF);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  int bh, kt;  // key tiles with the most query tiles (the first ones, causal) first
+  grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt);
+  const int k0 = kt * kBN;
+  const int num_q_tiles = (args.M + kBM - 1) / kBM;
+  const int i0 = first_q_tile_for(k0, args.P_SEQ, args.causal);
+  const int nq = num_q_tiles > i0 ? num_q_tiles - i0 : 0;
+
+  uint8_t* sK = base;
+  uint8_t* sV = base + C::TILE;
+  auto sQ = [&](int i) { return base + (2 + i) * C::TILE; };
+  auto sDO = [&](int i) { return base + (2 + QST + i) * C::TILE; };
+
+  WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_kv, 1);
+    for (int i = 0; i < QST; ++i) {
+      mbar_init(&bar_qf[i], 1);
+      mbar_init(&bar_qe[i], 1);
+    }
+    for (int i = 0; i < OST; ++i) {
+      mbar_init(&bar_of[i], 1);
+      mbar_init(&bar_oe[i], 1);
+    }
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_consumed, kRowWarps);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_ds, kRowWarps);
+    mbar_init(&bar_done, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bar_pub[i], kRowWarps / 2);
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == kWarpProducer) {
+    // ---------------------- producer: lane 0 K, V and the Q ring; lane 1 the dO ring
+    if (lane < 2 && nq > 0) {
+      const bool is_q = (lane == 0);
+      const int depth = is_q ? QST : OST;
+      uint64_t* full = is_q ? bar_qf : bar_of;
+      uint64_t* empty = is_q ? bar_qe : bar_oe;
+      const CUtensorMap* map = is_q ? &tm_q : &tm_do;
+      if (is_q) {
+        mbar_expect_tx(&bar_kv, 2 * C::TILE);
+        load_tile_b<D>(sK, &tm_k, &bar_kv, k0, bh);
+        load_tile_b<D>(sV, &tm_v, &bar_kv, k0, bh);
+      }
+      int issued = 0;
+      for (int u = 0; u < nq; ++u) {
+        const int st = u % depth;
+        if (u >= depth && !mbar_wait(&empty[st], ((u / depth) - 1) & 1, ctl, kErrTimeoutMma)) break;
+        mbar_expect_tx(&full[st], C::TILE);
+        load_tile_b<D>(is_q ? sQ(st) : sDO(st), map, &full[st], (i0 + u) * kBM, bh);
+        issued = u + 1;
+      }
+      int zero = 0;
+      WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
+      if (is_q) mbar_wait(&bar_kv, 0, drain, kErrTimeoutTma);
+      for (int u = issued - depth > 0 ? issued - depth : 0; u < issued; ++u)
+        mbar_wait(&full[u % depth], (u / depth) & 1, drain, kErrTimeoutTma);
+    }
+  } else if (warp == kWarpMma) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0 && nq > 0) {
+      constexpr uint32_t idesc_s = idesc_f16(kBN, kBM, BF, false, false);  // M = keys, N = queries
+      constexpr uint32_t idesc_g = idesc_f16(kBN, D, BF, false, true);     // M = keys, N = D
+      bool ok = mbar_wait(&bar_kv, 0, ctl, kErrTimeoutTma) && mbar_wait(&bar_qf[0], 0, ctl, kErrTimeoutTma) &&
+                mbar_wait(&bar_of[0], 0, ctl, kErrTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(0)), idesc_s);   // S^T = K Q^T
+        mma_commit(&bar_s);
+        mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(0)), idesc_s);  // dP^T = V dO^T
+        mma_commit(&bar_dp);
+      }
+      for (int u = 0; ok && u < nq; ++u) {
+        const int sq = u % QST, so = u % OST;
+        const int sq1 = (u + 1) % QST, so1 = (u + 1) % OST;
+        const bool next = u + 1 < nq;
+        if (next) {
+          if (!(ok = mbar_wait(&bar_consumed, u & 1, ctl, kErrTimeoutSoftmax))) break;
+          if (!(ok = mbar_wait(&bar_qf[sq1], ((u + 1) / QST) & 1, ctl, kErrTimeoutTma))) break;
+          tc_fence_after();
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(sq1)), idesc_s);
+          mma_commit(&bar_s);
+        }
+        if (!(ok = mbar_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        mma_tY_il<D>(tmem + C::COL_DV, tmem + C::COL_B, smem_u32(sDO(so)), idesc_g, u > 0);      // dV += P^T dO
+        mma_commit(&bar_oe[so]);
+        mma_tY_il<D>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, u > 0);  // dK += dS^T Q
+        mma_commit(&bar_qe[sq]);
+        if (next) {
+          if (!(ok = mbar_wait(&bar_of[so1], ((u + 1) / OST) & 1, ctl, kErrTimeoutTma))) break;
+          tc_fence_after();
+          mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(so1)), idesc_s);
+          mma_commit(&bar_dp);
+        }
+      }
+      if (ok) mma_commit(&bar_done);
+    }
+  } else {
+    // ------------------------------------------- key-row softmax gradient
+    const int hc = warp >> 2;                // query half of the tile: columns [64 hc, 64 hc + 64)
+    const int cb = 64 * hc;
+    const int j = k0 + (threadIdx.x & 127);  // this thread's key
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    // L and delta of the half's 64 queries: the half's 128 threads each load
+    // one of the 128 values (coalesced) a tile ahead, store it once they are
+    // done with the current tile and publish the buffer on bar_pub; the
+    // reads are then shared-memory broadcasts.  Queries past M read L = +inf
+    // (P = 0) and delta = 0.
+    const int ld_arr = (threadIdx.x & 127) >> 6;  // 0: L, 1: delta
+    const int ld_col = threadIdx.x & 63;
+    auto ld_fetch = [&](int u) -> float {
+      const int q = (i0 + u) * kBM + cb + ld_col;
+      if (q >= args.M) return ld_arr ? 0.f : INFINITY;
+      return __ldg((ld_arr ? args.delta : args.lse) + static_cast<size_t>(bh) * args.M + q);
+    };
+    auto ld_slot = [&](int u) { return sLD + ((u & 1) * 2 + hc) * 128; };
+    if (nq > 0) {
+      ld_slot(0)[ld_arr * 64 + ld_col] = ld_fetch(0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pub[hc]);
+    }
+    bool ok = true;
+    for (int u = 0; u < nq; ++u) {
+      const int q0 = (i0 + u) * kBM;
+      const int qb = q0 + cb;  // first query of this thread's columns
+      const float pre = (u + 1 < nq) ? ld_fetch(u + 1) : 0.f;
+      if (!(ok = warp_wait(&bar_s, u & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld_x32(lane_addr + C::COL_A + cb, TB_CHUNK(sv, 0));
+      tmem_ld_x32(lane_addr + C::COL_A + cb + 32, TB_CHUNK(sv, 1));
+      tmem_ld_wait(TB_CHUNK(sv, 0));
+      tmem_ld_wait(TB_CHUNK(sv, 1));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_consumed);  // score buffer free for S^T(u + 1)
+      if (!(ok = warp_wait(&bar_pub[(u & 1) * 2 + hc], (u >> 1) & 1, ctl, kErrTimeoutSoftmax))) break;
+      const float* sL = ld_slot(u);
+      const float* sD = sL + 64;
+      float p[64];
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = *reinterpret_cast<const float4*>(sL + 4 * c4);
+        p[4 * c4 + 0] = ex2(fmaf(__uint_as_float(sv[4 * c4 + 0]), args.scale_log2, -l4.x * kLog2e));
+        p[4 * c4 + 1] = ex2(fmaf(__uint_as_float(sv[4 * c4 + 1]), args.scale_log2, -l4.y * kLog2e));
+        p[4 * c4 + 2] = ex2(fmaf(__uint_as_float(sv[4 * c4 + 2]), args.scale_log2, -l4.z * kLog2e));
+        p[4 * c4 + 3] = ex2(fmaf(__uint_as_float(sv[4 * c4 + 3]), args.scale_log2, -l4.w * kLog2e));
+      }
+      if (args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) {  // key j visible from q iff q >= j - P_SEQ
+        const int lo = j - args.P_SEQ - qb;
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < lo) p[c] = 0.f;
+      }
+      if (!(ok = warp_wait(&bar_dp, u & 1, ctl, kErrTimeoutMma))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        // chunk c (32 queries): read dP^T, write P^T and dS^T (16 packed
+        // columns each) back into the same 32 columns
+        uint32_t dp[32];
+        tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, dp);
+        tmem_ld_wait(dp);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int e4 = 0; e4 < 8; ++e4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(sD + 32 * c + 4 * e4);
+          const int c0 = 32 * c + 4 * e4;
+          pp[2 * e4] = pack2<BF>(p[c0], p[c0 + 1]);
+          pp[2 * e4 + 1] = pack2<BF>(p[c0 + 2], p[c0 + 3]);
+          pd[2 * e4] = pack2<BF>(p[c0] * (__uint_as_float(dp[4 * e4]) - d4.x),
+                                 p[c0 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d4.y));
+          pd[2 * e4 + 1] = pack2<BF>(p[c0 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d4.z),
+                                     p[c0 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d4.w));
+        }
+        tmem_st_x16(lane_addr + C::COL_B + cb + 32 * c, pp);
+        tmem_st_x16(lane_addr + C::COL_B + cb + 32 * c + 16, pd);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ds);
+      if (u + 1 < nq) {  // every warp of the half is past tile u - 1, the buffer's previous tile
+        ld_slot(u + 1)[ld_arr * 64 + ld_col] = pre;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_pub[((u + 1) & 1) * 2 + hc]);
+      }
+    }
+    // ------------------------------------------------------------ epilogue
+    if (nq > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
+    tc_fence_after();
+    const bool st_row = j < args.N;
+    const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * D;
+    T* dvp = reinterpret_cast<T*>(args.dv) + off;
+    T* dkp = reinterpret_cast<T*>(args.dk) + off;
+    const int dc = hc * (D / 2);
+    if (ok && nq > 0) {
+      epilogue_half<T, D>(lane_addr + C::COL_DV, dvp, dc, st_row, true, 1.f);
+      epilogue_half<T, D>(lane_addr + C::COL_DK, dkp, dc, st_row, true, args.sm_scale);
+    } else if (st_row) {
+      zero_half<T, D>(dvp, dc);
+      zero_half<T, D>(dkp, dc);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+}
+
 // ---------------------------------------------------------------- host side
 template <typename T, int MODE, int D>
 static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
@@ -992,9 +1315,25 @@ static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t 
   return cudaGetLastError();
 }
 
+template <typename T, int D>
+static cudaError_t launch_dkdv_std_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
+  using C = DkdvStdCfg<D>;
+  auto kern = attn_bwd_dkdv_std_kernel<T, D>;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
+  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
-  if (mode == kStd && D == 64) return bf16 ? launch_dkdv_t<__nv_bfloat16, kStd, 64>(m, a, s) : launch_dkdv_t<__half, kStd, 64>(m, a, s);
-  if (mode == kStd && D == 128) return bf16 ? launch_dkdv_t<__nv_bfloat16, kStd, 128>(m, a, s) : launch_dkdv_t<__half, kStd, 128>(m, a, s);
+  if (mode == kStd && D == 64) return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 64>(m, a, s) : launch_dkdv_std_t<__half, 64>(m, a, s);
+  if (mode == kStd && D == 128) return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 128>(m, a, s) : launch_dkdv_std_t<__half, 128>(m, a, s);
   if (mode == kPiecewise && D == 64) return bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dkdv_t<__half, kPiecewise, 64>(m, a, s);
   return cudaErrorNotSupported;
 }

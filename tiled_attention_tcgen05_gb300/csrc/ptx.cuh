@@ -17,6 +17,7 @@ enum : uint32_t {
   kErrTimeoutMma = 1u << 1,    // a wait for an MMA result ran out
   kErrTimeoutSoftmax = 1u << 2,  // a wait for softmax/producer output ran out
   kErrTimeoutOther = 1u << 3,
+  kErrSmemLayout = 1u << 4,    // a kernel could not lay out its shared memory (did not run)
 };
 
 struct WaitCtl {
