@@ -126,6 +126,7 @@ __device__ __forceinline__ void zero_half(T* row, int c0) {
 }
 
 #define TB_CHUNK(arr, c) (*reinterpret_cast<uint32_t(*)[32]>(&(arr)[32 * (c)]))
+#define TB_CHUNK16(arr, c) (*reinterpret_cast<uint32_t(*)[16]>(&(arr)[16 * (c)]))
 
 // ======================================================================
 //                        dK, dV (key-stationary)
@@ -1199,55 +1200,80 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float pre = (u + 1 < nq) ? ld_fetch(u + 1) : 0.f;
       if (!(ok = warp_wait(&bar_s, u & 1, ctl, kErrTimeoutMma))) break;
       tc_fence_after();
+      // 16-lane shapes: in each 16-lane group g of its warp, thread t holds
+      // keys (t / 4) and (t / 4 + 8) at the query pairs 8 jj + 2 m, +1
+      // (m = t % 4) of the half, so it needs 16 of the half's L and delta
+      // values instead of 64.  sv[32 g + 4 jj + e], e = {(k, q), (k, q + 1),
+      // (k + 8, q), (k + 8, q + 1)}.
       uint32_t sv[64];
-      tmem_ld_x32(lane_addr + C::COL_A + cb, TB_CHUNK(sv, 0));
-      tmem_ld_x32(lane_addr + C::COL_A + cb + 32, TB_CHUNK(sv, 1));
+      tmem_ld_16x256b_x8(lane_addr + C::COL_A + cb, TB_CHUNK(sv, 0));
+      tmem_ld_16x256b_x8(lane_addr + (16u << 16) + C::COL_A + cb, TB_CHUNK(sv, 1));
       tmem_ld_wait(TB_CHUNK(sv, 0));
       tmem_ld_wait(TB_CHUNK(sv, 1));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_consumed);  // score buffer free for S^T(u + 1)
       if (!(ok = warp_wait(&bar_pub[(u & 1) * 2 + hc], (u >> 1) & 1, ctl, kErrTimeoutSoftmax))) break;
-      const float* sL = ld_slot(u);
+      const int m = lane & 3;
+      const float* sL = ld_slot(u) + 2 * m;
       const float* sD = sL + 64;
       float p[64];
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(sL + 4 * c4);
-        p[4 * c4 + 0] = ex2(fmaf(__uint_as_float(sv[4 * c4 + 0]), args.scale_log2, -l4.x * kLog2e));
-        p[4 * c4 + 1] = ex2(fmaf(__uint_as_float(sv[4 * c4 + 1]), args.scale_log2, -l4.y * kLog2e));
-        p[4 * c4 + 2] = ex2(fmaf(__uint_as_float(sv[4 * c4 + 2]), args.scale_log2, -l4.z * kLog2e));
-        p[4 * c4 + 3] = ex2(fmaf(__uint_as_float(sv[4 * c4 + 3]), args.scale_log2, -l4.w * kLog2e));
-      }
-      if (args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) {  // key j visible from q iff q >= j - P_SEQ
-        const int lo = j - args.P_SEQ - qb;
+      for (int jj = 0; jj < 8; ++jj) {
+        const float2 l2 = *reinterpret_cast<const float2*>(sL + 8 * jj);
+        const float n0 = -l2.x * kLog2e, n1 = -l2.y * kLog2e;
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < lo) p[c] = 0.f;
+        for (int g = 0; g < 2; ++g) {
+          const int i = 32 * g + 4 * jj;
+          p[i + 0] = ex2(fmaf(__uint_as_float(sv[i + 0]), args.scale_log2, n0));
+          p[i + 1] = ex2(fmaf(__uint_as_float(sv[i + 1]), args.scale_log2, n1));
+          p[i + 2] = ex2(fmaf(__uint_as_float(sv[i + 2]), args.scale_log2, n0));
+          p[i + 3] = ex2(fmaf(__uint_as_float(sv[i + 3]), args.scale_log2, n1));
+        }
+      }
+      if (args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) {  // key k visible from q iff q >= k - P_SEQ
+        // element (g, jj, e) is masked iff 8 jj + (e & 1) < lo + 16 g + 8 (e >> 1)
+        const int lo = k0 + 32 * (warp & 3) + (lane >> 2) - args.P_SEQ - qb - 2 * m;
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (8 * jj + (e & 1) < lo + 16 * g + 8 * (e >> 1)) p[32 * g + 4 * jj + e] = 0.f;
       }
       if (!(ok = warp_wait(&bar_dp, u & 1, ctl, kErrTimeoutMma))) break;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         // chunk c (32 queries): read dP^T, write P^T and dS^T (16 packed
-        // columns each) back into the same 32 columns
-        uint32_t dp[32];
-        tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, dp);
-        tmem_ld_wait(dp);
-        uint32_t pp[16], pd[16];
+        // columns each, pair 4 jq + m) back into the same 32 columns
+        uint32_t dp[32];  // [g][16]
+        tmem_ld_16x256b_x4(lane_addr + C::COL_B + cb + 32 * c, TB_CHUNK16(dp, 0));
+        tmem_ld_16x256b_x4(lane_addr + (16u << 16) + C::COL_B + cb + 32 * c, TB_CHUNK16(dp, 1));
+        tmem_ld_wait(TB_CHUNK16(dp, 0));
+        tmem_ld_wait(TB_CHUNK16(dp, 1));
+        float2 d2[4];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(sD + 32 * c + 4 * e4);
-          const int c0 = 32 * c + 4 * e4;
-          pp[2 * e4] = pack2<BF>(p[c0], p[c0 + 1]);
-          pp[2 * e4 + 1] = pack2<BF>(p[c0 + 2], p[c0 + 3]);
-          pd[2 * e4] = pack2<BF>(p[c0] * (__uint_as_float(dp[4 * e4]) - d4.x),
-                                 p[c0 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d4.y));
-          pd[2 * e4 + 1] = pack2<BF>(p[c0 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d4.z),
-                                     p[c0 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d4.w));
+        for (int jq = 0; jq < 4; ++jq) d2[jq] = *reinterpret_cast<const float2*>(sD + 8 * (4 * c + jq));
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          uint32_t pp[8], pd[8];
+#pragma unroll
+          for (int jq = 0; jq < 4; ++jq) {
+            const int i = 32 * g + 4 * (4 * c + jq);
+            const int di = 16 * g + 4 * jq;
+            pp[2 * jq] = pack2<BF>(p[i], p[i + 1]);
+            pp[2 * jq + 1] = pack2<BF>(p[i + 2], p[i + 3]);
+            pd[2 * jq] = pack2<BF>(p[i] * (__uint_as_float(dp[di]) - d2[jq].x),
+                                   p[i + 1] * (__uint_as_float(dp[di + 1]) - d2[jq].y));
+            pd[2 * jq + 1] = pack2<BF>(p[i + 2] * (__uint_as_float(dp[di + 2]) - d2[jq].x),
+                                       p[i + 3] * (__uint_as_float(dp[di + 3]) - d2[jq].y));
+          }
+          const uint32_t ga = lane_addr + (static_cast<uint32_t>(16 * g) << 16) + C::COL_B + cb + 32 * c;
+          tmem_st_16x128b_x4(ga, pp);
+          tmem_st_16x128b_x4(ga + 16, pd);
         }
-        tmem_st_x16(lane_addr + C::COL_B + cb + 32 * c, pp);
-        tmem_st_x16(lane_addr + C::COL_B + cb + 32 * c + 16, pd);
       }
       tmem_st_wait();
       tc_fence_before();
