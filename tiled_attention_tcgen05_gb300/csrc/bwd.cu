@@ -929,7 +929,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(&bar_consumed);  // S buffer free for S(t + 1)
       float p[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) p[c] = ex2(fmaf(__uint_as_float(sv[c]), args.scale_log2, neg_L2));
+      for (int c = 0; c < 64; c += 2) {
+        const float2 y = ffma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                               make_float2(args.scale_log2, args.scale_log2), make_float2(neg_L2, neg_L2));
+        p[c] = ex2(y.x);
+        p[c + 1] = ex2(y.y);
+      }
       if ((args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) || k0 + kBN > args.N) {
         int lim = args.N - 1 - k0;  // keys past N are padding
         if (args.causal) lim = min(lim, row + args.P_SEQ - k0);
@@ -949,8 +954,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int c0 = 32 * c + 2 * e;
-          pk[e] = pack2<BF>(p[c0] * (__uint_as_float(dp[2 * e]) - dlt),
-                            p[c0 + 1] * (__uint_as_float(dp[2 * e + 1]) - dlt));
+          const float2 ds = fmul2(make_float2(p[c0], p[c0 + 1]),
+                                  fadd2(make_float2(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                        make_float2(-dlt, -dlt)));
+          pk[e] = pack2<BF>(ds.x, ds.y);
         }
         tmem_st_x16(lane_addr + C::COL_B + cb + 16 * c, pk);  // dS (16-bit) over dP
       }
@@ -1217,18 +1224,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int m = lane & 3;
       const float* sL = ld_slot(u) + 2 * m;
       const float* sD = sL + 64;
+      const float2 sc2 = make_float2(args.scale_log2, args.scale_log2);
       float p[64];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const float2 l2 = *reinterpret_cast<const float2*>(sL + 8 * jj);
-        const float n0 = -l2.x * kLog2e, n1 = -l2.y * kLog2e;
+        const float2 nl = fmul2(l2, make_float2(-kLog2e, -kLog2e));
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const int i = 32 * g + 4 * jj;
-          p[i + 0] = ex2(fmaf(__uint_as_float(sv[i + 0]), args.scale_log2, n0));
-          p[i + 1] = ex2(fmaf(__uint_as_float(sv[i + 1]), args.scale_log2, n1));
-          p[i + 2] = ex2(fmaf(__uint_as_float(sv[i + 2]), args.scale_log2, n0));
-          p[i + 3] = ex2(fmaf(__uint_as_float(sv[i + 3]), args.scale_log2, n1));
+          const float2 y0 = ffma2(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sc2, nl);
+          const float2 y1 = ffma2(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])), sc2, nl);
+          p[i + 0] = ex2(y0.x);
+          p[i + 1] = ex2(y0.y);
+          p[i + 2] = ex2(y1.x);
+          p[i + 3] = ex2(y1.y);
         }
       }
       if (args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) {  // key k visible from q iff q >= k - P_SEQ
@@ -1253,9 +1263,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_ld_16x256b_x4(lane_addr + (16u << 16) + C::COL_B + cb + 32 * c, TB_CHUNK16(dp, 1));
         tmem_ld_wait(TB_CHUNK16(dp, 0));
         tmem_ld_wait(TB_CHUNK16(dp, 1));
-        float2 d2[4];
+        float2 nd2[4];  // -delta of the thread's query pairs
 #pragma unroll
-        for (int jq = 0; jq < 4; ++jq) d2[jq] = *reinterpret_cast<const float2*>(sD + 8 * (4 * c + jq));
+        for (int jq = 0; jq < 4; ++jq) {
+          const float2 d2 = *reinterpret_cast<const float2*>(sD + 8 * (4 * c + jq));
+          nd2[jq] = make_float2(-d2.x, -d2.y);
+        }
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           uint32_t pp[8], pd[8];
@@ -1265,10 +1278,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int di = 16 * g + 4 * jq;
             pp[2 * jq] = pack2<BF>(p[i], p[i + 1]);
             pp[2 * jq + 1] = pack2<BF>(p[i + 2], p[i + 3]);
-            pd[2 * jq] = pack2<BF>(p[i] * (__uint_as_float(dp[di]) - d2[jq].x),
-                                   p[i + 1] * (__uint_as_float(dp[di + 1]) - d2[jq].y));
-            pd[2 * jq + 1] = pack2<BF>(p[i + 2] * (__uint_as_float(dp[di + 2]) - d2[jq].x),
-                                       p[i + 3] * (__uint_as_float(dp[di + 3]) - d2[jq].y));
+            const float2 s0 = fmul2(make_float2(p[i], p[i + 1]),
+                                    fadd2(make_float2(__uint_as_float(dp[di]), __uint_as_float(dp[di + 1])), nd2[jq]));
+            const float2 s1 = fmul2(make_float2(p[i + 2], p[i + 3]),
+                                    fadd2(make_float2(__uint_as_float(dp[di + 2]), __uint_as_float(dp[di + 3])), nd2[jq]));
+            pd[2 * jq] = pack2<BF>(s0.x, s0.y);
+            pd[2 * jq + 1] = pack2<BF>(s1.x, s1.y);
           }
           const uint32_t ga = lane_addr + (static_cast<uint32_t>(16 * g) << 16) + C::COL_B + cb + 32 * c;
           tmem_st_16x128b_x4(ga, pp);

@@ -671,15 +671,15 @@ __global__ void __launch_bounds__(320, 1)
         for (int j = 0; j < 128; ++j)
           if (j > lim) x[j] = -INFINITY;
       }
-      float mx8[8];
+      float mx8[8];  // eight three-input max chains of 16 scores each
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+      for (int k = 0; k < 8; ++k) {
+        mx8[k] = fmax3(x[k], x[8 + k], x[16 + k]);
 #pragma unroll
-      for (int j = 8; j < 128; j += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmaxf(mx8[k], x[j + k]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int j = 24; j < 120; j += 16) mx8[k] = fmax3(mx8[k], x[j + k], x[j + 8 + k]);
+        mx8[k] = fmaxf(mx8[k], x[120 + k]);
+      }
+      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
       const float m_new = fmaxf(m_ref, mx * args.scale_log2);
       bool resc = false;
       float alpha = 1.f;
@@ -691,21 +691,26 @@ __global__ void __launch_bounds__(320, 1)
         m_ref = m_new;
       }
       const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // P = 2^(x c - m): scale, shift and row sum two columns per packed
+      // instruction (the softmax warps share issue slots with the MMA warp,
+      // so their instruction count is what limits the step).
+      const float2 sc2 = make_float2(args.scale_log2, args.scale_log2);
+      const float2 nm2 = make_float2(neg_m, neg_m);
+      float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(x[32 * c + 2 * e], args.scale_log2, neg_m));
-          const float p1 = ex2(fmaf(x[32 * c + 2 * e + 1], args.scale_log2, neg_m));
-          rs8[(2 * e) & 7] += p0;
-          rs8[(2 * e + 1) & 7] += p1;
-          pk[e] = pack2<BF>(p0, p1);
+          const float2 y = ffma2(make_float2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nm2);
+          const float2 pr = make_float2(ex2(y.x), ex2(y.y));
+          rs2[e & 3] = fadd2(rs2[e & 3], pr);
+          pk[e] = pack2<BF>(pr.x, pr.y);
         }
         tmem_st_x16(lane_addr + col_s[w] + 16 * c, pk);
       }
-      const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+      const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
+      const float rs = rsa.x + rsa.y;
       l = l * alpha + rs;
       if (t > 0 && __any_sync(0xffffffffu, resc)) {
         if (!(ok = warp_wait(&bar_o[w], (t - 1) & 1, ctl, kErrTimeoutMma))) break;
