@@ -23,7 +23,10 @@
  *  - causal != 0 keeps key j for query i iff j <= i + (N - M) (bottom-right
  *    alignment, [PW] _fwd_kernel; for M == N this is j <= i as in [FA-JVP]).
  *  - sm_scale <= 0 (or not finite) selects 1/sqrt(D), like the pages' None.
- *  - D must be 64 or 128.  dt TA_F16 / TA_BF16 run the tcgen05 kernels (P
+ *  - D must be 16, 32, 64 or 128 (the head sizes both pages' kernels accept
+ *    up to 128; D = 16 and 32 run the D = 64 kernels with the columns past D
+ *    read as zeros and never written).  dt TA_F16 / TA_BF16 run the tcgen05
+ *    kernels (P
  *    and dS rounded to 16 bits as MMA operands, fp32 accumulation); TA_F32
  *    is the fp32 mode: float32 tensors computed in float32 with SIMT FMA
  *    and accurate expf/logf (a correctness path, not a throughput path).
@@ -122,7 +125,7 @@ size_t piecewise_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype
  * dS = P o (dP - delta) is routed to (dq1, dk1) where distance < w and to
  * (dq2, dk2) where distance >= w; dv = P^T dO.
  * Out: dq1, dq2 [B,H,M,D], dk1, dk2, dv [B,H,N,D] (dt).
- * 16-bit dtypes support D = 64 only (the key-stationary pass keeps dV, dK1
+ * 16-bit dtypes support D <= 64 only (the key-stationary pass keeps dV, dK1
  * and dK2 of a 128-key tile in tensor memory); D = 128 returns
  * TA_ERR_UNSUPPORTED unless dt is TA_F32. */
 ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,

@@ -27,6 +27,8 @@ FWD_CASES = [
     (1, 1, 5, 700, 64, "bf16", False),
     (1, 1, 700, 5, 128, "f16", False),
     (2, 1, 129, 257, 64, "bf16", True),
+    (1, 2, 200, 200, 32, "bf16", True),    # D = 32, 16: the D = 64 kernels over zero-filled columns
+    (1, 2, 131, 257, 16, "f16", False),
 ]
 
 
@@ -64,7 +66,8 @@ def test_bwd_small(gpu_lib, B, H, M, N, D, dtype, causal):
 
 @pytest.mark.parametrize("B,H,M,N,D,dtype,causal", [
     (1, 2, 128, 128, 64, "f16", False), (1, 2, 256, 256, 64, "f16", True), (1, 2, 256, 256, 128, "bf16", True),
-    (1, 1, 200, 333, 64, "f16", True), (1, 1, 333, 200, 128, "bf16", False), (1, 1, 300, 100, 64, "f16", True)])
+    (1, 1, 200, 333, 64, "f16", True), (1, 1, 333, 200, 128, "bf16", False), (1, 1, 300, 100, 64, "f16", True),
+    (1, 2, 200, 200, 32, "bf16", True), (1, 1, 130, 190, 16, "f16", False)])
 def test_jvp_small(gpu_lib, B, H, M, N, D, dtype, causal):
     ta = gpu_lib
     names = ("q", "k", "v", "tq", "tk", "tv")
@@ -88,6 +91,8 @@ PW_CASES = [
     (1, 2, 200, 333, 64, "bf16", True, 77),
     (1, 2, 333, 200, 64, "f16", True, 64),
     (1, 1, 512, 512, 128, "bf16", True, 256),  # forward only at D = 128
+    (1, 2, 256, 256, 32, "bf16", True, 60),
+    (1, 1, 200, 200, 16, "f16", True, 33),
 ]
 
 
@@ -225,7 +230,8 @@ F32_TOL = 1e-4
 
 
 @pytest.mark.parametrize("B,H,M,N,D,causal", [(1, 2, 128, 128, 64, False), (1, 2, 200, 333, 128, True),
-                                              (1, 1, 333, 200, 64, True), (2, 1, 96, 96, 128, False)])
+                                              (1, 1, 333, 200, 64, True), (2, 1, 96, 96, 128, False),
+                                              (1, 2, 150, 150, 32, True), (1, 1, 100, 170, 16, False)])
 def test_fp32_mode_fwd_bwd_jvp(gpu_lib, B, H, M, N, D, causal):
     ta = gpu_lib
     names = ("q", "k", "v", "do", "tq", "tk", "tv")
@@ -247,7 +253,7 @@ def test_fp32_mode_fwd_bwd_jvp(gpu_lib, B, H, M, N, D, causal):
         compare(name, got, ref, F32_TOL)
 
 
-@pytest.mark.parametrize("D,w", [(64, 100), (128, 40), (64, -20)])
+@pytest.mark.parametrize("D,w", [(64, 100), (128, 40), (64, -20), (32, 0), (16, 50)])
 def test_fp32_mode_piecewise(gpu_lib, D, w):
     import synth_inputs as si
     ta = gpu_lib

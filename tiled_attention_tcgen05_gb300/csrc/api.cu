@@ -57,7 +57,8 @@ static EncodeTiledFn encode_fn() {
 }
 
 // [BH, S, D] 16-bit tensor viewed as a 3-D map with 64 x 128 x 1 boxes and
-// 128-byte swizzle; rows past S read as zeros.
+// 128-byte swizzle; rows past S (and, for D < 64, columns past D) read as
+// zeros.
 static bool make_map(CUtensorMap* map, const void* ptr, long long BH, long long S, int D, bool bf16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -128,7 +129,7 @@ struct Problem {
 static ta_status check_common(int B, int H, int M, int N, int D, ta_dtype dt, float sm_scale, Problem* pr) {
   if (B < 0 || H < 0 || M < 0 || N < 0) return TA_ERR_INVALID_ARG;
   if (dt != TA_F16 && dt != TA_BF16 && dt != TA_F32) return TA_ERR_UNSUPPORTED;
-  if (D != 64 && D != 128) return TA_ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return TA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffll) return TA_ERR_INVALID_ARG;
   if ((M + kBM - 1) / kBM > 65535 || (N + kBN - 1) / kBN > 65535) return TA_ERR_UNSUPPORTED;
@@ -167,6 +168,7 @@ static FwdArgs fwd_args(const Problem& p, int causal, int w, void* o, float* lse
   a.w = w;
   a.sm_scale = p.sm_scale;
   a.scale_log2 = p.sm_scale * kLog2e;
+  a.dg = p.D;
   a.err = error_word_ptr();
   a.timeout_ns = g_timeout_ns;
   return a;
@@ -184,10 +186,16 @@ static BwdArgs bwd_args(const Problem& p, int causal, int w, const float* lse, c
   a.w = w;
   a.sm_scale = p.sm_scale;
   a.scale_log2 = p.sm_scale * kLog2e;
+  a.dg = p.D;
   a.err = error_word_ptr();
   a.timeout_ns = g_timeout_ns;
   return a;
 }
+
+// Head dimension the 16-bit tensor-core kernels are instantiated for: D = 16
+// and 32 run the D = 64 kernels, whose TMA boxes are 64 columns wide; the
+// columns past D read as zeros and are never stored.
+static int kernel_d(int D) { return D <= 64 ? 64 : 128; }
 
 static size_t delta_bytes(long long BH, int M) {
   return (static_cast<size_t>(BH) * static_cast<size_t>(M) * sizeof(float) + 255) & ~size_t(255);
@@ -224,7 +232,7 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
   FwdArgs a = fwd_args(p, causal, w, o, lse, to);
   static const char* names[3] = {"attn_fwd", "piecewise_fwd", "attn_fwd_jvp"};
   prof_begin(names[mode], s);
-  cudaError_t e = launch_fwd(mode, p.bf16, p.D, maps, a, s);
+  cudaError_t e = launch_fwd(mode, p.bf16, kernel_d(p.D), maps, a, s);
   prof_end(s);
   return cuda_status(e);
 }
@@ -284,11 +292,11 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
   a.dq2 = dq2;
   a.dk2 = dk2;
   prof_begin(pw ? "piecewise_bwd_dkdv" : "attn_bwd_dkdv", s);
-  e = launch_bwd_dkdv(mode, p.bf16, p.D, maps, a, s);
+  e = launch_bwd_dkdv(mode, p.bf16, kernel_d(p.D), maps, a, s);
   prof_end(s);
   if (e != cudaSuccess) return TA_ERR_CUDA;
   prof_begin(pw ? "piecewise_bwd_dq" : "attn_bwd_dq", s);
-  e = launch_bwd_dq(mode, p.bf16, p.D, maps, a, s);
+  e = launch_bwd_dq(mode, p.bf16, kernel_d(p.D), maps, a, s);
   prof_end(s);
   return cuda_status(e);
 }
@@ -386,7 +394,7 @@ ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const vo
   if (st != TA_OK) return st;
   // TMEM holds S, dP, dV, dK1 and dK2 of a 128-key tile only for D <= 64
   // (the fp32 mode has no such limit).
-  if (D != 64 && dt != TA_F32) return TA_ERR_UNSUPPORTED;
+  if (D > 64 && dt != TA_F32) return TA_ERR_UNSUPPORTED;
   if (p.BH == 0 || (M == 0 && N == 0)) return TA_OK;
   if (M == 0) st = check_ptrs({dk1, dk2, dv});
   else if (N == 0) st = check_ptrs({o, dO, dq1, dq2, ws});

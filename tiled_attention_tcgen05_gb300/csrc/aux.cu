@@ -51,7 +51,13 @@ cudaError_t launch_delta(bool bf16, int D, const void* o, const void* dO, float*
   if (blocks > cap) blocks = cap;
   const uint4* a = static_cast<const uint4*>(o);
   const uint4* b = static_cast<const uint4*>(dO);
-  if (D == 64) {
+  if (D == 16) {
+    if (bf16) delta_kernel<__nv_bfloat16, 16><<<blocks, 256, 0, s>>>(a, b, delta, rows);
+    else delta_kernel<__half, 16><<<blocks, 256, 0, s>>>(a, b, delta, rows);
+  } else if (D == 32) {
+    if (bf16) delta_kernel<__nv_bfloat16, 32><<<blocks, 256, 0, s>>>(a, b, delta, rows);
+    else delta_kernel<__half, 32><<<blocks, 256, 0, s>>>(a, b, delta, rows);
+  } else if (D == 64) {
     if (bf16) delta_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, s>>>(a, b, delta, rows);
     else delta_kernel<__half, 64><<<blocks, 256, 0, s>>>(a, b, delta, rows);
   } else if (D == 128) {

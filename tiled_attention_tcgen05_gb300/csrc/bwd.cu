@@ -86,8 +86,9 @@ __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_
   }
 }
 
+// Stores the first 8 * ng (ng <= 4) of 32 fp32 values (x scale) as T.
 template <typename T>
-__device__ __forceinline__ void store_chunk32(T* dst, const uint32_t* v, float scale) {
+__device__ __forceinline__ void store_chunk32(T* dst, const uint32_t* v, float scale, int ng) {
   constexpr bool BF = DT<T>::bf16;
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -97,32 +98,32 @@ __device__ __forceinline__ void store_chunk32(T* dst, const uint32_t* v, float s
     u.y = pack2<BF>(__uint_as_float(v[8 * q + 2]) * scale, __uint_as_float(v[8 * q + 3]) * scale);
     u.z = pack2<BF>(__uint_as_float(v[8 * q + 4]) * scale, __uint_as_float(v[8 * q + 5]) * scale);
     u.w = pack2<BF>(__uint_as_float(v[8 * q + 6]) * scale, __uint_as_float(v[8 * q + 7]) * scale);
-    d4[q] = u;
+    if (q < ng) d4[q] = u;
   }
 }
 
 // Reads columns [c0, c0 + D/2) of a D-column fp32 accumulator row from TMEM
-// and stores them (x scale) into the matching half of one row of T;
-// `touched` false writes zeros.  Warp-collective.
+// and stores those below dg (x scale) into the matching half of one row of T
+// (dg columns in memory); `touched` false writes zeros.  Warp-collective.
 template <typename T, int D>
 __device__ __forceinline__ void epilogue_half(uint32_t taddr, T* row, int c0, bool store, bool touched,
-                                              float scale) {
+                                              float scale, int dg) {
 #pragma unroll
   for (int c = 0; c < D / 64; ++c) {
     uint32_t v[32];
     tmem_ld_x32(taddr + c0 + 32 * c, v);
     tmem_ld_wait(v);
-    if (store) store_chunk32<T>(row + c0 + 32 * c, v, touched ? scale : 0.f);
+    if (store) store_chunk32<T>(row + c0 + 32 * c, v, touched ? scale : 0.f, chunk_groups(dg, c0 + 32 * c));
   }
 }
 
 template <typename T, int D>
-__device__ __forceinline__ void zero_half(T* row, int c0) {
+__device__ __forceinline__ void zero_half(T* row, int c0, int dg) {
   uint32_t z[32];
 #pragma unroll
   for (int e = 0; e < 32; ++e) z[e] = 0;
 #pragma unroll
-  for (int c = 0; c < D / 64; ++c) store_chunk32<T>(row + c0 + 32 * c, z, 0.f);
+  for (int c = 0; c < D / 64; ++c) store_chunk32<T>(row + c0 + 32 * c, z, 0.f, chunk_groups(dg, c0 + 32 * c));
 }
 
 #define TB_CHUNK(arr, c) (*reinterpret_cast<uint32_t(*)[32]>(&(arr)[32 * (c)]))
@@ -427,23 +428,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const bool live = ok && nq > 0;
     const bool st_row = j < args.N;
-    const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * D;
+    const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * args.dg;
     T* dv = reinterpret_cast<T*>(args.dv) + off;
     T* dk = reinterpret_cast<T*>(args.dk) + off;
     const int dc = hc * (D / 2);  // this thread's half of the D columns
     if (live) {
-      epilogue_half<T, D>(lane_addr + C::COL_DV, dv, dc, st_row, true, 1.f);
+      epilogue_half<T, D>(lane_addr + C::COL_DV, dv, dc, st_row, true, 1.f, args.dg);
       if constexpr (!PW) {
-        epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, true, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, true, args.sm_scale, args.dg);
       } else {
         T* dk2 = reinterpret_cast<T*>(args.dk2) + off;
-        epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, touched1, args.sm_scale);
-        epilogue_half<T, D>(lane_addr + C::COL_DK2, dk2, dc, st_row, touched2, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, touched1, args.sm_scale, args.dg);
+        epilogue_half<T, D>(lane_addr + C::COL_DK2, dk2, dc, st_row, touched2, args.sm_scale, args.dg);
       }
     } else if (st_row) {
-      zero_half<T, D>(dv, dc);
-      zero_half<T, D>(dk, dc);
-      if constexpr (PW) zero_half<T, D>(reinterpret_cast<T*>(args.dk2) + off, dc);
+      zero_half<T, D>(dv, dc, args.dg);
+      zero_half<T, D>(dk, dc, args.dg);
+      if constexpr (PW) zero_half<T, D>(reinterpret_cast<T*>(args.dk2) + off, dc, args.dg);
     }
   }
 
@@ -699,19 +700,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (nkv > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
     const bool live = ok && nkv > 0;
-    T* dq = reinterpret_cast<T*>(args.dq) + g * D;
+    T* dq = reinterpret_cast<T*>(args.dq) + g * args.dg;
     const int dc = hc * (D / 2);
     if (live) {
       if constexpr (!PW) {
-        epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, true, args.sm_scale);
+        epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, true, args.sm_scale, args.dg);
       } else {
-        T* dq2 = reinterpret_cast<T*>(args.dq2) + g * D;
-        epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, touched1, args.sm_scale);
-        epilogue_half<T, D>(lane_addr + C::COL_DQ2, dq2, dc, in_m, touched2, args.sm_scale);
+        T* dq2 = reinterpret_cast<T*>(args.dq2) + g * args.dg;
+        epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, touched1, args.sm_scale, args.dg);
+        epilogue_half<T, D>(lane_addr + C::COL_DQ2, dq2, dc, in_m, touched2, args.sm_scale, args.dg);
       }
     } else if (in_m) {
-      zero_half<T, D>(dq, dc);
-      if constexpr (PW) zero_half<T, D>(reinterpret_cast<T*>(args.dq2) + g * D, dc);
+      zero_half<T, D>(dq, dc, args.dg);
+      if constexpr (PW) zero_half<T, D>(reinterpret_cast<T*>(args.dq2) + g * args.dg, dc, args.dg);
     }
   }
 
@@ -968,12 +969,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (nkv > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
-    T* dq = reinterpret_cast<T*>(args.dq) + g * D;
+    T* dq = reinterpret_cast<T*>(args.dq) + g * args.dg;
     const int dc = hc * (D / 2);
     if (ok && nkv > 0) {
-      epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, true, args.sm_scale);
+      epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, true, args.sm_scale, args.dg);
     } else if (in_m) {
-      zero_half<T, D>(dq, dc);
+      zero_half<T, D>(dq, dc, args.dg);
     }
   }
 
@@ -1304,16 +1305,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (nq > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
     const bool st_row = j < args.N;
-    const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * D;
+    const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * args.dg;
     T* dvp = reinterpret_cast<T*>(args.dv) + off;
     T* dkp = reinterpret_cast<T*>(args.dk) + off;
     const int dc = hc * (D / 2);
     if (ok && nq > 0) {
-      epilogue_half<T, D>(lane_addr + C::COL_DV, dvp, dc, st_row, true, 1.f);
-      epilogue_half<T, D>(lane_addr + C::COL_DK, dkp, dc, st_row, true, args.sm_scale);
+      epilogue_half<T, D>(lane_addr + C::COL_DV, dvp, dc, st_row, true, 1.f, args.dg);
+      epilogue_half<T, D>(lane_addr + C::COL_DK, dkp, dc, st_row, true, args.sm_scale, args.dg);
     } else if (st_row) {
-      zero_half<T, D>(dvp, dc);
-      zero_half<T, D>(dkp, dc);
+      zero_half<T, D>(dvp, dc, args.dg);
+      zero_half<T, D>(dkp, dc, args.dg);
     }
   }
 

@@ -32,6 +32,7 @@ struct FwdArgs {
   int w;          // piecewise threshold
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
+  int dg;            // head dimension of the tensors in memory (row stride, columns stored)
   uint32_t* err;
   uint64_t timeout_ns;
 };
@@ -49,9 +50,17 @@ struct BwdArgs {
   int w;
   float scale_log2;
   float sm_scale;
+  int dg;  // head dimension of the tensors in memory (row stride, columns stored)
   uint32_t* err;
   uint64_t timeout_ns;
 };
+
+// Number of 8-column (16-byte) groups of the 32-column chunk starting at
+// column c0 that exist in a row of dg columns (0 to 4).
+__host__ __device__ inline int chunk_groups(int dg, int c0) {
+  const int n = (dg - c0) >> 3;
+  return n < 0 ? 0 : (n > 4 ? 4 : n);
+}
 
 // Number of key tiles that query tile [q0, q0 + kBM) visits.
 __host__ __device__ inline int kv_tiles_for(int q0, int M, int N, int P_SEQ, int causal) {

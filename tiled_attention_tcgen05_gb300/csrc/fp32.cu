@@ -2,9 +2,10 @@
 // with FFMA and accurate expf/logf (no 16-bit rounding of P or dS, no tensor
 // cores).  A correctness path for fp32 callers, not a throughput path.
 //
-// Layout: one warp per row; each lane keeps D/32 of the row's D elements in
-// registers, and the eight warps of a block share key (or query) tiles staged
-// in shared memory.  Dot products are a lane-local FMA chain plus a five-step
+// Layout: one warp per row; each lane keeps DP/32 of the row's elements in
+// registers (DP = D rounded up to a multiple of 32; lanes past D hold zeros),
+// and the eight warps of a block share key (or query) tiles staged in shared
+// memory with rows of DP floats.  Dot products are a lane-local FMA chain plus a five-step
 // butterfly reduction, so every lane ends with the full value.
 //
 // Page sources as for the 16-bit kernels: "Triton fused attention tutorial,
@@ -35,19 +36,35 @@ __device__ __forceinline__ float dot_lane(const float (&a)[E], const float* b_ro
   return warp_sum(s);
 }
 
-template <int E>
+// Row width in shared memory and registers: D rounded up to whole warps.
+template <int D>
+constexpr int padded_d() { return (D + 31) / 32 * 32; }
+
+// Column lane + 32 e exists in a D-column row.
+template <int D>
+__device__ __forceinline__ bool col_ok(int lane, int e) { return D % 32 == 0 || lane + 32 * e < D; }
+
+template <int E, int D>
 __device__ __forceinline__ void load_row(float (&r)[E], const float* row, int lane) {
 #pragma unroll
-  for (int e = 0; e < E; ++e) r[e] = row[lane + 32 * e];
+  for (int e = 0; e < E; ++e) r[e] = col_ok<D>(lane, e) ? row[lane + 32 * e] : 0.f;
 }
 
-// Cooperative copy of `rows` rows (from row0) of a [S, D] slice into smem;
-// rows past S are zero-filled.
+template <int E, int D>
+__device__ __forceinline__ void store_row(float* row, const float (&r)[E], float scale, int lane) {
+#pragma unroll
+  for (int e = 0; e < E; ++e)
+    if (col_ok<D>(lane, e)) row[lane + 32 * e] = r[e] * scale;
+}
+
+// Cooperative copy of kF32Tile rows (from row0) of a [S, D] slice into smem
+// rows of DP floats; rows past S and columns past D are zero-filled.
 template <int D>
 __device__ __forceinline__ void stage(float* dst, const float* src, int row0, int S) {
-  for (int idx = threadIdx.x; idx < kF32Tile * D; idx += blockDim.x) {
-    const int r = idx / D, c = idx % D;
-    dst[idx] = (row0 + r < S) ? src[static_cast<size_t>(row0 + r) * D + c] : 0.f;
+  constexpr int DP = padded_d<D>();
+  for (int idx = threadIdx.x; idx < kF32Tile * DP; idx += blockDim.x) {
+    const int r = idx / DP, c = idx % DP;
+    dst[idx] = (row0 + r < S && c < D) ? src[static_cast<size_t>(row0 + r) * D + c] : 0.f;
   }
 }
 
@@ -59,10 +76,11 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_fwd_kernel(const float* __
                                                                  const float* __restrict__ q2,
                                                                  const float* __restrict__ k2,
                                                                  const float* __restrict__ v2, FwdArgs a) {
-  constexpr int E = D / 32;
+  constexpr int DP = padded_d<D>();
+  constexpr int E = DP / 32;
   constexpr bool PW = MODE == kPiecewise, JVP = MODE == kJvp;
-  __shared__ float sK[kF32Tile * D], sV[kF32Tile * D];
-  __shared__ float sK2[(PW || JVP) ? kF32Tile * D : 1], sV2[JVP ? kF32Tile * D : 1];
+  __shared__ float sK[kF32Tile * DP], sV[kF32Tile * DP];
+  __shared__ float sK2[(PW || JVP) ? kF32Tile * DP : 1], sV2[JVP ? kF32Tile * DP : 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
   const int i = blockIdx.y * kF32Warps + warp;
@@ -70,8 +88,8 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_fwd_kernel(const float* __
   const size_t qoff = (static_cast<size_t>(bh) * a.M + (live ? i : 0)) * D;
   const size_t koff = static_cast<size_t>(bh) * a.N * D;
   float qr[E], q2r[E], acc[E], uacc[E];
-  load_row<E>(qr, q + qoff, lane);
-  if constexpr (PW || JVP) load_row<E>(q2r, q2 + qoff, lane);  // q2 | tq
+  load_row<E, D>(qr, q + qoff, lane);
+  if constexpr (PW || JVP) load_row<E, D>(q2r, q2 + qoff, lane);  // q2 | tq
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = uacc[e] = 0.f;
   float m = -INFINITY, l = 0.f, mu = 0.f;
@@ -93,8 +111,8 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_fwd_kernel(const float* __
     for (int jj = 0; jj < jn; ++jj) {
       const int j = j0 + jj;
       float s;
-      if (PW && (static_cast<long long>(i) + a.P_SEQ - j >= a.w)) s = dot_lane<E>(q2r, sK2 + jj * D, lane);
-      else s = dot_lane<E>(qr, sK + jj * D, lane);
+      if (PW && (static_cast<long long>(i) + a.P_SEQ - j >= a.w)) s = dot_lane<E>(q2r, sK2 + jj * DP, lane);
+      else s = dot_lane<E>(qr, sK + jj * DP, lane);
       s *= a.sm_scale;
       const float m_new = fmaxf(m, s);
       const float alpha = expf(m - m_new);  // m = -inf on the first key: alpha = 0
@@ -102,26 +120,26 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_fwd_kernel(const float* __
       l = l * alpha + p;
       m = m_new;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, sV[jj * D + lane + 32 * e], acc[e] * alpha);
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(p, sV[jj * DP + lane + 32 * e], acc[e] * alpha);
       if constexpr (JVP) {
         // t = sm_scale (tq . k + q . tk)
-        const float t = a.sm_scale * (dot_lane<E>(q2r, sK + jj * D, lane) + dot_lane<E>(qr, sK2 + jj * D, lane));
+        const float t = a.sm_scale * (dot_lane<E>(q2r, sK + jj * DP, lane) + dot_lane<E>(qr, sK2 + jj * DP, lane));
         mu = mu * alpha + p * t;
 #pragma unroll
         for (int e = 0; e < E; ++e)
-          uacc[e] = fmaf(p, fmaf(t, sV[jj * D + lane + 32 * e], sV2[jj * D + lane + 32 * e]), uacc[e] * alpha);
+          uacc[e] = fmaf(p, fmaf(t, sV[jj * DP + lane + 32 * e], sV2[jj * DP + lane + 32 * e]), uacc[e] * alpha);
       }
     }
   }
   if (!live) return;
   float* orow = reinterpret_cast<float*>(a.o) + qoff;
   const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) orow[lane + 32 * e] = acc[e] * inv;
+  store_row<E, D>(orow, acc, inv, lane);
   if constexpr (JVP) {
-    float* trow = reinterpret_cast<float*>(a.to) + qoff;
+    float tv[E];
 #pragma unroll
-    for (int e = 0; e < E; ++e) trow[lane + 32 * e] = uacc[e] * inv - (mu * inv) * (acc[e] * inv);
+    for (int e = 0; e < E; ++e) tv[e] = uacc[e] * inv - (mu * inv) * (acc[e] * inv);
+    store_row<E, D>(reinterpret_cast<float*>(a.to) + qoff, tv, 1.f, lane);
   }
   if (lane == 0) a.lse[static_cast<size_t>(bh) * a.M + i] = l > 0.f ? m + logf(l) : -INFINITY;
 }
@@ -130,13 +148,14 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_fwd_kernel(const float* __
 template <int D>
 __global__ void __launch_bounds__(256) f32_delta_kernel(const float* o, const float* dO, float* delta,
                                                         long long rows) {
-  constexpr int E = D / 32;
+  constexpr int E = padded_d<D>() / 32;
   const int lane = threadIdx.x & 31;
   for (long long r = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)); r < rows;
        r += static_cast<long long>(gridDim.x) * 8) {
     float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < E; ++e) s = fmaf(o[r * D + lane + 32 * e], dO[r * D + lane + 32 * e], s);
+    for (int e = 0; e < E; ++e)
+      if (col_ok<D>(lane, e)) s = fmaf(o[r * D + lane + 32 * e], dO[r * D + lane + 32 * e], s);
     s = warp_sum(s);
     if (lane == 0) delta[r] = s;
   }
@@ -150,9 +169,10 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_dq_kernel(const float* __r
                                                                 const float* __restrict__ dO,
                                                                 const float* __restrict__ q2,
                                                                 const float* __restrict__ k2, BwdArgs a) {
-  constexpr int E = D / 32;
+  constexpr int DP = padded_d<D>();
+  constexpr int E = DP / 32;
   constexpr bool PW = MODE == kPiecewise;
-  __shared__ float sK[kF32Tile * D], sV[kF32Tile * D], sK2[PW ? kF32Tile * D : 1];
+  __shared__ float sK[kF32Tile * DP], sV[kF32Tile * DP], sK2[PW ? kF32Tile * DP : 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
   const int i = blockIdx.y * kF32Warps + warp;
@@ -160,9 +180,9 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_dq_kernel(const float* __r
   const size_t qoff = (static_cast<size_t>(bh) * a.M + (live ? i : 0)) * D;
   const size_t koff = static_cast<size_t>(bh) * a.N * D;
   float qr[E], q2r[E], dor[E], g1[E], g2[E];
-  load_row<E>(qr, q + qoff, lane);
-  if constexpr (PW) load_row<E>(q2r, q2 + qoff, lane);
-  load_row<E>(dor, dO + qoff, lane);
+  load_row<E, D>(qr, q + qoff, lane);
+  if constexpr (PW) load_row<E, D>(q2r, q2 + qoff, lane);
+  load_row<E, D>(dor, dO + qoff, lane);
 #pragma unroll
   for (int e = 0; e < E; ++e) g1[e] = g2[e] = 0.f;
   const float L = live ? a.lse[static_cast<size_t>(bh) * a.M + i] : 0.f;
@@ -184,10 +204,10 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_dq_kernel(const float* __r
     for (int jj = 0; jj < jn; ++jj) {
       const int j = j0 + jj;
       const bool far = PW && (static_cast<long long>(i) + a.P_SEQ - j >= a.w);
-      const float s = far ? dot_lane<E>(q2r, sK2 + jj * D, lane) : dot_lane<E>(qr, sK + jj * D, lane);
+      const float s = far ? dot_lane<E>(q2r, sK2 + jj * DP, lane) : dot_lane<E>(qr, sK + jj * DP, lane);
       const float p = expf(s * a.sm_scale - L);
-      const float ds = p * (dot_lane<E>(dor, sV + jj * D, lane) - dl);
-      const float* kr = far ? sK2 + jj * D : sK + jj * D;
+      const float ds = p * (dot_lane<E>(dor, sV + jj * DP, lane) - dl);
+      const float* kr = far ? sK2 + jj * DP : sK + jj * DP;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         if (far) g2[e] = fmaf(ds, kr[lane + 32 * e], g2[e]);
@@ -196,14 +216,8 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_dq_kernel(const float* __r
     }
   }
   if (!live) return;
-  float* d1 = reinterpret_cast<float*>(a.dq) + qoff;
-#pragma unroll
-  for (int e = 0; e < E; ++e) d1[lane + 32 * e] = g1[e] * a.sm_scale;
-  if constexpr (PW) {
-    float* d2 = reinterpret_cast<float*>(a.dq2) + qoff;
-#pragma unroll
-    for (int e = 0; e < E; ++e) d2[lane + 32 * e] = g2[e] * a.sm_scale;
-  }
+  store_row<E, D>(reinterpret_cast<float*>(a.dq) + qoff, g1, a.sm_scale, lane);
+  if constexpr (PW) store_row<E, D>(reinterpret_cast<float*>(a.dq2) + qoff, g2, a.sm_scale, lane);
 }
 
 // ------------------------------------------------------- dK, dV (key rows)
@@ -214,9 +228,10 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_dkdv_kernel(const float* _
                                                                   const float* __restrict__ dO,
                                                                   const float* __restrict__ q2,
                                                                   const float* __restrict__ k2, BwdArgs a) {
-  constexpr int E = D / 32;
+  constexpr int DP = padded_d<D>();
+  constexpr int E = DP / 32;
   constexpr bool PW = MODE == kPiecewise;
-  __shared__ float sQ[kF32Tile * D], sDO[kF32Tile * D], sQ2[PW ? kF32Tile * D : 1];
+  __shared__ float sQ[kF32Tile * DP], sDO[kF32Tile * DP], sQ2[PW ? kF32Tile * DP : 1];
   __shared__ float sL[kF32Tile], sDl[kF32Tile];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
@@ -225,9 +240,9 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_dkdv_kernel(const float* _
   const size_t koff = (static_cast<size_t>(bh) * a.N + (live ? j : 0)) * D;
   const size_t qoff = static_cast<size_t>(bh) * a.M * D;
   float kr[E], k2r[E], vr[E], gk1[E], gk2[E], gv[E];
-  load_row<E>(kr, k + koff, lane);
-  if constexpr (PW) load_row<E>(k2r, k2 + koff, lane);
-  load_row<E>(vr, v + koff, lane);
+  load_row<E, D>(kr, k + koff, lane);
+  if constexpr (PW) load_row<E, D>(k2r, k2 + koff, lane);
+  load_row<E, D>(vr, v + koff, lane);
 #pragma unroll
   for (int e = 0; e < E; ++e) gk1[e] = gk2[e] = gv[e] = 0.f;
   int lo = 0;  // first query any key of this block is visible from
@@ -250,31 +265,22 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_dkdv_kernel(const float* _
     for (int ii = ib; ii < ie; ++ii) {
       const int i = i0 + ii;
       const bool far = PW && (static_cast<long long>(i) + a.P_SEQ - j >= a.w);
-      const float s = far ? dot_lane<E>(k2r, sQ2 + ii * D, lane) : dot_lane<E>(kr, sQ + ii * D, lane);
+      const float s = far ? dot_lane<E>(k2r, sQ2 + ii * DP, lane) : dot_lane<E>(kr, sQ + ii * DP, lane);
       const float p = expf(s * a.sm_scale - sL[ii]);
-      const float ds = p * (dot_lane<E>(vr, sDO + ii * D, lane) - sDl[ii]);
-      const float* qrow = far ? sQ2 + ii * D : sQ + ii * D;
+      const float ds = p * (dot_lane<E>(vr, sDO + ii * DP, lane) - sDl[ii]);
+      const float* qrow = far ? sQ2 + ii * DP : sQ + ii * DP;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        gv[e] = fmaf(p, sDO[ii * D + lane + 32 * e], gv[e]);
+        gv[e] = fmaf(p, sDO[ii * DP + lane + 32 * e], gv[e]);
         if (far) gk2[e] = fmaf(ds, qrow[lane + 32 * e], gk2[e]);
         else gk1[e] = fmaf(ds, qrow[lane + 32 * e], gk1[e]);
       }
     }
   }
   if (!live) return;
-  float* dv = reinterpret_cast<float*>(a.dv) + koff;
-  float* dk = reinterpret_cast<float*>(a.dk) + koff;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    dv[lane + 32 * e] = gv[e];
-    dk[lane + 32 * e] = gk1[e] * a.sm_scale;
-  }
-  if constexpr (PW) {
-    float* dk2 = reinterpret_cast<float*>(a.dk2) + koff;
-#pragma unroll
-    for (int e = 0; e < E; ++e) dk2[lane + 32 * e] = gk2[e] * a.sm_scale;
-  }
+  store_row<E, D>(reinterpret_cast<float*>(a.dv) + koff, gv, 1.f, lane);
+  store_row<E, D>(reinterpret_cast<float*>(a.dk) + koff, gk1, a.sm_scale, lane);
+  if constexpr (PW) store_row<E, D>(reinterpret_cast<float*>(a.dk2) + koff, gk2, a.sm_scale, lane);
 }
 
 // ---------------------------------------------------------------- host side
@@ -288,10 +294,16 @@ static cudaError_t f32_fwd_t(const F32Ptrs& p, const FwdArgs& a, cudaStream_t s)
 cudaError_t launch_f32_fwd(int mode, int D, const F32Ptrs& p, const FwdArgs& a, cudaStream_t s) {
 #define TA_F32_FWD(MODE_, D_) \
   if (mode == MODE_ && D == D_) return f32_fwd_t<MODE_, D_>(p, a, s);
+  TA_F32_FWD(kStd, 16)
+  TA_F32_FWD(kStd, 32)
   TA_F32_FWD(kStd, 64)
   TA_F32_FWD(kStd, 128)
+  TA_F32_FWD(kPiecewise, 16)
+  TA_F32_FWD(kPiecewise, 32)
   TA_F32_FWD(kPiecewise, 64)
   TA_F32_FWD(kPiecewise, 128)
+  TA_F32_FWD(kJvp, 16)
+  TA_F32_FWD(kJvp, 32)
   TA_F32_FWD(kJvp, 64)
   TA_F32_FWD(kJvp, 128)
 #undef TA_F32_FWD
@@ -303,7 +315,9 @@ cudaError_t launch_f32_delta(int D, const float* o, const float* dO, float* delt
   if (rows <= 0) return cudaSuccess;
   long long blocks = (rows + 7) / 8;
   if (blocks > 65535ll * 8) blocks = 65535ll * 8;
-  if (D == 64) f32_delta_kernel<64><<<blocks, 256, 0, s>>>(o, dO, delta, rows);
+  if (D == 16) f32_delta_kernel<16><<<blocks, 256, 0, s>>>(o, dO, delta, rows);
+  else if (D == 32) f32_delta_kernel<32><<<blocks, 256, 0, s>>>(o, dO, delta, rows);
+  else if (D == 64) f32_delta_kernel<64><<<blocks, 256, 0, s>>>(o, dO, delta, rows);
   else if (D == 128) f32_delta_kernel<128><<<blocks, 256, 0, s>>>(o, dO, delta, rows);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -321,6 +335,10 @@ static cudaError_t f32_bwd_t(const F32Ptrs& p, const BwdArgs& a, cudaStream_t s)
 }
 
 cudaError_t launch_f32_bwd(int mode, int D, const F32Ptrs& p, const BwdArgs& a, cudaStream_t s) {
+  if (mode == kStd && D == 16) return f32_bwd_t<kStd, 16>(p, a, s);
+  if (mode == kStd && D == 32) return f32_bwd_t<kStd, 32>(p, a, s);
+  if (mode == kPiecewise && D == 16) return f32_bwd_t<kPiecewise, 16>(p, a, s);
+  if (mode == kPiecewise && D == 32) return f32_bwd_t<kPiecewise, 32>(p, a, s);
   if (mode == kStd && D == 64) return f32_bwd_t<kStd, 64>(p, a, s);
   if (mode == kStd && D == 128) return f32_bwd_t<kStd, 128>(p, a, s);
   if (mode == kPiecewise && D == 64) return f32_bwd_t<kPiecewise, 64>(p, a, s);

@@ -102,8 +102,9 @@ __device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_
   }
 }
 
+// Stores the first 8 * ng (ng <= 4) of 32 fp32 values (x scale) as T.
 template <typename T>
-__device__ __forceinline__ void store_row_chunk(T* dst, const float* v32, float scale) {
+__device__ __forceinline__ void store_row_chunk(T* dst, const float* v32, float scale, int ng = 4) {
   constexpr bool BF = DT<T>::bf16;
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
@@ -113,7 +114,7 @@ __device__ __forceinline__ void store_row_chunk(T* dst, const float* v32, float 
     u.y = pack2<BF>(v32[8 * q + 2] * scale, v32[8 * q + 3] * scale);
     u.z = pack2<BF>(v32[8 * q + 4] * scale, v32[8 * q + 5] * scale);
     u.w = pack2<BF>(v32[8 * q + 6] * scale, v32[8 * q + 7] * scale);
-    d4[q] = u;
+    if (q < ng) d4[q] = u;
   }
 }
 
@@ -431,9 +432,9 @@ __global__ void __launch_bounds__(192, 1)
     const bool live = ok && nkv > 0;
     const float inv_l = (live && l > 0.f) ? 1.f / l : 0.f;
     if (row < args.M) {
-      T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * D;
+      T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
       T* trow = nullptr;
-      if constexpr (MODE == kJvp) trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * D;
+      if constexpr (MODE == kJvp) trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
       args.lse[static_cast<size_t>(bh) * args.M + row] =
           (live && l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
       (void)trow;
@@ -443,8 +444,8 @@ __global__ void __launch_bounds__(192, 1)
         for (int j = 0; j < 32; ++j) z[j] = 0.f;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          store_row_chunk<T>(orow + 32 * c, z, 0.f);
-          if constexpr (MODE == kJvp) store_row_chunk<T>(trow + 32 * c, z, 0.f);
+          store_row_chunk<T>(orow + 32 * c, z, 0.f, chunk_groups(args.dg, 32 * c));
+          if constexpr (MODE == kJvp) store_row_chunk<T>(trow + 32 * c, z, 0.f, chunk_groups(args.dg, 32 * c));
         }
       }
     }
@@ -459,8 +460,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) of[j] = __uint_as_float(ov[j]) * inv_l;
         if (row < args.M) {
-          T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * D;
-          store_row_chunk<T>(orow + 32 * c, of, 1.f);
+          T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
+          store_row_chunk<T>(orow + 32 * c, of, 1.f, chunk_groups(args.dg, 32 * c));
         }
         if constexpr (MODE == kJvp) {
           uint32_t uv[32];
@@ -471,8 +472,8 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) tv[j] = __uint_as_float(uv[j]) * inv_l - mu_l * of[j];
           if (row < args.M) {
-            T* trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * D;
-            store_row_chunk<T>(trow + 32 * c, tv, 1.f);
+            T* trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
+            store_row_chunk<T>(trow + 32 * c, tv, 1.f, chunk_groups(args.dg, 32 * c));
           }
         }
       }
@@ -735,7 +736,7 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     const bool live = ok && n > 0;
     const float inv_l = (live && l > 0.f) ? 1.f / l : 0.f;
-    T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + (row < args.M ? row : 0)) * D;
+    T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + (row < args.M ? row : 0)) * args.dg;
     if (row < args.M)
       args.lse[static_cast<size_t>(bh) * args.M + row] = (live && l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
 #pragma unroll
@@ -751,7 +752,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) of[j] = 0.f;
       }
-      if (row < args.M) store_row_chunk<T>(orow + 32 * c, of, inv_l);
+      if (row < args.M) store_row_chunk<T>(orow + 32 * c, of, inv_l, chunk_groups(args.dg, 32 * c));
     }
   }
 
