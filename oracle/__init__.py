@@ -40,6 +40,17 @@ Definitions, and the page passages they follow:
   (``_bwd_kv_kernel`` / ``_bwd_q_kernel``): dS is routed to (dq1, dk1) where
   ``d_ij < w`` and to (dq2, dk2) where ``d_ij >= w``; dv = P^T dO.
 
+* Merge of two partial attention states (the "backward_phase_2" page:
+  ``reference_forward`` and the merge backward kernel): for two normalised
+  outputs O1, O2 of the same queries over disjoint key sets, with their
+  log-sum-exps L1, L2: ``m = max(L1, L2)``, ``a = exp(L1 - m)``,
+  ``b = exp(L2 - m)``, ``alpha = a / (a + b)``, ``beta = b / (a + b)``,
+  ``O = alpha O1 + beta O2``, ``L = m + ln(a + b)``.  Backward, with the
+  incoming dO and an optional dL (zero when absent): ``dO1 = alpha dO``,
+  ``dO2 = beta dO``, ``t = sum_d dO (O1 - O2)``, ``dL1 = alpha dL + alpha beta t``,
+  ``dL2 = beta dL - alpha beta t``.  A row whose two parts both saw no key
+  (L1 = L2 = -inf) merges to O = 0, L = -inf with zero gradients.
+
 Every function here is pinned by the ``-m "not gpu"`` oracle tests (finite
 differences, closed forms, invariants, special cases); none is unpinned.
 """
@@ -51,6 +62,7 @@ __all__ = [
     "allowed_mask", "attention_fwd", "attention_bwd", "attention_jvp",
     "piecewise_fwd", "piecewise_bwd", "attention_fwd_bhsd", "attention_bwd_bhsd",
     "attention_jvp_bhsd", "piecewise_fwd_bhsd", "piecewise_bwd_bhsd", "default_scale",
+    "lse_merge_fwd", "lse_merge_bwd", "lse_merge_fwd_bhsd", "lse_merge_bwd_bhsd",
 ]
 
 
@@ -173,6 +185,43 @@ def piecewise_bwd(q1, k1, q2, k2, v, do, causal: bool, sm_scale=None, w: int = 0
     return (s * (dS1 @ k1), s * (dS1.T @ q1), s * (dS2 @ k2), s * (dS2.T @ q2), dv)
 
 
+# ---------------------------------------------------------------- LSE merge
+def _merge_weights(l1, l2):
+    """alpha, beta, m and the mask of rows where both parts are empty."""
+    m = np.maximum(l1, l2)
+    empty = np.isneginf(m)
+    ms = np.where(empty, 0.0, m)
+    a = np.exp(l1 - ms)  # exp(-inf) = 0 for an empty part
+    b = np.exp(l2 - ms)
+    z = np.where(empty, 1.0, a + b)
+    alpha = np.where(empty, 0.0, a / z)
+    beta = np.where(empty, 0.0, b / z)
+    return alpha, beta, ms, z, empty
+
+
+def lse_merge_fwd(o1, l1, o2, l2):
+    """One head: O1, O2 [M, D], L1, L2 [M] -> merged (O, L)."""
+    o1, o2, l1, l2 = _f64(o1, o2, l1, l2)
+    alpha, beta, ms, z, empty = _merge_weights(l1, l2)
+    O = alpha[:, None] * o1 + beta[:, None] * o2
+    L = np.where(empty, -np.inf, ms + np.log(z))
+    return O, L
+
+
+def lse_merge_bwd(o1, l1, o2, l2, do, dl=None):
+    """One head: gradients (dO1, dL1, dO2, dL2) of the merge given dO [M, D]
+    and dL [M] (None = 0)."""
+    o1, o2, l1, l2, do = _f64(o1, o2, l1, l2, do)
+    dl = np.zeros_like(l1) if dl is None else _f64(dl)[0]
+    alpha, beta, _, _, _ = _merge_weights(l1, l2)
+    t = (do * (o1 - o2)).sum(axis=1)
+    do1 = alpha[:, None] * do
+    do2 = beta[:, None] * do
+    dl1 = alpha * dl + alpha * beta * t
+    dl2 = beta * dl - alpha * beta * t
+    return do1, dl1, do2, dl2
+
+
 # ------------------------------------------------------- [B,H,S,D] wrappers
 def _heads(B, H, heads):
     if heads is None:
@@ -220,6 +269,18 @@ def piecewise_fwd_bhsd(q1, k1, q2, k2, v, causal, sm_scale=None, w=0, heads=None
 
 def piecewise_bwd_bhsd(q1, k1, q2, k2, v, do, causal, sm_scale=None, w=0, heads=None):
     return _run_bhsd(piecewise_bwd, (q1, k1, q2, k2, v, do), (causal, sm_scale, w), heads, 5)
+
+
+def lse_merge_fwd_bhsd(o1, l1, o2, l2, heads=None):
+    """[B,H,M,D] / [B,H,M] inputs -> (O, L)."""
+    return _run_bhsd(lse_merge_fwd, (o1, l1, o2, l2), (), heads, 2)
+
+
+def lse_merge_bwd_bhsd(o1, l1, o2, l2, do, dl=None, heads=None):
+    if dl is None:
+        return _run_bhsd(lambda a, b, c, d, e: lse_merge_bwd(a, b, c, d, e, None), (o1, l1, o2, l2, do), (),
+                         heads, 4)
+    return _run_bhsd(lse_merge_bwd, (o1, l1, o2, l2, do, dl), (), heads, 4)
 
 
 # ------------------------------------------------------- sampled query rows

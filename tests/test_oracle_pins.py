@@ -361,3 +361,92 @@ def test_sampled_rows_match_brute_force_and_finite_differences(M, N, causal):
 
     g = _fd_grad(f, q)
     np.testing.assert_allclose(dQ, g[rows], atol=2e-8, rtol=1e-6)
+
+
+# ---------------------------------------------------------------- LSE merge
+def _brute_attention_masked(q, k, v, keep, s):
+    """Attention over an explicit keep mask with loops (rows with no key: O = 0, L = -inf)."""
+    M, N = keep.shape
+    O = np.zeros((M, v.shape[1]))
+    L = np.full(M, -math.inf)
+    for i in range(M):
+        sc = [(j, s * float(q[i] @ k[j])) for j in range(N) if keep[i, j]]
+        if not sc:
+            continue
+        mx = max(x for _, x in sc)
+        den = sum(math.exp(x - mx) for _, x in sc)
+        L[i] = mx + math.log(den)
+        for j, x in sc:
+            O[i] += math.exp(x - L[i]) * v[j]
+    return O, L
+
+
+@pytest.mark.parametrize("M,N,split,causal", [(7, 11, 4, False), (9, 9, 5, True), (6, 10, 0, False),
+                                              (8, 12, 12, True)])
+def test_merge_of_two_key_sets_is_attention_over_their_union(M, N, split, causal):
+    """Attention over keys [0, split) and [split, N) separately, merged, is
+    attention over all N keys -- also when one part is empty for some or all
+    rows (causal: the later keys are invisible to the first queries)."""
+    q, k, v = rand(M, 5), rand(N, 5), rand(N, 3)
+    s = 0.7
+    keep = oracle.allowed_mask(M, N, causal)
+    part1 = keep.copy()
+    part1[:, split:] = False
+    part2 = keep.copy()
+    part2[:, :split] = False
+    O1, L1 = _brute_attention_masked(q, k, v, part1, s)
+    O2, L2 = _brute_attention_masked(q, k, v, part2, s)
+    O, L = oracle.lse_merge_fwd(O1, L1, O2, L2)
+    Of, Lf = oracle.attention_fwd(q, k, v, causal, s)
+    np.testing.assert_allclose(O, Of, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(L), np.isneginf(Lf))
+    np.testing.assert_allclose(L[np.isfinite(Lf)], Lf[np.isfinite(Lf)], atol=1e-12)
+
+
+def test_merge_is_symmetric_and_handles_empty_parts():
+    M, D = 6, 4
+    o1, o2 = rand(M, D), rand(M, D)
+    l1, l2 = rand(M) * 3, rand(M) * 3
+    O, L = oracle.lse_merge_fwd(o1, l1, o2, l2)
+    Os, Ls = oracle.lse_merge_fwd(o2, l2, o1, l1)
+    np.testing.assert_allclose(O, Os, atol=1e-14)
+    np.testing.assert_allclose(L, Ls, atol=1e-14)
+    # closed form: L = ln(e^L1 + e^L2), O = (e^L1 O1 + e^L2 O2) / e^L
+    np.testing.assert_allclose(L, np.log(np.exp(l1) + np.exp(l2)), atol=1e-12)
+    np.testing.assert_allclose(O, (np.exp(l1)[:, None] * o1 + np.exp(l2)[:, None] * o2) / np.exp(L)[:, None],
+                               atol=1e-12)
+    # one empty part passes the other through; two empty parts give O = 0, L = -inf
+    l2e = l2.copy()
+    l2e[:3] = -np.inf
+    l1e = l1.copy()
+    l1e[1] = -np.inf
+    O, L = oracle.lse_merge_fwd(o1, l1e, o2, l2e)
+    np.testing.assert_allclose(O[0], o1[0], atol=1e-15)
+    assert L[0] == l1e[0] and np.isneginf(L[1]) and np.all(O[1] == 0)
+    do1, dl1, do2, dl2 = oracle.lse_merge_bwd(o1, l1e, o2, l2e, rand(M, D), rand(M))
+    assert np.all(do1[1] == 0) and np.all(do2[1] == 0) and dl1[1] == 0 and dl2[1] == 0
+    assert np.all(do2[0] == 0) and dl2[0] == 0
+
+
+@pytest.mark.parametrize("with_dl", [False, True])
+def test_merge_backward_matches_finite_differences(with_dl):
+    M, D = 5, 3
+    o1, o2, l1, l2 = rand(M, D), rand(M, D), rand(M), rand(M)
+    G, g = rand(M, D), (rand(M) if with_dl else np.zeros(M))
+
+    def f(o1_, l1_, o2_, l2_):
+        O, L = oracle.lse_merge_fwd(o1_, l1_, o2_, l2_)
+        return float((G * O).sum() + (g * L).sum())
+
+    do1, dl1, do2, dl2 = oracle.lse_merge_bwd(o1, l1, o2, l2, G, g if with_dl else None)
+    h = 1e-6
+    args = [o1, l1, o2, l2]
+    for idx, grad in zip(range(4), (do1, dl1, do2, dl2)):
+        fd = np.zeros_like(args[idx])
+        for pos in np.ndindex(args[idx].shape):
+            a_p = [a.copy() for a in args]
+            a_m = [a.copy() for a in args]
+            a_p[idx][pos] += h
+            a_m[idx][pos] -= h
+            fd[pos] = (f(*a_p) - f(*a_m)) / (2 * h)
+        np.testing.assert_allclose(grad, fd, atol=1e-8, rtol=1e-7)
