@@ -72,6 +72,7 @@ size_t attn_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt);
 /* Backward of attn_fwd for the loss <dO, O>.
  * [FA-JVP] _attn_bwd_preprocess (delta = rowsum(dO o O)), _attn_bwd_dkdv,
  * _attn_bwd_dq and JVPAttn.backward, with the thread's non-causal fix;
+ * [MERGE] "backward_phase_2" (a two-state online-softmax merge and its backward).
  * [PW] _bwd_preprocess / _bwd_kv_kernel / _bwd_q_kernel.
  * In: q,k,v, o and lse from attn_fwd, dO [B,H,M,D].  Out: dq [B,H,M,D],
  * dk, dv [B,H,N,D] (dt).  ws: >= attn_bwd_workspace_bytes(...) bytes of
@@ -133,6 +134,28 @@ ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const vo
                         void* dk2, void* dv, void* ws, size_t ws_bytes, int B, int H, int M, int N, int D,
                         ta_dtype dt, int causal, float sm_scale, int w, void* stream);
 
+
+/* Merge of two partial attention states of the same queries over disjoint
+ * key sets (split-KV / context-parallel combine), [MERGE] reference_forward:
+ * with m = max(L1, L2), a = exp(L1 - m), b = exp(L2 - m):
+ * O = (a O1 + b O2) / (a + b), L = m + ln(a + b).  A row whose parts both
+ * saw no key (L1 = L2 = -inf) gives O = 0, L = -inf.
+ * In: o1, o2 [B,H,M,D] (dt), lse1, lse2 [B,H,M] fp32.  Out: o (dt), lse.
+ * Outputs may alias o1 / lse1 (each element is read before it is written).
+ * D in {16, 32, 64, 128}; every pointer 16-byte aligned; errors as attn_fwd. */
+ta_status attn_merge_fwd(const void* o1, const float* lse1, const void* o2, const float* lse2, void* o,
+                         float* lse, int B, int H, int M, int D, ta_dtype dt, void* stream);
+
+/* Backward of attn_merge_fwd ([MERGE] merge backward kernel), with
+ * alpha = a / (a + b), beta = b / (a + b), t = sum_d dO (O1 - O2):
+ * dO1 = alpha dO, dO2 = beta dO, dL1 = alpha dL + alpha beta t,
+ * dL2 = beta dL - alpha beta t.  dlse (the gradient of the merged L) may be
+ * NULL, meaning zero.  Rows with L1 = L2 = -inf get zero gradients.
+ * In: o1, o2, dO [B,H,M,D] (dt), lse1, lse2, dlse [B,H,M] fp32.
+ * Out: do1, do2 (dt), dlse1, dlse2 (fp32). */
+ta_status attn_merge_bwd(const void* o1, const float* lse1, const void* o2, const float* lse2, const void* dO,
+                         const float* dlse, void* do1, float* dlse1, void* do2, float* dlse2, int B, int H,
+                         int M, int D, ta_dtype dt, void* stream);
 /* Synchronises `stream`, then reads and clears the device error word that
  * the kernels set when a bounded wait runs out.  TA_OK, TA_ERR_TIMEOUT or
  * TA_ERR_CUDA (an asynchronous CUDA error). */

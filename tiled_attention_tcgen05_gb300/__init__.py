@@ -22,7 +22,7 @@ import os
 
 import torch
 
-__all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_fwd_jvp", "piecewise_fwd", "piecewise_bwd",
+__all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_fwd_jvp", "piecewise_fwd", "piecewise_bwd", "merge_fwd", "merge_bwd",
            "attn_bwd_workspace_bytes", "sync_status", "selftest_wait_timeout", "profile_enable",
            "profile_read", "set_wait_timeout_ms", "TAError", "STATUS"]
 
@@ -43,6 +43,8 @@ _SIGS = {
     "piecewise_fwd": ([_vp] * 7 + [_i] * 7 + [_f, _i, _vp], _i),
     "piecewise_bwd_workspace_bytes": ([_i] * 6, _sz),
     "piecewise_bwd": ([_vp] * 14 + [_sz] + [_i] * 7 + [_f, _i, _vp], _i),
+    "attn_merge_fwd": ([_vp] * 6 + [_i] * 5 + [_vp], _i),
+    "attn_merge_bwd": ([_vp] * 10 + [_i] * 5 + [_vp], _i),
     "ta_sync_status": ([_vp], _i),
     "ta_status_str": ([_i], ctypes.c_char_p),
     "ta_selftest_wait_timeout": ([_i, _vp], _i),
@@ -190,6 +192,41 @@ def piecewise_bwd(q1, k1, q2, k2, v, o, lse, do, w, causal=False, sm_scale=None,
                                               D, dt, int(bool(causal)), _scale(sm_scale), int(w),
                                               _stream(stream)))
     return dq1, dk1, dq2, dk2, dv
+
+
+def _lse_of(name, t, B, H, M, dev):
+    if t.dtype != torch.float32 or tuple(t.shape) != (B, H, M) or not t.is_contiguous() or t.device != dev:
+        raise ValueError(f"{name} must be a contiguous float32 [B, H, M] tensor on {dev}")
+
+
+def merge_fwd(o1, lse1, o2, lse2, o=None, lse=None, stream=None):
+    """Merge of two partial attention states over disjoint key sets:
+    returns (o, lse) with O = (e^L1 O1 + e^L2 O2) / e^L, L = ln(e^L1 + e^L2)."""
+    lib = load()
+    B, H, M, _, D, dt = _prep({"o1": o1, "o2": o2}, ("o1", "o2"), ("o1",))
+    _lse_of("lse1", lse1, B, H, M, o1.device)
+    _lse_of("lse2", lse2, B, H, M, o1.device)
+    o = torch.empty_like(o1) if o is None else o
+    lse = torch.empty_like(lse1) if lse is None else lse
+    _check("attn_merge_fwd", lib.attn_merge_fwd(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _ptr(o), _ptr(lse),
+                                                B, H, M, D, dt, _stream(stream)))
+    return o, lse
+
+
+def merge_bwd(o1, lse1, o2, lse2, do, dlse=None, stream=None):
+    """Backward of merge_fwd: returns (do1, dlse1, do2, dlse2); dlse None = 0."""
+    lib = load()
+    B, H, M, _, D, dt = _prep({"o1": o1, "o2": o2, "do": do}, ("o1", "o2", "do"), ("o1",))
+    _lse_of("lse1", lse1, B, H, M, o1.device)
+    _lse_of("lse2", lse2, B, H, M, o1.device)
+    if dlse is not None:
+        _lse_of("dlse", dlse, B, H, M, o1.device)
+    do1, do2 = torch.empty_like(o1), torch.empty_like(o2)
+    dl1, dl2 = torch.empty_like(lse1), torch.empty_like(lse2)
+    _check("attn_merge_bwd", lib.attn_merge_bwd(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), _ptr(do), _ptr(dlse),
+                                                _ptr(do1), _ptr(dl1), _ptr(do2), _ptr(dl2), B, H, M, D, dt,
+                                                _stream(stream)))
+    return do1, dl1, do2, dl2
 
 
 def sync_status(stream=None) -> str:

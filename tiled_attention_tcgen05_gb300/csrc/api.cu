@@ -358,6 +358,51 @@ ta_status piecewise_fwd(const void* q1, const void* k1, const void* q2, const vo
                  static_cast<cudaStream_t>(stream));
 }
 
+static ta_status check_merge(int B, int H, int M, int D, ta_dtype dt, long long* rows) {
+  if (B < 0 || H < 0 || M < 0) return TA_ERR_INVALID_ARG;
+  if (dt != TA_F16 && dt != TA_BF16 && dt != TA_F32) return TA_ERR_UNSUPPORTED;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return TA_ERR_UNSUPPORTED;
+  *rows = static_cast<long long>(B) * H * M;
+  return TA_OK;
+}
+
+ta_status attn_merge_fwd(const void* o1, const float* lse1, const void* o2, const float* lse2, void* o,
+                         float* lse, int B, int H, int M, int D, ta_dtype dt, void* stream) {
+  long long rows = 0;
+  ta_status st = check_merge(B, H, M, D, dt, &rows);
+  if (st != TA_OK) return st;
+  if (rows == 0) return TA_OK;
+  st = check_ptrs({o1, lse1, o2, lse2, o, lse});
+  if (st != TA_OK) return st;
+  MergePtrs mp{};
+  mp.o1 = o1, mp.o2 = o2, mp.l1 = lse1, mp.l2 = lse2, mp.o = o, mp.lse = lse;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  prof_begin("attn_merge_fwd", s);
+  cudaError_t e = launch_merge(false, static_cast<int>(dt), D, mp, rows, s);
+  prof_end(s);
+  return cuda_status(e);
+}
+
+ta_status attn_merge_bwd(const void* o1, const float* lse1, const void* o2, const float* lse2, const void* dO,
+                         const float* dlse, void* do1, float* dlse1, void* do2, float* dlse2, int B, int H,
+                         int M, int D, ta_dtype dt, void* stream) {
+  long long rows = 0;
+  ta_status st = check_merge(B, H, M, D, dt, &rows);
+  if (st != TA_OK) return st;
+  if (rows == 0) return TA_OK;
+  st = check_ptrs({o1, lse1, o2, lse2, dO, do1, dlse1, do2, dlse2});
+  if (st != TA_OK) return st;
+  if (dlse && !aligned16(dlse)) return TA_ERR_ALIGNMENT;
+  MergePtrs mp{};
+  mp.o1 = o1, mp.o2 = o2, mp.l1 = lse1, mp.l2 = lse2, mp.dO = dO, mp.dl = dlse;
+  mp.do1 = do1, mp.do2 = do2, mp.dl1 = dlse1, mp.dl2 = dlse2;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  prof_begin("attn_merge_bwd", s);
+  cudaError_t e = launch_merge(true, static_cast<int>(dt), D, mp, rows, s);
+  prof_end(s);
+  return cuda_status(e);
+}
+
 size_t attn_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt) {
   (void)N;
   (void)D;

@@ -17,17 +17,22 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint4* __restrict__ o,
   constexpr int RPB = 256 / G;
   const int g = threadIdx.x % G;
   const long long stride = static_cast<long long>(gridDim.x) * RPB;
-  for (long long row = static_cast<long long>(blockIdx.x) * RPB + threadIdx.x / G; row < rows; row += stride) {
-    const uint4 a = __ldg(o + row * G + g);
-    const uint4 b = __ldg(dO + row * G + g);
-    const T* ap = reinterpret_cast<const T*>(&a);
-    const T* bp = reinterpret_cast<const T*>(&b);
+  // Block-uniform loop bound: the butterfly always runs with the whole warp.
+  for (long long rb = static_cast<long long>(blockIdx.x) * RPB; rb < rows; rb += stride) {
+    const long long row = rb + threadIdx.x / G;
+    const bool act = row < rows;
     float acc = 0.f;
+    if (act) {
+      const uint4 a = __ldg(o + row * G + g);
+      const uint4 b = __ldg(dO + row * G + g);
+      const T* ap = reinterpret_cast<const T*>(&a);
+      const T* bp = reinterpret_cast<const T*>(&b);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc = fmaf(static_cast<float>(ap[i]), static_cast<float>(bp[i]), acc);
+      for (int i = 0; i < 8; ++i) acc = fmaf(static_cast<float>(ap[i]), static_cast<float>(bp[i]), acc);
+    }
 #pragma unroll
     for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (g == 0) delta[row] = acc;
+    if (act && g == 0) delta[row] = acc;
   }
 }
 

@@ -42,6 +42,16 @@ cudaError_t launch_f32_delta(int D, const float* o, const float* dO, float* delt
                              cudaStream_t s);
 cudaError_t launch_f32_bwd(int mode, int D, const F32Ptrs& p, const BwdArgs& a, cudaStream_t s);
 
+// Merge of two partial attention states (forward and backward); dtype 0 =
+// fp16, 1 = bf16, 2 = fp32.  dl may be null (zero).
+struct MergePtrs {
+  const void *o1, *o2, *dO;
+  const float *l1, *l2, *dl;
+  void *o, *do1, *do2;
+  float *lse, *dl1, *dl2;
+};
+cudaError_t launch_merge(bool bwd, int dtype, int D, const MergePtrs& p, long long rows, cudaStream_t s);
+
 // Profiling hooks (no-ops unless ta_profile_enable(1)).
 void prof_begin(const char* name, cudaStream_t s);
 void prof_end(cudaStream_t s);
