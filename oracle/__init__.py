@@ -33,7 +33,8 @@ Definitions, and the page passages they follow:
 * Forward-mode JVP (tutorial ``_attn_fwd_inner`` with ``ENABLE_JVP`` and the
   ``_attn_fwd`` JVP epilogue): ``T_ij = sm_scale (tq_i . k_j + q_i . tk_j)``,
   ``mu_i = sum_j P_ij T_ij``, ``tO = (P o T) V - mu o O + P tV``.  This is the
-  derivative of O along (tq, tk, tv): ``dP = P o (T - mu)``.
+  derivative of O along (tq, tk, tv): ``dP = P o (T - mu)``; mu itself is the
+  derivative of L (``attention_jvp_tl``).
 * Piecewise attention ("FlagAttention piecewise.py", ``_fwd_kernel``
   ``piecewise_mask``): with the signed distance ``d_ij = i + N - M - j``, the
   score uses (q2, k2) when ``d_ij >= w`` and (q1, k1) otherwise.  Backward
@@ -63,6 +64,7 @@ __all__ = [
     "piecewise_fwd", "piecewise_bwd", "attention_fwd_bhsd", "attention_bwd_bhsd",
     "attention_jvp_bhsd", "piecewise_fwd_bhsd", "piecewise_bwd_bhsd", "default_scale",
     "lse_merge_fwd", "lse_merge_bwd", "lse_merge_fwd_bhsd", "lse_merge_bwd_bhsd",
+    "attention_jvp_tl", "attention_jvp_tl_bhsd",
 ]
 
 
@@ -144,6 +146,20 @@ def attention_jvp(q, k, v, tq, tk, tv, causal: bool, sm_scale=None):
     mu = PT.sum(axis=1)
     tO = PT @ v - mu[:, None] * O + P @ tv
     return O, L, tO
+
+
+def attention_jvp_tl(q, k, tq, tk, causal: bool, sm_scale=None):
+    """One head: tL, the derivative of L along (tq, tk).  L is the log-sum-exp
+    of the scaled scores, so tL_i = sum_j P_ij T_ij = mu_i, the quantity the
+    JVP epilogue divides by l (mu / l in the "Triton fused attention tutorial,
+    updated with JVP support" _attn_fwd JVP epilogue); 0 for rows that see no
+    key (L is the constant -inf there)."""
+    q, k, tq, tk = _f64(q, k, tq, tk)
+    s = default_scale(q.shape[1], sm_scale)
+    keep = allowed_mask(q.shape[0], k.shape[0], causal)
+    P, _ = _softmax(s * (q @ k.T), keep)
+    T = np.where(keep, s * (tq @ k.T + q @ tk.T), 0.0)
+    return (P * T).sum(axis=1)
 
 
 # ---------------------------------------------------------------- piecewise
@@ -269,6 +285,11 @@ def piecewise_fwd_bhsd(q1, k1, q2, k2, v, causal, sm_scale=None, w=0, heads=None
 
 def piecewise_bwd_bhsd(q1, k1, q2, k2, v, do, causal, sm_scale=None, w=0, heads=None):
     return _run_bhsd(piecewise_bwd, (q1, k1, q2, k2, v, do), (causal, sm_scale, w), heads, 5)
+
+
+def attention_jvp_tl_bhsd(q, k, tq, tk, causal, sm_scale=None, heads=None):
+    """[B,H,S,D] inputs -> tL [B,H,M]."""
+    return _run_bhsd(lambda *a: (attention_jvp_tl(*a),), (q, k, tq, tk), (causal, sm_scale), heads, 1)[0]
 
 
 def lse_merge_fwd_bhsd(o1, l1, o2, l2, heads=None):

@@ -450,3 +450,22 @@ def test_merge_backward_matches_finite_differences(with_dl):
             a_m[idx][pos] -= h
             fd[pos] = (f(*a_p) - f(*a_m)) / (2 * h)
         np.testing.assert_allclose(grad, fd, atol=1e-8, rtol=1e-7)
+
+
+@pytest.mark.parametrize("M,N,causal", [(6, 6, True), (5, 9, False), (9, 5, True)])
+def test_jvp_tangent_of_lse_matches_finite_differences(M, N, causal):
+    """tL = mu is the derivative of L along (tq, tk) (central differences);
+    rows that see no key have L = -inf and tL = 0."""
+    q, k, tq, tk = rand(M, 4), rand(N, 4), rand(M, 4), rand(N, 4)
+    s = 0.6
+    tl = oracle.attention_jvp_tl(q, k, tq, tk, causal, s)
+    h = 1e-6
+    _, Lp = oracle.attention_fwd(q + h * tq, k + h * tk, rand(N, 2), causal, s)
+    _, Lm = oracle.attention_fwd(q - h * tq, k - h * tk, rand(N, 2), causal, s)
+    fin = np.isfinite(Lp)
+    fd = (Lp[fin] - Lm[fin]) / (2 * h)
+    np.testing.assert_allclose(tl[fin], fd, atol=1e-7)
+    assert np.all(tl[~fin] == 0)
+    # and it is the mu of the JVP: tO = (P o T) V - mu O + P tV with tv = 0, v = 1 gives tO = sum(P o T) - mu = 0
+    _, _, tO = oracle.attention_jvp(q, k, np.ones((N, 1)), tq, tk, np.zeros((N, 1)), causal, s)
+    np.testing.assert_allclose(tO[fin], 0.0, atol=1e-12)
