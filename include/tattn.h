@@ -106,10 +106,13 @@ ta_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const vo
  * [FA-JVP] _attn_fwd_inner ENABLE_JVP branch and the _attn_fwd JVP epilogue:
  * with T = sm_scale (tq K^T + Q tk^T) (zero where masked), mu_i = sum_j P_ij T_ij,
  * tO = (P o T) V - mu o O + P tV.
- * In: q,tq [B,H,M,D], k,v,tk,tv [B,H,N,D].  Out: o, to [B,H,M,D] (dt), lse. */
+ * tlse, when not NULL, receives the tangent of L: tL_i = mu_i (the mu the
+ * epilogue divides by l), 0 for rows that see no key.
+ * In: q,tq [B,H,M,D], k,v,tk,tv [B,H,N,D].  Out: o, to [B,H,M,D] (dt), lse,
+ * tlse [B,H,M] fp32. */
 ta_status attn_fwd_jvp(const void* q, const void* k, const void* v, const void* tq, const void* tk,
-                       const void* tv, void* o, float* lse, void* to, int B, int H, int M, int N, int D,
-                       ta_dtype dt, int causal, float sm_scale, void* stream);
+                       const void* tv, void* o, float* lse, void* to, float* tlse, int B, int H, int M, int N,
+                       int D, ta_dtype dt, int causal, float sm_scale, void* stream);
 
 /* Piecewise attention forward ([PW] attention(), _fwd_kernel): the score of
  * (i, j) is sm_scale * q2_i . k2_j when the signed distance i + N - M - j >= w,

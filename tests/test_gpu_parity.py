@@ -72,12 +72,14 @@ def test_jvp_small(gpu_lib, B, H, M, N, D, dtype, causal):
     ta = gpu_lib
     names = ("q", "k", "v", "tq", "tk", "tv")
     cpu, g = inputs(B, H, M, N, D, dtype, 13, names)
-    o, lse, to = ta.attn_fwd_jvp(*(g[n] for n in names), causal=causal)
+    o, lse, to, tlse = ta.attn_fwd_jvp(*(g[n] for n in names), causal=causal, with_tlse=True)
     assert ta.sync_status() == "TA_OK"
     O, L, tO = oracle.attention_jvp_bhsd(*(cpu[n] for n in names), causal)
+    tL = oracle.attention_jvp_tl_bhsd(cpu["q"], cpu["k"], cpu["tq"], cpu["tk"], causal)
     compare("O", o, O, o_tol(dtype))
     compare("L", lse, L, TOL["L"])
     compare("tO", to, tO, TOL["tO"])
+    compare("tL", tlse, tL, TOL["tO"])
 
 
 PW_CASES = [
@@ -243,13 +245,15 @@ def test_fp32_mode_fwd_bwd_jvp(gpu_lib, B, H, M, N, D, causal):
     g = {n: t.cuda() for n, t in cpu.items()}
     o, lse = ta.attn_fwd(g["q"], g["k"], g["v"], causal)
     dq, dk, dv = ta.attn_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal)
-    o2, lse2, to = ta.attn_fwd_jvp(g["q"], g["k"], g["v"], g["tq"], g["tk"], g["tv"], causal=causal)
+    o2, lse2, to, tlse = ta.attn_fwd_jvp(g["q"], g["k"], g["v"], g["tq"], g["tk"], g["tv"], causal=causal,
+                                         with_tlse=True)
     assert ta.sync_status() == "TA_OK"
     O, L = oracle.attention_fwd_bhsd(cpu["q"], cpu["k"], cpu["v"], causal)
     dQ, dK, dV = oracle.attention_bwd_bhsd(cpu["q"], cpu["k"], cpu["v"], cpu["do"], causal)
     _, _, tO = oracle.attention_jvp_bhsd(cpu["q"], cpu["k"], cpu["v"], cpu["tq"], cpu["tk"], cpu["tv"], causal)
+    tL = oracle.attention_jvp_tl_bhsd(cpu["q"], cpu["k"], cpu["tq"], cpu["tk"], causal)
     for name, got, ref in (("O", o, O), ("L", lse, L), ("dQ", dq, dQ), ("dK", dk, dK), ("dV", dv, dV),
-                           ("O(jvp)", o2, O), ("tO", to, tO)):
+                           ("O(jvp)", o2, O), ("tO", to, tO), ("tL", tlse, tL)):
         compare(name, got, ref, F32_TOL)
 
 

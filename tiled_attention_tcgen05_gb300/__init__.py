@@ -8,7 +8,7 @@ library is missing or fails to load, every call raises.
 Entry points (same names as the C ABI):
   attn_fwd(q, k, v, causal, sm_scale)                -> (o, lse)
   attn_bwd(q, k, v, o, lse, do, causal, sm_scale)    -> (dq, dk, dv)
-  attn_fwd_jvp(q, k, v, tq, tk, tv, causal, sm_scale) -> (o, lse, to)
+  attn_fwd_jvp(q, k, v, tq, tk, tv, causal, sm_scale, with_tlse) -> (o, lse, to[, tlse])
   piecewise_fwd(q1, k1, q2, k2, v, w, causal, sm_scale) -> (o, lse)
   piecewise_bwd(q1, k1, q2, k2, v, o, lse, do, w, causal, sm_scale)
                                                      -> (dq1, dk1, dq2, dk2, dv)
@@ -39,7 +39,7 @@ _SIGS = {
     "attn_fwd": ([_vp] * 5 + [_i] * 7 + [_f, _vp], _i),
     "attn_bwd_workspace_bytes": ([_i] * 6, _sz),
     "attn_bwd": ([_vp] * 10 + [_sz] + [_i] * 7 + [_f, _vp], _i),
-    "attn_fwd_jvp": ([_vp] * 9 + [_i] * 7 + [_f, _vp], _i),
+    "attn_fwd_jvp": ([_vp] * 10 + [_i] * 7 + [_f, _vp], _i),
     "piecewise_fwd": ([_vp] * 7 + [_i] * 7 + [_f, _i, _vp], _i),
     "piecewise_bwd_workspace_bytes": ([_i] * 6, _sz),
     "piecewise_bwd": ([_vp] * 14 + [_sz] + [_i] * 7 + [_f, _i, _vp], _i),
@@ -153,17 +153,20 @@ def attn_bwd(q, k, v, o, lse, do, causal=False, sm_scale=None, dq=None, dk=None,
     return dq, dk, dv
 
 
-def attn_fwd_jvp(q, k, v, tq, tk, tv, causal=False, sm_scale=None, stream=None):
+def attn_fwd_jvp(q, k, v, tq, tk, tv, causal=False, sm_scale=None, with_tlse=False, stream=None):
+    """Returns (o, lse, to), or (o, lse, to, tlse) with with_tlse=True (tlse =
+    the tangent of lse along (tq, tk))."""
     lib = load()
     B, H, M, N, D, dt = _prep({"q": q, "k": k, "v": v, "tq": tq, "tk": tk, "tv": tv}, ("q", "tq"),
                               ("k", "v", "tk", "tv"))
     o = torch.empty_like(q)
     to = torch.empty_like(q)
     lse = torch.empty((B, H, M), device=q.device, dtype=torch.float32)
+    tlse = torch.empty_like(lse) if with_tlse else None
     _check("attn_fwd_jvp", lib.attn_fwd_jvp(_ptr(q), _ptr(k), _ptr(v), _ptr(tq), _ptr(tk), _ptr(tv), _ptr(o),
-                                            _ptr(lse), _ptr(to), B, H, M, N, D, dt, int(bool(causal)),
-                                            _scale(sm_scale), _stream(stream)))
-    return o, lse, to
+                                            _ptr(lse), _ptr(to), _ptr(tlse), B, H, M, N, D, dt,
+                                            int(bool(causal)), _scale(sm_scale), _stream(stream)))
+    return (o, lse, to, tlse) if with_tlse else (o, lse, to)
 
 
 def piecewise_fwd(q1, k1, q2, k2, v, w, causal=False, sm_scale=None, stream=None):

@@ -154,11 +154,12 @@ static ta_status check_ptrs(std::initializer_list<const void*> ps) {
 
 static ta_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TA_OK : TA_ERR_CUDA; }
 
-static FwdArgs fwd_args(const Problem& p, int causal, int w, void* o, float* lse, void* to) {
+static FwdArgs fwd_args(const Problem& p, int causal, int w, void* o, float* lse, void* to, float* tlse) {
   FwdArgs a;
   a.o = o;
   a.lse = lse;
   a.to = to;
+  a.tlse = tlse;
   a.BH = static_cast<int>(p.BH);
   a.M = p.M;
   a.N = p.N;
@@ -203,11 +204,12 @@ static size_t delta_bytes(long long BH, int M) {
 
 static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* k, const void* v,
                          const void* q2, const void* k2, const void* v2, void* o, float* lse, void* to,
-                         int causal, int w, cudaStream_t s) {
+                         float* tlse, int causal, int w, cudaStream_t s) {
   if (p.BH == 0 || p.M == 0) return TA_OK;
   if (p.N == 0) {
     prof_begin("empty_rows", s);
     cudaError_t e = launch_empty_rows(p.esize, p.D, o, lse, to, p.BH * p.M, s);
+    if (e == cudaSuccess && tlse) e = launch_zero(tlse, static_cast<size_t>(p.BH) * p.M * sizeof(float), s);
     prof_end(s);
     return cuda_status(e);
   }
@@ -216,7 +218,7 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
     F32Ptrs fp{static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
                static_cast<const float*>(q2), static_cast<const float*>(k2), static_cast<const float*>(v2),
                nullptr};
-    FwdArgs a = fwd_args(p, causal, w, o, lse, to);
+    FwdArgs a = fwd_args(p, causal, w, o, lse, to, tlse);
     prof_begin(f32_names[mode], s);
     cudaError_t e = launch_f32_fwd(mode, p.D, fp, a, s);
     prof_end(s);
@@ -229,7 +231,7 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
             make_map(&maps.k2, k2 ? k2 : k, p.BH, p.N, p.D, p.bf16) &&
             make_map(&maps.v2, v2 ? v2 : v, p.BH, p.N, p.D, p.bf16);
   if (!ok) return TA_ERR_CUDA;
-  FwdArgs a = fwd_args(p, causal, w, o, lse, to);
+  FwdArgs a = fwd_args(p, causal, w, o, lse, to, tlse);
   static const char* names[3] = {"attn_fwd", "piecewise_fwd", "attn_fwd_jvp"};
   prof_begin(names[mode], s);
   cudaError_t e = launch_fwd(mode, p.bf16, kernel_d(p.D), maps, a, s);
@@ -329,20 +331,21 @@ ta_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* 
   if (p.BH * M == 0) return TA_OK;
   st = (N > 0) ? check_ptrs({q, k, v, o, lse}) : check_ptrs({o, lse});
   if (st != TA_OK) return st;
-  return run_fwd(kStd, p, q, k, v, nullptr, nullptr, nullptr, o, lse, nullptr, causal, 0,
+  return run_fwd(kStd, p, q, k, v, nullptr, nullptr, nullptr, o, lse, nullptr, nullptr, causal, 0,
                  static_cast<cudaStream_t>(stream));
 }
 
 ta_status attn_fwd_jvp(const void* q, const void* k, const void* v, const void* tq, const void* tk,
-                       const void* tv, void* o, float* lse, void* to, int B, int H, int M, int N, int D,
-                       ta_dtype dt, int causal, float sm_scale, void* stream) {
+                       const void* tv, void* o, float* lse, void* to, float* tlse, int B, int H, int M, int N,
+                       int D, ta_dtype dt, int causal, float sm_scale, void* stream) {
   Problem p;
   ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
   if (st != TA_OK) return st;
   if (p.BH * M == 0) return TA_OK;
   st = (N > 0) ? check_ptrs({q, k, v, tq, tk, tv, o, lse, to}) : check_ptrs({o, lse, to});
   if (st != TA_OK) return st;
-  return run_fwd(kJvp, p, q, k, v, tq, tk, tv, o, lse, to, causal, 0, static_cast<cudaStream_t>(stream));
+  if (tlse && !aligned16(tlse)) return TA_ERR_ALIGNMENT;
+  return run_fwd(kJvp, p, q, k, v, tq, tk, tv, o, lse, to, tlse, causal, 0, static_cast<cudaStream_t>(stream));
 }
 
 ta_status piecewise_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, void* o,
@@ -354,7 +357,7 @@ ta_status piecewise_fwd(const void* q1, const void* k1, const void* q2, const vo
   if (p.BH * M == 0) return TA_OK;
   st = (N > 0) ? check_ptrs({q1, k1, q2, k2, v, o, lse}) : check_ptrs({o, lse});
   if (st != TA_OK) return st;
-  return run_fwd(kPiecewise, p, q1, k1, v, q2, k2, nullptr, o, lse, nullptr, causal, w,
+  return run_fwd(kPiecewise, p, q1, k1, v, q2, k2, nullptr, o, lse, nullptr, nullptr, causal, w,
                  static_cast<cudaStream_t>(stream));
 }
 

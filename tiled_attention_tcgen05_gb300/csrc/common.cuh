@@ -26,6 +26,7 @@ struct FwdArgs {
   void* o;
   float* lse;
   void* to;       // JVP tangent output (kJvp only)
+  float* tlse;    // JVP tangent of L (kJvp only; may be null)
   int BH, M, N, P_SEQ;
   int num_q_tiles;
   int causal;

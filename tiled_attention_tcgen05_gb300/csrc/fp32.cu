@@ -142,6 +142,9 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_fwd_kernel(const float* __
     store_row<E, D>(reinterpret_cast<float*>(a.to) + qoff, tv, 1.f, lane);
   }
   if (lane == 0) a.lse[static_cast<size_t>(bh) * a.M + i] = l > 0.f ? m + logf(l) : -INFINITY;
+  if constexpr (JVP) {  // tL = sum_j P_ij T_ij
+    if (lane == 0 && a.tlse) a.tlse[static_cast<size_t>(bh) * a.M + i] = l > 0.f ? mu * inv : 0.f;
+  }
 }
 
 // ------------------------------------------------------------ delta (fp32)

@@ -437,6 +437,9 @@ __global__ void __launch_bounds__(192, 1)
       if constexpr (MODE == kJvp) trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
       args.lse[static_cast<size_t>(bh) * args.M + row] =
           (live && l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+      if constexpr (MODE == kJvp) {  // tL = sum_j P_ij T_ij = mu / l
+        if (args.tlse) args.tlse[static_cast<size_t>(bh) * args.M + row] = (live && l > 0.f) ? mu * inv_l : 0.f;
+      }
       (void)trow;
       if (!live) {
         float z[32];
