@@ -238,6 +238,35 @@ def run_reference(args, rank, world):
     return 0
 
 
+def merge_measure(ta, torch, dev, stream, o1, l1, o2, do, hbm_peak, iters=20):
+    """Times the two-state merge forward and backward (HBM-bound) on states of
+    the benchmark's shape, outside the step's timed region; algorithmic bytes
+    are every operand read and written once."""
+    l2 = l1.flip(-1).contiguous()
+    dl = l1.clone()
+    rows, D, e = o1.numel() // o1.shape[-1], o1.shape[-1], o1.element_size()
+    fwd_bytes = 3 * rows * D * e + 3 * rows * 4
+    bwd_bytes = 5 * rows * D * e + 5 * rows * 4
+    out = {}
+    for name, fn, nbytes in (("fwd", lambda: ta.merge_fwd(o1, l1, o2, l2, stream=stream), fwd_bytes),
+                             ("bwd", lambda: ta.merge_bwd(o1, l1, o2, l2, do, dl, stream=stream), bwd_bytes)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / iters
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "bytes": nbytes, "achieved": gbs, "frac": gbs / hbm_peak}
+    out.update({"bound": "hbm", "unit": "GB/s", "peak": hbm_peak,
+                "workload": "merge of two [B,H,M,D] states, B1 H32 M8192 D128 bf16 (inputs larger than L2)"})
+    return out
+
+
 # -------------------------------------------------------------- GPU arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -357,6 +386,10 @@ def run_ours(args, rank, world, local_rank):
             k["unit"] = "TFLOP/s" if b == "tensor" else "GB/s"
             k["frac_of_" + src] = k["achieved"] / (bf16_peak if b == "tensor" else hbm_peak)
 
+    merge = merge_measure(ta, torch, dev, stream, o, lse, dq, g["do"], hbm_peak)
+    if ta.sync_status(stream) != "TA_OK":
+        raise RuntimeError("device error word set in the merge measurement")
+
     cpu_heads = 6
     cpu_secs, cpu_f = cpu_oracle_sample(cpu_heads, os.cpu_count() or 1)
     launches = sum(k["launches"] for k in kernels.values())
@@ -384,6 +417,7 @@ def run_ours(args, rank, world, local_rank):
                      "frac": achieved / peak, "peak_source": src + (" (burst)" if bound == "tensor" else ""),
                      "traffic": ncu_traffic(dom), "algorithmic_per_launch": algo},
         "kernels": kernels,
+        "merge": merge,
         "cpu_baseline": {"value": cpu_f / cpu_secs / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),
                          "kind": "oracle",
                          "sample": "%d of 32 heads (b=0, h<%d), fwd+bwd, fp64 numpy, %.1f s"
