@@ -138,6 +138,16 @@ ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const vo
                         ta_dtype dt, int causal, float sm_scale, int w, void* stream);
 
 
+/* FP8 forward ([FA-JVP] _attn_fwd with FP8_OUTPUT and the tutorial's fp8
+ * benchmark path): q [B,H,M,D] and k [B,H,N,D] in float8 e5m2, V passed
+ * TRANSPOSED as vt [B,H,D,N] e5m2 (the layout the tutorial builds for fp8),
+ * P rounded to e5m2 for the P V product, fp32 accumulation; out: o [B,H,M,D]
+ * in e5m2 and lse [B,H,M] fp32 (natural log, as attn_fwd).  Same masking,
+ * empty-row and sm_scale rules as attn_fwd.  D in {64, 128}; N a multiple of
+ * 16 (rows of vt start 16-byte aligned), else TA_ERR_UNSUPPORTED. */
+ta_status attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int H, int M,
+                       int N, int D, int causal, float sm_scale, void* stream);
+
 /* Merge of two partial attention states of the same queries over disjoint
  * key sets (split-KV / context-parallel combine), [MERGE] reference_forward:
  * with m = max(L1, L2), a = exp(L1 - m), b = exp(L2 - m):

@@ -34,6 +34,7 @@ DTYPES = {
     "bf16": torch.bfloat16,
     "f32": torch.float32,
     "f64": torch.float64,
+    "e5m2": torch.float8_e5m2,
 }
 
 
@@ -76,7 +77,7 @@ def randn(shape, dtype: str, seed: int) -> torch.Tensor:
     """CPU tensor of the given shape, N(0,1) entries rounded to `dtype`."""
     n = int(np.prod(shape)) if len(shape) else 1
     x = torch.from_numpy(normal_f64(seed, n)).reshape(tuple(shape))
-    if dtype in ("f16", "bf16"):
+    if dtype in ("f16", "bf16", "e5m2"):  # through fp32, round to nearest even
         return x.to(torch.float32).to(DTYPES[dtype]).contiguous()
     return x.to(DTYPES[dtype]).contiguous()
 

@@ -22,7 +22,7 @@ import os
 
 import torch
 
-__all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_fwd_jvp", "piecewise_fwd", "piecewise_bwd", "merge_fwd", "merge_bwd",
+__all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_fwd_jvp", "piecewise_fwd", "piecewise_bwd", "merge_fwd", "merge_bwd", "attn_fwd_fp8",
            "attn_bwd_workspace_bytes", "sync_status", "selftest_wait_timeout", "profile_enable",
            "profile_read", "set_wait_timeout_ms", "TAError", "STATUS"]
 
@@ -44,6 +44,7 @@ _SIGS = {
     "piecewise_bwd_workspace_bytes": ([_i] * 6, _sz),
     "piecewise_bwd": ([_vp] * 14 + [_sz] + [_i] * 7 + [_f, _i, _vp], _i),
     "attn_merge_fwd": ([_vp] * 6 + [_i] * 5 + [_vp], _i),
+    "attn_fwd_fp8": ([_vp] * 5 + [_i] * 6 + [_f, _vp], _i),
     "attn_merge_bwd": ([_vp] * 10 + [_i] * 5 + [_vp], _i),
     "ta_sync_status": ([_vp], _i),
     "ta_status_str": ([_i], ctypes.c_char_p),
@@ -195,6 +196,25 @@ def piecewise_bwd(q1, k1, q2, k2, v, o, lse, do, w, causal=False, sm_scale=None,
                                               D, dt, int(bool(causal)), _scale(sm_scale), int(w),
                                               _stream(stream)))
     return dq1, dk1, dq2, dk2, dv
+
+
+def attn_fwd_fp8(q, k, vt, causal=False, sm_scale=None, stream=None):
+    """e5m2 forward: q [B,H,M,D], k [B,H,N,D], vt = V transposed [B,H,D,N], all
+    torch.float8_e5m2 CUDA tensors; returns (o [B,H,M,D] e5m2, lse fp32)."""
+    lib = load()
+    f8 = torch.float8_e5m2
+    for name, t in (("q", q), ("k", k), ("vt", vt)):
+        if t.dtype != f8 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D float8_e5m2 CUDA tensor")
+    B, H, M, D = q.shape
+    N = k.shape[2]
+    if tuple(k.shape) != (B, H, N, D) or tuple(vt.shape) != (B, H, D, N):
+        raise ValueError("expected k [B,H,N,D] and vt [B,H,D,N]")
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, M), device=q.device, dtype=torch.float32)
+    _check("attn_fwd_fp8", lib.attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(vt), _ptr(o), _ptr(lse), B, H, M, N, D,
+                                            int(bool(causal)), _scale(sm_scale), _stream(stream)))
+    return o, lse
 
 
 def _lse_of(name, t, B, H, M, dev):

@@ -73,6 +73,23 @@ static bool make_map(CUtensorMap* map, const void* ptr, long long BH, long long 
   return r == CUDA_SUCCESS;
 }
 
+// [BH, rows, cols] 8-bit tensor as a 3-D map with box_cols x box_rows x 1
+// boxes and 128-byte swizzle (cols * 1 byte is the row stride; columns past
+// cols and rows past `rows` read as zeros).
+static bool make_map_u8(CUtensorMap* map, const void* ptr, long long BH, long long rows, long long cols, int box_cols,
+                        int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows * cols)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------- profiling
 struct ProfRec {
   const char* name;
@@ -402,6 +419,35 @@ ta_status attn_merge_bwd(const void* o1, const float* lse1, const void* o2, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   prof_begin("attn_merge_bwd", s);
   cudaError_t e = launch_merge(true, static_cast<int>(dt), D, mp, rows, s);
+  prof_end(s);
+  return cuda_status(e);
+}
+
+ta_status attn_fwd_fp8(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int H, int M,
+                       int N, int D, int causal, float sm_scale, void* stream) {
+  Problem p;
+  ta_status st = check_common(B, H, M, N, D, TA_BF16, sm_scale, &p);  // shapes and scale
+  if (st != TA_OK) return st;
+  if (D != 64 && D != 128) return TA_ERR_UNSUPPORTED;
+  if (N % 16 != 0) return TA_ERR_UNSUPPORTED;  // the rows of V^T must start 16-byte aligned
+  p.esize = 1;
+  if (p.BH * M == 0) return TA_OK;
+  st = (N > 0) ? check_ptrs({q, k, vt, o, lse}) : check_ptrs({o, lse});
+  if (st != TA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (N == 0) {
+    prof_begin("empty_rows", s);
+    cudaError_t e = launch_empty_rows(1, D, o, lse, nullptr, p.BH * M, s);
+    prof_end(s);
+    return cuda_status(e);
+  }
+  FwdMaps maps;
+  bool ok = make_map_u8(&maps.q, q, p.BH, M, D, 128, 128) && make_map_u8(&maps.k, k, p.BH, N, D, 128, 128) &&
+            make_map_u8(&maps.v, vt, p.BH, D, N, 128, D);
+  if (!ok) return TA_ERR_CUDA;
+  FwdArgs a = fwd_args(p, causal, 0, o, lse, nullptr, nullptr);
+  prof_begin("attn_fwd_fp8", s);
+  cudaError_t e = launch_fwd_f8(D, maps, a, s);
   prof_end(s);
   return cuda_status(e);
 }

@@ -19,6 +19,9 @@ struct BwdMaps {
 };
 
 cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s);
+// e5m2 forward: maps.q, maps.k are [BH, S, D] 8-bit maps with 128 x 128 boxes,
+// maps.v the transposed V [BH, D, N] with 128 x D boxes.
+cudaError_t launch_fwd_f8(int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s);
 
 // delta_i = sum_d O_id dO_id for BH*M rows.
 cudaError_t launch_delta(bool bf16, int D, const void* o, const void* dO, float* delta, long long rows,
