@@ -267,6 +267,36 @@ def merge_measure(ta, torch, dev, stream, o1, l1, o2, do, hbm_peak, iters=20):
     return out
 
 
+def fp8_measure(ta, torch, si, dev, stream, w, bf16_peak, iters=10):
+    """Times the e5m2 forward (attn_fwd_fp8) on the benchmark's shape, outside
+    the step's timed region, against the fp8 dense peak taken as the measured
+    bf16 peak x the nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)."""
+    B, H, M, N, D, causal = w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"]
+    q = si.randn((B, H, M, D), "e5m2", si.seed_for(3, 10)).to(dev)
+    k = si.randn((B, H, N, D), "e5m2", si.seed_for(3, 11)).to(dev)
+    vt = si.randn((B, H, D, N), "e5m2", si.seed_for(3, 12)).to(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # larger than L2
+    for _ in range(3):
+        ta.attn_fwd_fp8(q, k, vt, causal, stream=stream)
+    torch.cuda.synchronize(dev)
+    ms = 0.0
+    with torch.cuda.stream(stream):
+        for _ in range(iters):  # the e5m2 inputs (100 MB) fit in L2: flush it before each timed launch
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ta.attn_fwd_fp8(q, k, vt, causal, stream=stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms += e0.elapsed_time(e1) / iters
+    flops = 4.0 * B * H * M * N * D * (0.5 if causal else 1.0)
+    peak = bf16_peak * (4.5 / 2.25)
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"ms": ms, "flops": flops, "achieved": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peak,
+            "peak_source": "measured bf16 burst x 2 (nominal fp8 / bf16)", "frac": tf / peak,
+            "workload": "e5m2 forward, B1 H32 M=N=8192 D128 causal (L2 flushed before each timed launch)"}
+
+
 # -------------------------------------------------------------- GPU arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -387,6 +417,7 @@ def run_ours(args, rank, world, local_rank):
             k["frac_of_" + src] = k["achieved"] / (bf16_peak if b == "tensor" else hbm_peak)
 
     merge = merge_measure(ta, torch, dev, stream, o, lse, dq, g["do"], hbm_peak)
+    fp8 = fp8_measure(ta, torch, si, dev, stream, w, bf16_peak)
     if ta.sync_status(stream) != "TA_OK":
         raise RuntimeError("device error word set in the merge measurement")
 
@@ -418,6 +449,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": ncu_traffic(dom), "algorithmic_per_launch": algo},
         "kernels": kernels,
         "merge": merge,
+        "fp8_fwd": fp8,
         "cpu_baseline": {"value": cpu_f / cpu_secs / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),
                          "kind": "oracle",
                          "sample": "%d of 32 heads (b=0, h<%d), fwd+bwd, fp64 numpy, %.1f s"
