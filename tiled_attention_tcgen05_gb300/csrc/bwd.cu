@@ -62,13 +62,16 @@ __device__ __forceinline__ void load_tile_b(uint8_t* dst, const CUtensorMap* map
 // d = A B^T over D: A, B are 128-row x D K-major swizzled tiles in smem.
 template <int D>
 __device__ __forceinline__ void mma_abT(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
-  const uint64_t da = sdesc_sw128(a_smem, 16, 1024);
-  const uint64_t db = sdesc_sw128(b_smem, 16, 1024);
+  const uint64_t da0 = sdesc_sw128(a_smem, 16, 1024);
+  const uint64_t db0 = sdesc_sw128(b_smem, 16, 1024);
+  uint64_t da[D / 16], db[D / 16];
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
-    mma_ss(d_tmem, da + off, db + off, idesc, kk > 0 ? 1u : 0u);
+    da[kk] = da0 + off;
+    db[kk] = db0 + off;
   }
+  mma_ss_n<D / 16>(d_tmem, da, db, idesc, 0u);
 }
 
 // d (+)= X Y: X is 128 x 128 16-bit in TMEM whose K-steps 0-3 sit at columns
@@ -78,12 +81,14 @@ template <int D>
 __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
                                        bool accumulate) {
   const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
+  uint32_t a[8];
+  uint64_t b[8];
 #pragma unroll
-  for (int kk = 0; kk < 128 / 16; ++kk) {
-    const uint32_t xc = x_tmem + (kk & 3) * 8 + (kk >> 2) * 64;
-    mma_ts(d_tmem, xc, dy + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 8; ++kk) {
+    a[kk] = x_tmem + (kk & 3) * 8 + (kk >> 2) * 64;
+    b[kk] = dy + static_cast<uint64_t>((kk * 16 * 128) >> 4);
   }
+  mma_ts_n<8>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
 // Stores the first 8 * ng (ng <= 4) of 32 fp32 values (x scale) as T.
@@ -267,16 +272,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0 && nq > 0) {
+    if (nq > 0) {
       constexpr uint32_t idesc_s = idesc_f16(kBN, kBM, BF, false, false);  // M = keys, N = queries
       constexpr uint32_t idesc_g = idesc_f16(kBN, D, BF, false, true);     // M = keys, N = D
-      bool ok = mbar_wait(&bar_kv, 0, ctl, kErrTimeoutTma);
+      bool ok = warp_wait(&bar_kv, 0, ctl, kErrTimeoutTma);
       bool acc1 = false, acc2 = false;
       int nstr = 0;
       for (int u = 0; ok && u < nq; ++u) {
         const int st = u % STAGES;
         const int q0 = (i0 + u) * kBM;
-        if (!(ok = mbar_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+        if (!(ok = warp_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
         tc_fence_after();
         int cls = kNearB;
         if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
@@ -288,15 +293,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(st)), idesc_s);
           mma_abT<D>(tmem + C::COL_B, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
         }
-        mma_commit(&bar_s);
+        commit_el(&bar_s);
         if (cls == (kNearB | kFarB)) {
-          if (!(ok = mbar_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
+          if (!(ok = warp_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
           tc_fence_after();
           ++nstr;
         }
         mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(st)), idesc_s);  // dP^T = V dO^T
-        mma_commit(&bar_dp);
-        if (!(ok = mbar_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
+        commit_el(&bar_dp);
+        if (!(ok = warp_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         mma_tY<D>(tmem + C::COL_DV, tmem + C::COL_A, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
         if constexpr (!PW) {
@@ -314,9 +319,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             acc1 = acc2 = true;
           }
         }
-        mma_commit(&bar_qempty[st]);
+        commit_el(&bar_qempty[st]);
       }
-      if (ok) mma_commit(&bar_done);
+      if (ok) commit_el(&bar_done);
     }
   } else {
     // ------------------------------------------- key-row softmax gradient
@@ -561,15 +566,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0 && nkv > 0) {
+    if (nkv > 0) {
       constexpr uint32_t idesc_s = idesc_f16(kBM, kBN, BF, false, false);
       constexpr uint32_t idesc_g = idesc_f16(kBM, D, BF, false, true);
-      bool ok = mbar_wait(&bar_q, 0, ctl, kErrTimeoutTma);
+      bool ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma);
       bool acc1 = false, acc2 = false;
       int nstr = 0;
       for (int t = 0; ok && t < nkv; ++t) {
         const int st = t % STAGES;
-        if (!(ok = mbar_wait(&bar_kv[st], (t / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+        if (!(ok = warp_wait(&bar_kv[st], (t / STAGES) & 1, ctl, kErrTimeoutTma))) break;
         tc_fence_after();
         int cls = kNearB;
         if constexpr (PW) cls = pw_class_b(q0, t * kBN, args.P_SEQ, args.w);
@@ -581,15 +586,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_abT<D>(tmem + C::COL_A, smem_u32(sQ), smem_u32(sK(st)), idesc_s);
           mma_abT<D>(tmem + C::COL_B, smem_u32(sQ2), smem_u32(sK2(st)), idesc_s);
         }
-        mma_commit(&bar_s);
+        commit_el(&bar_s);
         if (cls == (kNearB | kFarB)) {
-          if (!(ok = mbar_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
+          if (!(ok = warp_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
           tc_fence_after();
           ++nstr;
         }
         mma_abT<D>(tmem + C::COL_B, smem_u32(sDO), smem_u32(sV(st)), idesc_s);  // dP = dO V^T
-        mma_commit(&bar_dp);
-        if (!(ok = mbar_wait(&bar_ds, t & 1, ctl, kErrTimeoutSoftmax))) break;
+        commit_el(&bar_dp);
+        if (!(ok = warp_wait(&bar_ds, t & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         if constexpr (!PW) {
           mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, t > 0);  // dQ += dS K
@@ -606,9 +611,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             acc1 = acc2 = true;
           }
         }
-        mma_commit(&bar_kvempty[st]);
+        commit_el(&bar_kvempty[st]);
       }
-      if (ok) mma_commit(&bar_done);
+      if (ok) commit_el(&bar_done);
     }
   } else {
     // --------------------------------------------- query-row softmax gradient
@@ -750,12 +755,15 @@ struct DqStdCfg {
 // per K-step from a_tmem, and B a 128-row x D K-major swizzled tile in smem.
 template <int D>
 __device__ __forceinline__ void mma_tB(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc) {
-  const uint64_t db = sdesc_sw128(b_smem, 16, 1024);
+  const uint64_t db0 = sdesc_sw128(b_smem, 16, 1024);
+  uint32_t a[D / 16];
+  uint64_t b[D / 16];
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
-    mma_ts(d_tmem, a_tmem + kk * 8, db + off, idesc, kk > 0 ? 1u : 0u);
+    a[kk] = a_tmem + kk * 8;
+    b[kk] = db0 + static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
   }
+  mma_ts_n<D / 16>(d_tmem, a, b, idesc, 0u);
 }
 
 // Copies row r of a 128 x D 16-bit K-major 128-byte-swizzled tile from shared
@@ -861,38 +869,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0 && nkv > 0) {
+    if (nkv > 0) {
       constexpr uint32_t idesc_s = idesc_f16(kBM, kBN, BF, false, false);
       constexpr uint32_t idesc_g = idesc_f16(kBM, D, BF, false, true);
-      bool ok = mbar_wait(&bar_qfree, 0, ctl, kErrTimeoutSoftmax) && mbar_wait(&bar_kv[0], 0, ctl, kErrTimeoutTma);
+      bool ok = warp_wait(&bar_qfree, 0, ctl, kErrTimeoutSoftmax) && warp_wait(&bar_kv[0], 0, ctl, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         mma_tB<D>(tmem + C::COL_A, tmem + C::COL_QT, smem_u32(sK(0)), idesc_s);   // S = Q K^T
-        mma_commit(&bar_s);
+        commit_el(&bar_s);
         mma_tB<D>(tmem + C::COL_B, tmem + C::COL_DOT, smem_u32(sV(0)), idesc_s);  // dP = dO V^T
-        mma_commit(&bar_dp);
+        commit_el(&bar_dp);
       }
       for (int t = 0; ok && t < nkv; ++t) {
         const int st = t % STAGES;
         const int st1 = (t + 1) % STAGES;
         const bool next = t + 1 < nkv;
         if (next) {
-          if (!(ok = mbar_wait(&bar_consumed, t & 1, ctl, kErrTimeoutSoftmax))) break;
-          if (!(ok = mbar_wait(&bar_kv[st1], ((t + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+          if (!(ok = warp_wait(&bar_consumed, t & 1, ctl, kErrTimeoutSoftmax))) break;
+          if (!(ok = warp_wait(&bar_kv[st1], ((t + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
           tc_fence_after();
           mma_tB<D>(tmem + C::COL_A, tmem + C::COL_QT, smem_u32(sK(st1)), idesc_s);
-          mma_commit(&bar_s);
+          commit_el(&bar_s);
         }
-        if (!(ok = mbar_wait(&bar_ds, t & 1, ctl, kErrTimeoutSoftmax))) break;
+        if (!(ok = warp_wait(&bar_ds, t & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, t > 0);  // dQ += dS K
-        mma_commit(&bar_kvempty[st]);
+        commit_el(&bar_kvempty[st]);
         if (next) {
           mma_tB<D>(tmem + C::COL_B, tmem + C::COL_DOT, smem_u32(sV(st1)), idesc_s);
-          mma_commit(&bar_dp);
+          commit_el(&bar_dp);
         }
       }
-      if (ok) mma_commit(&bar_done);
+      if (ok) commit_el(&bar_done);
     }
   } else {
     // --------------------------------------------- query-row softmax gradient
@@ -1029,11 +1037,14 @@ template <int D>
 __device__ __forceinline__ void mma_tY_il(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
                                           bool accumulate) {
   const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
+  uint32_t a[8];
+  uint64_t b[8];
 #pragma unroll
-  for (int kk = 0; kk < 128 / 16; ++kk) {
-    mma_ts(d_tmem, x_tmem + (kk >> 1) * 32 + (kk & 1) * 8, dy + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < 8; ++kk) {
+    a[kk] = x_tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+    b[kk] = dy + static_cast<uint64_t>((kk * 16 * 128) >> 4);
   }
+  mma_ts_n<8>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
 template <typename T, int D>
@@ -1139,43 +1150,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ----------------------------------------------------------------- MMA
-    if (lane == 0 && nq > 0) {
+    if (nq > 0) {
       constexpr uint32_t idesc_s = idesc_f16(kBN, kBM, BF, false, false);  // M = keys, N = queries
       constexpr uint32_t idesc_g = idesc_f16(kBN, D, BF, false, true);     // M = keys, N = D
-      bool ok = mbar_wait(&bar_kv, 0, ctl, kErrTimeoutTma) && mbar_wait(&bar_qf[0], 0, ctl, kErrTimeoutTma) &&
-                mbar_wait(&bar_of[0], 0, ctl, kErrTimeoutTma);
+      bool ok = warp_wait(&bar_kv, 0, ctl, kErrTimeoutTma) && warp_wait(&bar_qf[0], 0, ctl, kErrTimeoutTma) &&
+                warp_wait(&bar_of[0], 0, ctl, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(0)), idesc_s);   // S^T = K Q^T
-        mma_commit(&bar_s);
+        commit_el(&bar_s);
         mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(0)), idesc_s);  // dP^T = V dO^T
-        mma_commit(&bar_dp);
+        commit_el(&bar_dp);
       }
       for (int u = 0; ok && u < nq; ++u) {
         const int sq = u % QST, so = u % OST;
         const int sq1 = (u + 1) % QST, so1 = (u + 1) % OST;
         const bool next = u + 1 < nq;
         if (next) {
-          if (!(ok = mbar_wait(&bar_consumed, u & 1, ctl, kErrTimeoutSoftmax))) break;
-          if (!(ok = mbar_wait(&bar_qf[sq1], ((u + 1) / QST) & 1, ctl, kErrTimeoutTma))) break;
+          if (!(ok = warp_wait(&bar_consumed, u & 1, ctl, kErrTimeoutSoftmax))) break;
+          if (!(ok = warp_wait(&bar_qf[sq1], ((u + 1) / QST) & 1, ctl, kErrTimeoutTma))) break;
           tc_fence_after();
           mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(sq1)), idesc_s);
-          mma_commit(&bar_s);
+          commit_el(&bar_s);
         }
-        if (!(ok = mbar_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
+        if (!(ok = warp_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         mma_tY_il<D>(tmem + C::COL_DV, tmem + C::COL_B, smem_u32(sDO(so)), idesc_g, u > 0);      // dV += P^T dO
-        mma_commit(&bar_oe[so]);
+        commit_el(&bar_oe[so]);
         mma_tY_il<D>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, u > 0);  // dK += dS^T Q
-        mma_commit(&bar_qe[sq]);
+        commit_el(&bar_qe[sq]);
         if (next) {
-          if (!(ok = mbar_wait(&bar_of[so1], ((u + 1) / OST) & 1, ctl, kErrTimeoutTma))) break;
+          if (!(ok = warp_wait(&bar_of[so1], ((u + 1) / OST) & 1, ctl, kErrTimeoutTma))) break;
           tc_fence_after();
           mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(so1)), idesc_s);
-          mma_commit(&bar_dp);
+          commit_el(&bar_dp);
         }
       }
-      if (ok) mma_commit(&bar_done);
+      if (ok) commit_el(&bar_done);
     }
   } else {
     // ------------------------------------------- key-row softmax gradient

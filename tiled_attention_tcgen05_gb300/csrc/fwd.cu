@@ -80,13 +80,16 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
 template <int D>
 __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc,
                                        bool accumulate) {
-  const uint64_t da = sdesc_sw128(a_smem, 16, 1024);
-  const uint64_t db = sdesc_sw128(b_smem, 16, 1024);
+  const uint64_t da0 = sdesc_sw128(a_smem, 16, 1024);
+  const uint64_t db0 = sdesc_sw128(b_smem, 16, 1024);
+  uint64_t da[D / 16], db[D / 16];
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
-    mma_ss(d_tmem, da + off, db + off, idesc, (accumulate || kk > 0) ? 1u : 0u);
+    da[kk] = da0 + off;
+    db[kk] = db0 + off;
   }
+  mma_ss_n<D / 16>(d_tmem, da, db, idesc, accumulate ? 1u : 0u);
 }
 
 // d (+)= P V: P is 128 x 128 (16-bit, TMEM), V is 128 keys x D stored with D
@@ -95,11 +98,14 @@ template <int D>
 __device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, uint32_t idesc,
                                        bool accumulate) {
   const uint64_t dv = sdesc_sw128(v_smem, kBM * 128, 1024);
+  uint32_t a[kBN / 16];
+  uint64_t b[kBN / 16];
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
-    mma_ts(d_tmem, p_tmem + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4), idesc,
-           (accumulate || kk > 0) ? 1u : 0u);
+    a[kk] = p_tmem + kk * 8;
+    b[kk] = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
   }
+  mma_ts_n<kBN / 16>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
 // Stores the first 8 * ng (ng <= 4) of 32 fp32 values (x scale) as T.
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 5) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0 && nkv > 0) {
+    if (nkv > 0) {
       constexpr uint32_t idesc_qk = idesc_f16(kBM, kBN, BF, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(kBM, D, BF, false, true);
       const uint32_t aQ = smem_u32(sQ);
@@ -241,8 +247,8 @@ __global__ void __launch_bounds__(192, 1)
       auto issue_pv = [&](int u, uint64_t* done_bar) -> bool {
         const int b = u % NBUF;
         const int st = u % STAGES;
-        if (!mbar_wait(&bar_p[b], (u / NBUF) & 1, ctl, kErrTimeoutSoftmax)) return false;
-        if (!mbar_wait(&bar_v[st], (u / STAGES) & 1, ctl, kErrTimeoutTma)) return false;
+        if (!warp_wait(&bar_p[b], (u / NBUF) & 1, ctl, kErrTimeoutSoftmax)) return false;
+        if (!warp_wait(&bar_v[st], (u / STAGES) & 1, ctl, kErrTimeoutTma)) return false;
         tc_fence_after();
         const uint32_t p_col = (NBUF == 2) ? (b ? C::COL_S1 : C::COL_S0) : C::COL_S0;
         mma_pv<D>(tmem + C::COL_O, tmem + p_col, smem_u32(sVt(st, 0)), idesc_pv, u > 0);
@@ -250,18 +256,18 @@ __global__ void __launch_bounds__(192, 1)
           mma_pv<D>(tmem + C::COL_U, tmem + C::COL_S1, smem_u32(sVt(st, 0)), idesc_pv, u > 0);
           mma_pv<D>(tmem + C::COL_U, tmem + C::COL_S0, smem_u32(sVt(st, 1)), idesc_pv, true);
         }
-        mma_commit(&bar_empty[st]);
-        mma_commit(done_bar);
+        commit_el(&bar_empty[st]);
+        commit_el(done_bar);
         return true;
       };
-      bool ok = mbar_wait(&bar_q, 0, ctl, kErrTimeoutTma);
+      bool ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma);
       for (int t = 0; ok && t < nkv; ++t) {
         const int st = t % STAGES;
         if (NBUF == 1 && t > 0) {
           ok = issue_pv(t - 1, &bar_o);
           if (!ok) break;
         }
-        if (!mbar_wait(&bar_k[st], (t / STAGES) & 1, ctl, kErrTimeoutTma)) {
+        if (!warp_wait(&bar_k[st], (t / STAGES) & 1, ctl, kErrTimeoutTma)) {
           ok = false;
           break;
         }
@@ -280,7 +286,7 @@ __global__ void __launch_bounds__(192, 1)
           mma_qk<D>(tmem + C::COL_S1, aQ2, aK, idesc_qk, false);
           mma_qk<D>(tmem + C::COL_S1, aQ, smem_u32(sKt(st, 1)), idesc_qk, true);
         }
-        mma_commit(&bar_s[b]);
+        commit_el(&bar_s[b]);
         if (NBUF == 2 && t > 0) {
           ok = issue_pv(t - 1, &bar_o);
         }
@@ -608,43 +614,43 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0 && nt > 0) {
+    if (nt > 0) {
       constexpr uint32_t idesc_qk = idesc_f16(kBM, kBN, BF, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(kBM, D, BF, false, true);
       const uint32_t aQ[2] = {smem_u32(sQ), smem_u32(sQ) + C::TILE};
-      bool ok = mbar_wait(&bar_q, 0, ctl, kErrTimeoutTma) && mbar_wait(&bar_k[0], 0, ctl, kErrTimeoutTma);
+      bool ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma) && warp_wait(&bar_k[0], 0, ctl, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         for (int w = 0; w < 2; ++w)
           if (n_t[w] > 0) {
             mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(0)), idesc_qk, false);
-            mma_commit(&bar_s[w]);
+            commit_el(&bar_s[w]);
           }
       }
-      if (ok) mma_commit(&bar_kempty[0]);  // K tile 0 is consumed once both score MMAs finish
+      if (ok) commit_el(&bar_kempty[0]);  // K tile 0 is consumed once both score MMAs finish
       for (int t = 0; ok && t < nt; ++t) {
         const int sv = t % VST;
         const int sk1 = (t + 1) % KST;
-        if (!(ok = mbar_wait(&bar_v[sv], (t / VST) & 1, ctl, kErrTimeoutTma))) break;
+        if (!(ok = warp_wait(&bar_v[sv], (t / VST) & 1, ctl, kErrTimeoutTma))) break;
         const bool next = t + 1 < nt;
-        if (next && !(ok = mbar_wait(&bar_k[sk1], ((t + 1) / KST) & 1, ctl, kErrTimeoutTma))) break;
+        if (next && !(ok = warp_wait(&bar_k[sk1], ((t + 1) / KST) & 1, ctl, kErrTimeoutTma))) break;
         for (int w = 0; w < 2; ++w) {
           if (t < n_t[w]) {
-            if (!(ok = mbar_wait(&bar_p[w], t & 1, ctl, kErrTimeoutSoftmax))) break;
+            if (!(ok = warp_wait(&bar_p[w], t & 1, ctl, kErrTimeoutSoftmax))) break;
             tc_fence_after();
             mma_pv<D>(tmem + col_o[w], tmem + col_s[w], smem_u32(sV(sv)), idesc_pv, t > 0);
-            mma_commit(&bar_o[w]);
+            commit_el(&bar_o[w]);
           }
           if (next && t + 1 < n_t[w]) {
             mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(sk1)), idesc_qk, false);
-            mma_commit(&bar_s[w]);
+            commit_el(&bar_s[w]);
           }
         }
         if (!ok) break;
-        mma_commit(&bar_vempty[sv]);
-        if (next) mma_commit(&bar_kempty[sk1]);
+        commit_el(&bar_vempty[sv]);
+        if (next) commit_el(&bar_kempty[sk1]);
       }
-      if (ok) mma_commit(&bar_ofinal);
+      if (ok) commit_el(&bar_ofinal);
     }
   } else {
     // ------------------------------- softmax / correction / epilogue (tile w)

@@ -29,34 +29,19 @@ struct F8Cfg {
   static_assert(256 + 2 * D <= 512, "TMEM overflow");
 };
 
-__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // S = Q K^T over D (e5m2): 128-row K-major tiles with 128-byte rows; each
 // K-step is 32 elements = 32 bytes further along the swizzle atom.
 template <int D>
 __device__ __forceinline__ void mma_qk_f8(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
-  const uint64_t da = sdesc_sw128(a_smem, 16, 1024);
-  const uint64_t db = sdesc_sw128(b_smem, 16, 1024);
+  const uint64_t da0 = sdesc_sw128(a_smem, 16, 1024);
+  const uint64_t db0 = sdesc_sw128(b_smem, 16, 1024);
+  uint64_t da[D / 32], db[D / 32];
 #pragma unroll
-  for (int kk = 0; kk < D / 32; ++kk)
-    mma_ss_f8(d_tmem, da + static_cast<uint64_t>((kk * 32) >> 4), db + static_cast<uint64_t>((kk * 32) >> 4), idesc,
-              kk > 0 ? 1u : 0u);
+  for (int kk = 0; kk < D / 32; ++kk) {
+    da[kk] = da0 + static_cast<uint64_t>((kk * 32) >> 4);
+    db[kk] = db0 + static_cast<uint64_t>((kk * 32) >> 4);
+  }
+  mma_ss_f8_n<D / 32>(d_tmem, da, db, idesc, 0u);
 }
 
 // O (+)= P V: P is 128 x 128 e5m2 in TMEM (four per 32-bit column, 8 columns
@@ -64,10 +49,14 @@ __device__ __forceinline__ void mma_qk_f8(uint32_t d_tmem, uint32_t a_smem, uint
 __device__ __forceinline__ void mma_pv_f8(uint32_t d_tmem, uint32_t p_tmem, uint32_t vt_smem, uint32_t idesc,
                                           bool accumulate) {
   const uint64_t dv = sdesc_sw128(vt_smem, 16, 1024);
+  uint32_t a[kBN / 32];
+  uint64_t b[kBN / 32];
 #pragma unroll
-  for (int kk = 0; kk < kBN / 32; ++kk)
-    mma_ts_f8(d_tmem, p_tmem + kk * 8, dv + static_cast<uint64_t>((kk * 32) >> 4), idesc,
-              (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < kBN / 32; ++kk) {
+    a[kk] = p_tmem + kk * 8;
+    b[kk] = dv + static_cast<uint64_t>((kk * 32) >> 4);
+  }
+  mma_ts_f8_n<kBN / 32>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
 // Four fp32 values -> four e5m2 bytes (round to nearest even, saturating to
@@ -192,45 +181,45 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0 && nt > 0) {
+    if (nt > 0) {
       // e5m2 has the format code of bf16 in the kind::f16 descriptor; both
       // operands K-major (V arrives transposed)
       constexpr uint32_t idesc_qk = idesc_f16(kBM, kBN, true, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(kBM, D, true, false, false);
       const uint32_t aQ[2] = {smem_u32(sQ), smem_u32(sQ) + C::QT};
-      bool ok = mbar_wait(&bar_q, 0, ctl, kErrTimeoutTma) && mbar_wait(&bar_k[0], 0, ctl, kErrTimeoutTma);
+      bool ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma) && warp_wait(&bar_k[0], 0, ctl, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
         for (int w = 0; w < 2; ++w)
           if (n_t[w] > 0) {
             mma_qk_f8<D>(tmem + col_s[w], aQ[w], smem_u32(sK(0)), idesc_qk);
-            mma_commit(&bar_s[w]);
+            commit_el(&bar_s[w]);
           }
       }
-      if (ok) mma_commit(&bar_kempty[0]);
+      if (ok) commit_el(&bar_kempty[0]);
       for (int t = 0; ok && t < nt; ++t) {
         const int sv = t % VST;
         const int sk1 = (t + 1) % KST;
-        if (!(ok = mbar_wait(&bar_v[sv], (t / VST) & 1, ctl, kErrTimeoutTma))) break;
+        if (!(ok = warp_wait(&bar_v[sv], (t / VST) & 1, ctl, kErrTimeoutTma))) break;
         const bool next = t + 1 < nt;
-        if (next && !(ok = mbar_wait(&bar_k[sk1], ((t + 1) / KST) & 1, ctl, kErrTimeoutTma))) break;
+        if (next && !(ok = warp_wait(&bar_k[sk1], ((t + 1) / KST) & 1, ctl, kErrTimeoutTma))) break;
         for (int w = 0; w < 2; ++w) {
           if (t < n_t[w]) {
-            if (!(ok = mbar_wait(&bar_p[w], t & 1, ctl, kErrTimeoutSoftmax))) break;
+            if (!(ok = warp_wait(&bar_p[w], t & 1, ctl, kErrTimeoutSoftmax))) break;
             tc_fence_after();
             mma_pv_f8(tmem + col_o[w], tmem + col_s[w], smem_u32(sV(sv)), idesc_pv, t > 0);
-            mma_commit(&bar_o[w]);
+            commit_el(&bar_o[w]);
           }
           if (next && t + 1 < n_t[w]) {
             mma_qk_f8<D>(tmem + col_s[w], aQ[w], smem_u32(sK(sk1)), idesc_qk);
-            mma_commit(&bar_s[w]);
+            commit_el(&bar_s[w]);
           }
         }
         if (!ok) break;
-        mma_commit(&bar_vempty[sv]);
-        if (next) mma_commit(&bar_kempty[sk1]);
+        commit_el(&bar_vempty[sv]);
+        if (next) commit_el(&bar_kempty[sk1]);
       }
-      if (ok) mma_commit(&bar_ofinal);
+      if (ok) commit_el(&bar_ofinal);
     }
   } else {
     // ------------------------------- softmax / correction / epilogue (tile w)

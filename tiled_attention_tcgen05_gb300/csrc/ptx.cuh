@@ -182,6 +182,231 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// ------------------------------------------------- batched MMA issue
+// N MMAs of one K-loop issued from ONE asm block by the elected lane of a
+// fully converged warp (every lane executes the call; elect.sync picks one).
+// The first MMA accumulates iff `acc` != 0, the rest always do.  Issuing a
+// whole K-loop this way keeps the issuing thread's instruction stream to the
+// MMAs themselves, which lets the tensor core run back to back; separate asm
+// statements per MMA from a single divergent lane issue far more slowly.
+
+__device__ __forceinline__ void mma_ss_x2(uint32_t d, const uint64_t (&a)[2], const uint64_t (&b)[2], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %6, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %5, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %4, %5, p1;\n"
+      "}\n"
+      ::"r"(d), "l"(a[0]), "l"(a[1]), "l"(b[0]), "l"(b[1]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_x4(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %10, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, p1;\n"
+      "}\n"
+      ::"r"(d), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_x8(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %18, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %17, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %17, p1;\n"
+      "}\n"
+      ::"r"(d), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_x2(uint32_t d, const uint32_t (&a)[2], const uint64_t (&b)[2], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %6, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %3, %5, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %4, %5, p1;\n"
+      "}\n"
+      ::"r"(d), "r"(a[0]), "r"(a[1]), "l"(b[0]), "l"(b[1]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_x4(uint32_t d, const uint32_t (&a)[4], const uint64_t (&b)[4], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %10, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, p1;\n"
+      "}\n"
+      ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_x8(uint32_t d, const uint32_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %18, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, p1;\n"
+      "}\n"
+      ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_f8_x2(uint32_t d, const uint64_t (&a)[2], const uint64_t (&b)[2], uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %6, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %3, %5, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %4, %5, p1;\n"
+      "}\n"
+      ::"r"(d), "l"(a[0]), "l"(a[1]), "l"(b[0]), "l"(b[1]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_f8_x4(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4], uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %10, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %5, %9, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %6, %9, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %9, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %9, p1;\n"
+      "}\n"
+      ::"r"(d), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_f8_x8(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %18, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %9, %17, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %10, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %11, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %12, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %13, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %6, %14, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %7, %15, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %8, %16, %17, p1;\n"
+      "}\n"
+      ::"r"(d), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_f8_x2(uint32_t d, const uint32_t (&a)[2], const uint64_t (&b)[2], uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %6, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %3, %5, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%2], %4, %5, p1;\n"
+      "}\n"
+      ::"r"(d), "r"(a[0]), "r"(a[1]), "l"(b[0]), "l"(b[1]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_f8_x4(uint32_t d, const uint32_t (&a)[4], const uint64_t (&b)[4], uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %10, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %5, %9, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%2], %6, %9, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %7, %9, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %8, %9, p1;\n"
+      "}\n"
+      ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_f8_x8(uint32_t d, const uint32_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred e, p0, p1;\n elect.sync _|e, 0xffffffff;\n"
+      " setp.ne.b32 p0, %18, 0;\n setp.eq.u32 p1, 1, 1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %9, %17, p0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%2], %10, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%3], %11, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%4], %12, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%5], %13, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%6], %14, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%7], %15, %17, p1;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%8], %16, %17, p1;\n"
+      "}\n"
+      ::"r"(d), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void mma_ss_n(uint32_t d, const uint64_t (&a)[N], const uint64_t (&b)[N], uint32_t idesc,
+                                         uint32_t acc) {
+  static_assert(N == 2 || N == 4 || N == 8, "batch of 2, 4 or 8");
+  if constexpr (N == 8) mma_ss_x8(d, a, b, idesc, acc);
+  else if constexpr (N == 4) mma_ss_x4(d, a, b, idesc, acc);
+  else mma_ss_x2(d, a, b, idesc, acc);
+}
+template <int N>
+__device__ __forceinline__ void mma_ts_n(uint32_t d, const uint32_t (&a)[N], const uint64_t (&b)[N], uint32_t idesc,
+                                         uint32_t acc) {
+  static_assert(N == 2 || N == 4 || N == 8, "batch of 2, 4 or 8");
+  if constexpr (N == 8) mma_ts_x8(d, a, b, idesc, acc);
+  else if constexpr (N == 4) mma_ts_x4(d, a, b, idesc, acc);
+  else mma_ts_x2(d, a, b, idesc, acc);
+}
+template <int N>
+__device__ __forceinline__ void mma_ss_f8_n(uint32_t d, const uint64_t (&a)[N], const uint64_t (&b)[N], uint32_t idesc,
+                                            uint32_t acc) {
+  static_assert(N == 2 || N == 4 || N == 8, "batch of 2, 4 or 8");
+  if constexpr (N == 8) mma_ss_f8_x8(d, a, b, idesc, acc);
+  else if constexpr (N == 4) mma_ss_f8_x4(d, a, b, idesc, acc);
+  else mma_ss_f8_x2(d, a, b, idesc, acc);
+}
+template <int N>
+__device__ __forceinline__ void mma_ts_f8_n(uint32_t d, const uint32_t (&a)[N], const uint64_t (&b)[N],
+                                            uint32_t idesc, uint32_t acc) {
+  static_assert(N == 2 || N == 4 || N == 8, "batch of 2, 4 or 8");
+  if constexpr (N == 8) mma_ts_f8_x8(d, a, b, idesc, acc);
+  else if constexpr (N == 4) mma_ts_f8_x4(d, a, b, idesc, acc);
+  else mma_ts_f8_x2(d, a, b, idesc, acc);
+}
+
+// tcgen05.commit by the elected lane of a fully converged warp.
+__device__ __forceinline__ void commit_el(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(smem_u32(bar))
+      : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (the layout a TMA load
 // with CU_TENSOR_MAP_SWIZZLE_128B produces).  Byte offsets: `lbo` is the
 // leading-dimension offset, `sbo` the stride-dimension offset (8-row groups).
