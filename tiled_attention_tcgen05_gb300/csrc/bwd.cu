@@ -727,6 +727,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
+// K-steps of chunk group g (the 32-key / 32-query chunk g of both column
+// halves): {2g, 2g + 1, 2g + 4, 2g + 5}.
+__device__ __forceinline__ constexpr int chunk_kstep(int g, int i) { return 2 * g + (i & 1) + 4 * (i >> 1); }
+
+// d (+)= X Y over the K-steps of chunk group g only (X, Y as in mma_tY); the
+// first MMA accumulates iff `accumulate`.  Whole converged warp.
+template <int G>
+__device__ __forceinline__ void mma_tY_g(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
+                                         bool accumulate) {
+  const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
+  uint32_t a[4];
+  uint64_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int kk = chunk_kstep(G, i);
+    a[i] = x_tmem + (kk & 3) * 8 + (kk >> 2) * 64;
+    b[i] = dy + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+  }
+  mma_ts_n<4>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
+}
+
+// The same for X with interleaved K-steps (as mma_tY_il).
+template <int G>
+__device__ __forceinline__ void mma_tY_il_g(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
+                                            bool accumulate) {
+  const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
+  uint32_t a[4];
+  uint64_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int kk = chunk_kstep(G, i);
+    a[i] = x_tmem + (kk >> 1) * 32 + (kk & 1) * 8;
+    b[i] = dy + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+  }
+  mma_ts_n<4>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
+}
+
 // ======================================================================
 //      dQ, standard mode: Q and dO in TMEM, three-or-more-deep K/V ring
 // ======================================================================
@@ -798,7 +835,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q, bar_qfree, bar_kv[STAGES], bar_kvempty[STAGES];
-  __shared__ __align__(8) uint64_t bar_s, bar_consumed, bar_dp, bar_ds, bar_done;
+  __shared__ __align__(8) uint64_t bar_s, bar_consumed, bar_dp, bar_ds[2], bar_done;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -829,7 +866,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_s, 1);
     mbar_init(&bar_consumed, kRowWarps);
     mbar_init(&bar_dp, 1);
-    mbar_init(&bar_ds, kRowWarps);
+    mbar_init(&bar_ds[0], kRowWarps);
+    mbar_init(&bar_ds[1], kRowWarps);
     mbar_init(&bar_done, 1);
     fence_mbar_init();
   }
@@ -891,9 +929,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_tB<D>(tmem + C::COL_A, tmem + C::COL_QT, smem_u32(sK(st1)), idesc_s);
           commit_el(&bar_s);
         }
-        if (!(ok = warp_wait(&bar_ds, t & 1, ctl, kErrTimeoutSoftmax))) break;
+        // dQ += dS K, chunk group 0 as soon as the softmax warps have formed it
+        if (!(ok = warp_wait(&bar_ds[0], t & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, t > 0);  // dQ += dS K
+        mma_tY_g<0>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, t > 0);
+        if (!(ok = warp_wait(&bar_ds[1], t & 1, ctl, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        mma_tY_g<1>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, true);
         commit_el(&bar_kvempty[st]);
         if (next) {
           mma_tB<D>(tmem + C::COL_B, tmem + C::COL_DOT, smem_u32(sV(st1)), idesc_s);
@@ -969,11 +1011,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pk[e] = pack2<BF>(ds.x, ds.y);
         }
         tmem_st_x16(lane_addr + C::COL_B + cb + 16 * c, pk);  // dS (16-bit) over dP
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_ds[c]);  // chunk group c of dS is in place
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_ds);
     }
     if (nkv > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
@@ -1027,7 +1069,7 @@ struct DkdvStdCfg {
   static constexpr int SMEM = USED + PAD;
   static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D;
   static_assert(PAD >= 0 && SMEM <= kSmemMax, "tiles do not fit in shared memory");
-  static_assert(BAR_BYTES >= 8 * (1 + 2 * QST + 2 * OST + 5 + 4) + 8, "barrier area too small");
+  static_assert(BAR_BYTES >= 8 * (1 + 2 * QST + 2 * OST + 6 + 4) + 8, "barrier area too small");
   static_assert(COL_DK + D <= 512, "TMEM overflow");
 };
 
@@ -1071,9 +1113,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t& bar_s = bar_oe[OST];
   uint64_t& bar_consumed = bar_oe[OST + 1];
   uint64_t& bar_dp = bar_oe[OST + 2];
-  uint64_t& bar_ds = bar_oe[OST + 3];
-  uint64_t& bar_done = bar_oe[OST + 4];
-  uint64_t* bar_pub = bar_oe + OST + 5;  // [buffer * 2 + half]: L / delta of a tile stored
+  uint64_t* bar_ds = bar_oe + OST + 3;  // [chunk group]
+  uint64_t& bar_done = bar_oe[OST + 5];
+  uint64_t* bar_pub = bar_oe + OST + 6;  // [buffer * 2 + half]: L / delta of a tile stored
   uint32_t& tmem_slot = *reinterpret_cast<uint32_t*>(bar_pub + 4);
   int& abort_flag = *(reinterpret_cast<int*>(bar_pub + 4) + 1);
   float* sLD = reinterpret_cast<float*>(base + C::LD_OFF);
@@ -1107,7 +1149,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_s, 1);
     mbar_init(&bar_consumed, kRowWarps);
     mbar_init(&bar_dp, 1);
-    mbar_init(&bar_ds, kRowWarps);
+    mbar_init(&bar_ds[0], kRowWarps);
+    mbar_init(&bar_ds[1], kRowWarps);
     mbar_init(&bar_done, 1);
     for (int i = 0; i < 4; ++i) mbar_init(&bar_pub[i], kRowWarps / 2);
     fence_mbar_init();
@@ -1173,11 +1216,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(sq1)), idesc_s);
           commit_el(&bar_s);
         }
-        if (!(ok = warp_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
+        // dV += P^T dO and dK += dS^T Q, chunk group 0 as soon as the softmax
+        // warps have formed it
+        if (!(ok = warp_wait(&bar_ds[0], u & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_tY_il<D>(tmem + C::COL_DV, tmem + C::COL_B, smem_u32(sDO(so)), idesc_g, u > 0);      // dV += P^T dO
+        mma_tY_il_g<0>(tmem + C::COL_DV, tmem + C::COL_B, smem_u32(sDO(so)), idesc_g, u > 0);
+        mma_tY_il_g<0>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, u > 0);
+        if (!(ok = warp_wait(&bar_ds[1], u & 1, ctl, kErrTimeoutSoftmax))) break;
+        tc_fence_after();
+        mma_tY_il_g<1>(tmem + C::COL_DV, tmem + C::COL_B, smem_u32(sDO(so)), idesc_g, true);
         commit_el(&bar_oe[so]);
-        mma_tY_il<D>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, u > 0);  // dK += dS^T Q
+        mma_tY_il_g<1>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, true);
         commit_el(&bar_qe[sq]);
         if (next) {
           if (!(ok = warp_wait(&bar_of[so1], ((u + 1) / OST) & 1, ctl, kErrTimeoutTma))) break;
@@ -1301,11 +1350,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_st_16x128b_x4(ga, pp);
           tmem_st_16x128b_x4(ga + 16, pd);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_ds[c]);  // chunk group c of P^T / dS^T is in place
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_ds);
       if (u + 1 < nq) {  // every warp of the half is past tile u - 1, the buffer's previous tile
         ld_slot(u + 1)[ld_arr * 64 + ld_col] = pre;
         __syncwarp();
