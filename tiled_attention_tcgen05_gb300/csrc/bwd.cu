@@ -5,7 +5,9 @@
 //   warps 0-7  element-wise softmax gradient; TMEM lane = row (warp % 4
 //              selects the 32-lane quarter), and warp / 4 selects which half
 //              of the tile's 128 columns the thread handles;
-//   warp 8     TMA producer;  warp 9  TMEM allocator and MMA issuer.
+//   warp 8     TMA producer;
+//   warp 9     TMEM allocator and MMA issuer (the whole warp; one elected
+//              lane issues each K-loop of MMAs as a single asm block).
 //
 //  * attn_bwd_dkdv_kernel: key-stationary.  The CTA keeps a 128-key tile of K
 //    and V in shared memory and walks the query tiles that see it.  Per query

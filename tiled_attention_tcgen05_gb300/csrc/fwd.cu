@@ -7,7 +7,8 @@
 //              which is TMEM lane r (tcgen05.ld 32x32b shape), so row max and
 //              row sum need no shuffles;
 //   warp 4     TMA producer (Q once, then a STAGES-deep ring of K/V tiles);
-//   warp 5     TMEM allocator and MMA issuer (one thread).
+//   warp 5     TMEM allocator and MMA issuer (the whole warp; one elected lane
+//              issues each K-loop of MMAs as a single asm block).
 // Per key tile t:  S = Q K_t^T (tcgen05.mma, A and B from shared memory) ->
 // softmax writes P (16-bit, packed two per TMEM column) over S -> O += P V_t
 // with P read straight from TMEM.  Standard mode double-buffers S so the
