@@ -35,6 +35,11 @@ Definitions, and the page passages they follow:
   ``mu_i = sum_j P_ij T_ij``, ``tO = (P o T) V - mu o O + P tV``.  This is the
   derivative of O along (tq, tk, tv): ``dP = P o (T - mu)``; mu itself is the
   derivative of L (``attention_jvp_tl``).
+* Backward of the JVP (``attention_jvp_bwd``): the gradients of
+  ``<dO, O> + <dtO, tO>`` with respect to q, k, v and the tangents, taken by
+  reverse-mode differentiation through the JVP forward's steps above in
+  reverse order.  The pages give the JVP forward and a backward for O only;
+  this is the plain chain rule applied to their definitions.
 * Piecewise attention ("FlagAttention piecewise.py", ``_fwd_kernel``
   ``piecewise_mask``): with the signed distance ``d_ij = i + N - M - j``, the
   score uses (q2, k2) when ``d_ij >= w`` and (q1, k1) otherwise.  Backward
@@ -64,7 +69,7 @@ __all__ = [
     "piecewise_fwd", "piecewise_bwd", "attention_fwd_bhsd", "attention_bwd_bhsd",
     "attention_jvp_bhsd", "piecewise_fwd_bhsd", "piecewise_bwd_bhsd", "default_scale",
     "lse_merge_fwd", "lse_merge_bwd", "lse_merge_fwd_bhsd", "lse_merge_bwd_bhsd",
-    "attention_jvp_tl", "attention_jvp_tl_bhsd",
+    "attention_jvp_tl", "attention_jvp_tl_bhsd", "attention_jvp_bwd", "attention_jvp_bwd_bhsd",
 ]
 
 
@@ -160,6 +165,49 @@ def attention_jvp_tl(q, k, tq, tk, causal: bool, sm_scale=None):
     P, _ = _softmax(s * (q @ k.T), keep)
     T = np.where(keep, s * (tq @ k.T + q @ tk.T), 0.0)
     return (P * T).sum(axis=1)
+
+
+def attention_jvp_bwd(q, k, v, tq, tk, tv, do, dto, causal: bool, sm_scale=None):
+    """One head: gradients (dq, dk, dv, dtq, dtk, dtv) of <dO, O> + <dtO, tO>,
+    with O and tO the outputs of ``attention_jvp``.
+
+    The pages stop at the JVP's forward; this is reverse-mode differentiation
+    of that forward's own steps, taken backwards one at a time:
+      S = s q k^T, P = softmax(S), O = P v,
+      T = s (tq k^T + q tk^T) (0 where masked), mu = rowsum(P o T),
+      tO = (P o T) v - mu o O + P tv.
+    """
+    q, k, v, tq, tk, tv, do, dto = _f64(q, k, v, tq, tk, tv, do, dto)
+    s = default_scale(q.shape[1], sm_scale)
+    keep = allowed_mask(q.shape[0], k.shape[0], causal)
+    P, _ = _softmax(s * (q @ k.T), keep)
+    O = P @ v
+    T = np.where(keep, s * (tq @ k.T + q @ tk.T), 0.0)
+    PT = P * T
+    mu = PT.sum(axis=1)
+    # tO = PT v - mu O + P tv
+    dPT = dto @ v.T
+    dv = PT.T @ dto
+    dmu = -(dto * O).sum(axis=1)
+    dO_total = do - mu[:, None] * dto
+    dP = dto @ tv.T
+    dtv = P.T @ dto
+    # mu = rowsum(PT)
+    dPT = dPT + dmu[:, None]
+    # PT = P o T
+    dP = dP + dPT * T
+    dT = np.where(keep, dPT * P, 0.0)
+    # O = P v
+    dP = dP + dO_total @ v.T
+    dv = dv + P.T @ dO_total
+    # P = softmax(S) over the kept keys (dS = P o (dP - rowsum(P o dP)))
+    dS = P * (dP - (P * dP).sum(axis=1)[:, None])
+    # S = s q k^T and T = s (tq k^T + q tk^T)
+    dq = s * (dS @ k) + s * (dT @ tk)
+    dk = s * (dS.T @ q) + s * (dT.T @ tq)
+    dtq = s * (dT @ k)
+    dtk = s * (dT.T @ q)
+    return dq, dk, dv, dtq, dtk, dtv
 
 
 # ---------------------------------------------------------------- piecewise
@@ -285,6 +333,11 @@ def piecewise_fwd_bhsd(q1, k1, q2, k2, v, causal, sm_scale=None, w=0, heads=None
 
 def piecewise_bwd_bhsd(q1, k1, q2, k2, v, do, causal, sm_scale=None, w=0, heads=None):
     return _run_bhsd(piecewise_bwd, (q1, k1, q2, k2, v, do), (causal, sm_scale, w), heads, 5)
+
+
+def attention_jvp_bwd_bhsd(q, k, v, tq, tk, tv, do, dto, causal, sm_scale=None, heads=None):
+    """[B,H,S,D] inputs -> (dq, dk, dv, dtq, dtk, dtv)."""
+    return _run_bhsd(attention_jvp_bwd, (q, k, v, tq, tk, tv, do, dto), (causal, sm_scale), heads, 6)
 
 
 def attention_jvp_tl_bhsd(q, k, tq, tk, causal, sm_scale=None, heads=None):

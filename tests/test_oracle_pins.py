@@ -469,3 +469,62 @@ def test_jvp_tangent_of_lse_matches_finite_differences(M, N, causal):
     # and it is the mu of the JVP: tO = (P o T) V - mu O + P tV with tv = 0, v = 1 gives tO = sum(P o T) - mu = 0
     _, _, tO = oracle.attention_jvp(q, k, np.ones((N, 1)), tq, tk, np.zeros((N, 1)), causal, s)
     np.testing.assert_allclose(tO[fin], 0.0, atol=1e-12)
+
+
+# ------------------------------------------------- backward of the JVP
+@pytest.mark.parametrize("M,N,D,causal", [(1, 1, 4, True), (4, 4, 4, False), (5, 5, 4, True),
+                                          (3, 6, 4, True), (6, 3, 4, True), (5, 7, 3, False)])
+def test_jvp_backward_matches_finite_differences(M, N, D, causal):
+    """Gradients of <dO, O> + <dtO, tO> against central differences of that
+    scalar, O and tO from the (separately pinned) JVP forward."""
+    xs = [rand(M, D), rand(N, D), rand(N, D), rand(M, D), rand(N, D), rand(N, D)]
+    do, dto = rand(M, D), rand(M, D)
+    s = 0.55
+
+    def f():
+        O, _, tO = oracle.attention_jvp(*xs, causal, s)
+        return float((O * do).sum() + (tO * dto).sum())
+
+    grads = oracle.attention_jvp_bwd(*xs, do, dto, causal, s)
+    for x, g in zip(xs, grads):
+        np.testing.assert_allclose(g, _fd_grad(f, x), atol=1e-8, rtol=1e-6)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_jvp_backward_tangent_grads_are_the_plain_backward_of_dto(causal):
+    """tO is linear in the tangents with the Jacobian of O, so the tangents'
+    gradients are the plain backward with dO replaced by dtO; with dtO = 0
+    the primal gradients are the plain backward of dO."""
+    M, N, D = 7, 9, 4
+    q, k, v, tq, tk, tv = rand(M, D), rand(N, D), rand(N, D), rand(M, D), rand(N, D), rand(N, D)
+    do, dto = rand(M, D), rand(M, D)
+    s = 0.5
+    _, _, _, dtq, dtk, dtv = oracle.attention_jvp_bwd(q, k, v, tq, tk, tv, do, dto, causal, s)
+    for a, b in zip((dtq, dtk, dtv), oracle.attention_bwd(q, k, v, dto, causal, s)):
+        np.testing.assert_allclose(a, b, atol=1e-13)
+    g = oracle.attention_jvp_bwd(q, k, v, tq, tk, tv, do, np.zeros((M, D)), causal, s)
+    for a, b in zip(g[:3], oracle.attention_bwd(q, k, v, do, causal, s)):
+        np.testing.assert_allclose(a, b, atol=1e-13)
+    for a in g[3:]:
+        assert np.all(a == 0)
+    # Euler: tO is homogeneous of degree 1 in the tangents
+    _, _, tO = oracle.attention_jvp(q, k, v, tq, tk, tv, causal, s)
+    lhs = float((dtq * tq).sum() + (dtk * tk).sum() + (dtv * tv).sum())
+    assert abs(lhs - float((dto * tO).sum())) < 1e-12 * max(1.0, abs(lhs))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_jvp_backward_second_order_part_is_symmetric(causal):
+    """With dO = 0 the primal gradients are the gradient of <dtO, J(x) t>, a
+    mixed second derivative: <G(t), u> = <G(u), t> for any two tangents."""
+    M, N, D = 6, 8, 3
+    x = [rand(M, D), rand(N, D), rand(N, D)]
+    t = [rand(M, D), rand(N, D), rand(N, D)]
+    u = [rand(M, D), rand(N, D), rand(N, D)]
+    dto = rand(M, D)
+    z = np.zeros((M, D))
+    gt = oracle.attention_jvp_bwd(*x, *t, z, dto, causal, 0.6)[:3]
+    gu = oracle.attention_jvp_bwd(*x, *u, z, dto, causal, 0.6)[:3]
+    a = sum(float((g * w).sum()) for g, w in zip(gt, u))
+    b = sum(float((g * w).sum()) for g, w in zip(gu, t))
+    assert abs(a - b) < 1e-11 * max(1.0, abs(a))
