@@ -10,6 +10,8 @@
  *             and the comment thread's non-causal backward fix.
  *   [PW]      "FlagAttention src/flag_attn/piecewise.py": _fwd_kernel,
  *             _bwd_preprocess, _bwd_kv_kernel, _bwd_q_kernel, attention().
+ *   [MERGE]   "backward_phase_2": a two-state online-softmax merge
+ *             (reference_forward) and its backward.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -72,7 +74,6 @@ size_t attn_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt);
 /* Backward of attn_fwd for the loss <dO, O>.
  * [FA-JVP] _attn_bwd_preprocess (delta = rowsum(dO o O)), _attn_bwd_dkdv,
  * _attn_bwd_dq and JVPAttn.backward, with the thread's non-causal fix;
- * [MERGE] "backward_phase_2" (a two-state online-softmax merge and its backward).
  * [PW] _bwd_preprocess / _bwd_kv_kernel / _bwd_q_kernel.
  * In: q,k,v, o and lse from attn_fwd, dO [B,H,M,D].  Out: dq [B,H,M,D],
  * dk, dv [B,H,N,D] (dt).  ws: >= attn_bwd_workspace_bytes(...) bytes of
@@ -113,6 +114,32 @@ ta_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const vo
 ta_status attn_fwd_jvp(const void* q, const void* k, const void* v, const void* tq, const void* tk,
                        const void* tv, void* o, float* lse, void* to, float* tlse, int B, int H, int M, int N,
                        int D, ta_dtype dt, int causal, float sm_scale, void* stream);
+
+/* Bytes of workspace attn_bwd_jvp needs: eps and delta2 [B,H,M] fp32 (each
+ * padded to 256 bytes). */
+size_t attn_bwd_jvp_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt);
+
+/* Backward of attn_fwd_jvp: the gradients of <dO, O> + <dtO, tO> with respect
+ * to q, k, v and the tangents tq, tk, tv.  [FA-JVP] gives the JVP forward
+ * (above) and a backward for O only; this is the chain rule taken back
+ * through that forward's steps.  With P, T and mu as in attn_fwd_jvp,
+ * eps_i = <dtO_i, O_i>, delta2_i = <dO_i, O_i> + <dtO_i, tO_i>:
+ *   dT = P o (dtO V^T - eps),  dS = P o (dO V^T + dtO tV^T - delta2) + (T - mu) o dT,
+ *   dq = sm_scale (dS K + dT tK),  dk = sm_scale (dS^T Q + dT^T tQ),
+ *   dv = P^T dO + (P o (T - mu))^T dtO,
+ * and (dtq, dtk, dtv) = the plain backward (attn_bwd) of dO := dtO, since tO
+ * is the Jacobian of O applied to the tangents.
+ * In: q,tq [B,H,M,D], k,v,tk,tv [B,H,N,D]; o, lse, to and tlse from
+ * attn_fwd_jvp (tlse is required here); dO, dtO [B,H,M,D].
+ * Out: dq, dtq [B,H,M,D], dk, dv, dtk, dtv [B,H,N,D] (dt).
+ * ws: >= attn_bwd_jvp_workspace_bytes(...) bytes of device memory, 16-byte
+ * aligned, contents need not be initialised; TA_ERR_INVALID_ARG if it is
+ * null or too small. */
+ta_status attn_bwd_jvp(const void* q, const void* k, const void* v, const void* tq, const void* tk, const void* tv,
+                       const void* o, const float* lse, const void* to, const float* tlse, const void* dO,
+                       const void* dtO, void* dq, void* dk, void* dv, void* dtq, void* dtk, void* dtv, void* ws,
+                       size_t ws_bytes, int B, int H, int M, int N, int D, ta_dtype dt, int causal,
+                       float sm_scale, void* stream);
 
 /* Piecewise attention forward ([PW] attention(), _fwd_kernel): the score of
  * (i, j) is sm_scale * q2_i . k2_j when the signed distance i + N - M - j >= w,

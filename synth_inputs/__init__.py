@@ -106,6 +106,6 @@ def attention_inputs(B, H, M, N, D, dtype, workload, names=("q", "k", "v", "do")
     """Dict of named CPU tensors; rows of q/do have length M, of k/v length N."""
     out = {}
     for idx, name in enumerate(names):
-        rows = M if name in ("q", "do", "tq", "q1", "q2") else N
+        rows = M if name in ("q", "do", "tq", "dto", "q1", "q2") else N
         out[name] = randn((B, H, rows, D), dtype, seed_for(workload, idx))
     return out

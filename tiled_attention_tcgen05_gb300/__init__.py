@@ -9,6 +9,8 @@ Entry points (same names as the C ABI):
   attn_fwd(q, k, v, causal, sm_scale)                -> (o, lse)
   attn_bwd(q, k, v, o, lse, do, causal, sm_scale)    -> (dq, dk, dv)
   attn_fwd_jvp(q, k, v, tq, tk, tv, causal, sm_scale, with_tlse) -> (o, lse, to[, tlse])
+  attn_bwd_jvp(q, k, v, tq, tk, tv, o, lse, to, tlse, do, dto, causal, sm_scale)
+                                                     -> (dq, dk, dv, dtq, dtk, dtv)
   piecewise_fwd(q1, k1, q2, k2, v, w, causal, sm_scale) -> (o, lse)
   piecewise_bwd(q1, k1, q2, k2, v, o, lse, do, w, causal, sm_scale)
                                                      -> (dq1, dk1, dq2, dk2, dv)
@@ -22,7 +24,7 @@ import os
 
 import torch
 
-__all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_fwd_jvp", "piecewise_fwd", "piecewise_bwd", "merge_fwd", "merge_bwd", "attn_fwd_fp8",
+__all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_fwd_jvp", "attn_bwd_jvp", "piecewise_fwd", "piecewise_bwd", "merge_fwd", "merge_bwd", "attn_fwd_fp8",
            "attn_bwd_workspace_bytes", "sync_status", "selftest_wait_timeout", "profile_enable",
            "profile_read", "set_wait_timeout_ms", "TAError", "STATUS"]
 
@@ -40,6 +42,8 @@ _SIGS = {
     "attn_bwd_workspace_bytes": ([_i] * 6, _sz),
     "attn_bwd": ([_vp] * 10 + [_sz] + [_i] * 7 + [_f, _vp], _i),
     "attn_fwd_jvp": ([_vp] * 10 + [_i] * 7 + [_f, _vp], _i),
+    "attn_bwd_jvp_workspace_bytes": ([_i] * 6, _sz),
+    "attn_bwd_jvp": ([_vp] * 19 + [_sz] + [_i] * 7 + [_f, _vp], _i),
     "piecewise_fwd": ([_vp] * 7 + [_i] * 7 + [_f, _i, _vp], _i),
     "piecewise_bwd_workspace_bytes": ([_i] * 6, _sz),
     "piecewise_bwd": ([_vp] * 14 + [_sz] + [_i] * 7 + [_f, _i, _vp], _i),
@@ -168,6 +172,27 @@ def attn_fwd_jvp(q, k, v, tq, tk, tv, causal=False, sm_scale=None, with_tlse=Fal
                                             _ptr(lse), _ptr(to), _ptr(tlse), B, H, M, N, D, dt,
                                             int(bool(causal)), _scale(sm_scale), _stream(stream)))
     return (o, lse, to, tlse) if with_tlse else (o, lse, to)
+
+
+def attn_bwd_jvp(q, k, v, tq, tk, tv, o, lse, to, tlse, do, dto, causal=False, sm_scale=None, ws=None,
+                 stream=None):
+    """Backward of attn_fwd_jvp: gradients of <do, o> + <dto, to> with respect
+    to (q, k, v, tq, tk, tv); o, lse, to, tlse are attn_fwd_jvp's outputs
+    (with_tlse=True)."""
+    lib = load()
+    B, H, M, N, D, dt = _prep({"q": q, "k": k, "v": v, "tq": tq, "tk": tk, "tv": tv, "o": o, "to": to, "do": do,
+                               "dto": dto}, ("q", "tq", "o", "to", "do", "dto"), ("k", "v", "tk", "tv"))
+    _lse_of("lse", lse, B, H, M, q.device)
+    _lse_of("tlse", tlse, B, H, M, q.device)
+    grads = [torch.empty_like(x) for x in (q, k, v, tq, tk, tv)]
+    nws = int(lib.attn_bwd_jvp_workspace_bytes(B, H, M, N, D, dt))
+    if ws is None:
+        ws = torch.empty(max(nws, 16), device=q.device, dtype=torch.uint8)
+    _check("attn_bwd_jvp", lib.attn_bwd_jvp(*(_ptr(x) for x in (q, k, v, tq, tk, tv, o, lse, to, tlse, do, dto)),
+                                            *(_ptr(g) for g in grads), _ptr(ws), ws.numel() * ws.element_size(),
+                                            B, H, M, N, D, dt, int(bool(causal)), _scale(sm_scale),
+                                            _stream(stream)))
+    return tuple(grads)
 
 
 def piecewise_fwd(q1, k1, q2, k2, v, w, causal=False, sm_scale=None, stream=None):

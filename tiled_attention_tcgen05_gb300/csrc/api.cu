@@ -56,15 +56,16 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [BH, S, D] 16-bit tensor viewed as a 3-D map with 64 x 128 x 1 boxes and
-// 128-byte swizzle; rows past S (and, for D < 64, columns past D) read as
+// [BH, S, D] 16-bit tensor viewed as a 3-D map with 64 x box_rows x 1 boxes
+// and 128-byte swizzle; rows past S (and, for D < 64, columns past D) read as
 // zeros.
-static bool make_map(CUtensorMap* map, const void* ptr, long long BH, long long S, int D, bool bf16) {
+static bool make_map(CUtensorMap* map, const void* ptr, long long BH, long long S, int D, bool bf16,
+                     int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -320,6 +321,102 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
   return cuda_status(e);
 }
 
+// Backward of the JVP.  The workspace holds eps = <dtO, O> and
+// delta2 = <dO, O> + <dtO, tO> per query row.  The tangents' gradients are the
+// plain backward with dO := dtO (whose delta is eps); the primal gradients
+// come from the kernels of the JVP backward.
+static ta_status run_bwd_jvp(const Problem& p, const void* q, const void* k, const void* v, const void* tq,
+                             const void* tk, const void* tv, const void* o, const float* lse, const void* to,
+                             const float* tlse, const void* dO, const void* dtO, void* dq, void* dk, void* dv,
+                             void* dtq, void* dtk, void* dtv, void* ws, size_t ws_bytes, int causal,
+                             cudaStream_t s) {
+  if (p.BH == 0) return TA_OK;
+  const size_t kv_bytes = static_cast<size_t>(p.BH) * p.N * p.D * p.esize;
+  if (p.M == 0) {  // no query: every key-side gradient is zero
+    cudaError_t e = cudaSuccess;
+    for (void* g : {dk, dv, dtk, dtv})
+      if (e == cudaSuccess) e = launch_zero(g, kv_bytes, s);
+    return cuda_status(e);
+  }
+  const size_t rb = delta_bytes(p.BH, p.M);
+  if (ws_bytes < 2 * rb) return TA_ERR_INVALID_ARG;
+  float* eps = static_cast<float*>(ws);
+  float* delta2 = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + rb);
+  prof_begin("bwd_jvp_delta", s);
+  cudaError_t e = p.f32 ? launch_f32_jvp_delta(p.D, static_cast<const float*>(o), static_cast<const float*>(dO),
+                                               static_cast<const float*>(to), static_cast<const float*>(dtO), eps,
+                                               delta2, p.BH * p.M, s)
+                        : launch_jvp_delta(p.bf16, p.D, o, dO, to, dtO, eps, delta2, p.BH * p.M, s);
+  prof_end(s);
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  const size_t q_bytes = static_cast<size_t>(p.BH) * p.M * p.D * p.esize;
+  if (p.N == 0) {
+    e = launch_zero(dq, q_bytes, s);
+    if (e == cudaSuccess) e = launch_zero(dtq, q_bytes, s);
+    return cuda_status(e);
+  }
+  BwdArgs at = bwd_args(p, causal, 0, lse, eps);  // tangents: plain backward of dtO
+  at.dq = dtq;
+  at.dk = dtk;
+  at.dv = dtv;
+  BwdArgs ap = bwd_args(p, causal, 0, lse, delta2);  // primal gradients
+  ap.mu = tlse;
+  ap.eps = eps;
+  ap.dq = dq;
+  ap.dk = dk;
+  ap.dv = dv;
+  if (p.f32) {
+    F32Ptrs fp{static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v), nullptr,
+               nullptr, nullptr, static_cast<const float*>(dtO)};
+    prof_begin("attn_bwd_jvp_tangents_f32", s);
+    e = launch_f32_bwd(kStd, p.D, fp, at, s);
+    prof_end(s);
+    if (e != cudaSuccess) return TA_ERR_CUDA;
+    F32JvpPtrs jp{static_cast<const float*>(q),  static_cast<const float*>(k),  static_cast<const float*>(v),
+                  static_cast<const float*>(tq), static_cast<const float*>(tk), static_cast<const float*>(tv),
+                  static_cast<const float*>(dO), static_cast<const float*>(dtO)};
+    prof_begin("attn_bwd_jvp_f32", s);
+    e = launch_f32_jvp_bwd(p.D, jp, ap, s);
+    prof_end(s);
+    return cuda_status(e);
+  }
+  BwdMaps maps;
+  JvpBwdMaps jm;
+  bool ok = make_map(&maps.q, q, p.BH, p.M, p.D, p.bf16) && make_map(&maps.k, k, p.BH, p.N, p.D, p.bf16) &&
+            make_map(&maps.v, v, p.BH, p.N, p.D, p.bf16) && make_map(&maps.dO, dtO, p.BH, p.M, p.D, p.bf16);
+  maps.q2 = maps.q;
+  maps.k2 = maps.k;
+  const void* mrows[4] = {q, tq, dO, dtO};
+  const void* nrows[4] = {k, tk, v, tv};
+  CUtensorMap* m128[4] = {&jm.q128, &jm.tq128, &jm.do128, &jm.dto128};
+  CUtensorMap* m64[4] = {&jm.q64, &jm.tq64, &jm.do64, &jm.dto64};
+  CUtensorMap* n128[4] = {&jm.k128, &jm.tk128, &jm.v128, &jm.tv128};
+  CUtensorMap* n64[4] = {&jm.k64, &jm.tk64, &jm.v64, &jm.tv64};
+  for (int i = 0; ok && i < 4; ++i)
+    ok = make_map(m128[i], mrows[i], p.BH, p.M, p.D, p.bf16, 128) &&
+         make_map(m64[i], mrows[i], p.BH, p.M, p.D, p.bf16, 64) &&
+         make_map(n128[i], nrows[i], p.BH, p.N, p.D, p.bf16, 128) &&
+         make_map(n64[i], nrows[i], p.BH, p.N, p.D, p.bf16, 64);
+  if (!ok) return TA_ERR_CUDA;
+  const int kd = kernel_d(p.D);
+  prof_begin("attn_bwd_jvp_tangents_dkdv", s);
+  e = launch_bwd_dkdv(kStd, p.bf16, kd, maps, at, s);
+  prof_end(s);
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  prof_begin("attn_bwd_jvp_tangents_dq", s);
+  e = launch_bwd_dq(kStd, p.bf16, kd, maps, at, s);
+  prof_end(s);
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  prof_begin("attn_bwd_jvp_dkdv", s);
+  e = launch_bwd_jvp(true, p.bf16, kd, jm, ap, s);
+  prof_end(s);
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  prof_begin("attn_bwd_jvp_dq", s);
+  e = launch_bwd_jvp(false, p.bf16, kd, jm, ap, s);
+  prof_end(s);
+  return cuda_status(e);
+}
+
 }  // namespace ta
 
 using namespace ta;
@@ -477,6 +574,27 @@ ta_status attn_bwd(const void* q, const void* k, const void* v, const void* o, c
   if (st != TA_OK) return st;
   return run_bwd(kStd, p, q, k, v, nullptr, nullptr, o, lse, dO, dq, dk, nullptr, nullptr, dv, ws, ws_bytes,
                  causal, 0, static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_bwd_jvp_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt) {
+  return 2 * attn_bwd_workspace_bytes(B, H, M, N, D, dt);
+}
+
+ta_status attn_bwd_jvp(const void* q, const void* k, const void* v, const void* tq, const void* tk, const void* tv,
+                       const void* o, const float* lse, const void* to, const float* tlse, const void* dO,
+                       const void* dtO, void* dq, void* dk, void* dv, void* dtq, void* dtk, void* dtv, void* ws,
+                       size_t ws_bytes, int B, int H, int M, int N, int D, ta_dtype dt, int causal,
+                       float sm_scale, void* stream) {
+  Problem p;
+  ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
+  if (st != TA_OK) return st;
+  if (p.BH == 0 || (M == 0 && N == 0)) return TA_OK;
+  if (M == 0) st = check_ptrs({dk, dv, dtk, dtv});
+  else if (N == 0) st = check_ptrs({o, to, dO, dtO, dq, dtq, ws});
+  else st = check_ptrs({q, k, v, tq, tk, tv, o, lse, to, tlse, dO, dtO, dq, dk, dv, dtq, dtk, dtv, ws});
+  if (st != TA_OK) return st;
+  return run_bwd_jvp(p, q, k, v, tq, tk, tv, o, lse, to, tlse, dO, dtO, dq, dk, dv, dtq, dtk, dtv, ws, ws_bytes,
+                     causal, static_cast<cudaStream_t>(stream));
 }
 
 ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,

@@ -1,6 +1,7 @@
 // Memory-bound helper kernels: the backward preprocess delta = rowsum(dO o O)
 // ("Triton fused attention tutorial, updated with JVP support",
-// _attn_bwd_preprocess; "FlagAttention piecewise.py", _bwd_preprocess), the
+// _attn_bwd_preprocess; "FlagAttention piecewise.py", _bwd_preprocess), its
+// two-sum counterpart for the backward of the JVP, the
 // fill for rows that see no key (piecewise _fwd_kernel, empty lines: O = 0,
 // L = -inf) and a zero fill.
 #include "common.cuh"
@@ -33,6 +34,47 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint4* __restrict__ o,
 #pragma unroll
     for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (act && g == 0) delta[row] = acc;
+  }
+}
+
+// Backward of the JVP: eps = <dtO, O> and delta2 = <dO, O> + <dtO, tO> per
+// row, the same 16-byte-per-thread layout as delta_kernel.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) jvp_delta_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
+                                                        const uint4* __restrict__ to, const uint4* __restrict__ dto,
+                                                        float* __restrict__ eps, float* __restrict__ delta2,
+                                                        long long rows) {
+  constexpr int G = D / 8;
+  constexpr int RPB = 256 / G;
+  const int g = threadIdx.x % G;
+  const long long stride = static_cast<long long>(gridDim.x) * RPB;
+  for (long long rb = static_cast<long long>(blockIdx.x) * RPB; rb < rows; rb += stride) {
+    const long long row = rb + threadIdx.x / G;
+    const bool act = row < rows;
+    float e = 0.f, d = 0.f;
+    if (act) {
+      const uint4 a = __ldg(o + row * G + g), b = __ldg(dO + row * G + g);
+      const uint4 c = __ldg(to + row * G + g), t = __ldg(dto + row * G + g);
+      const T* ap = reinterpret_cast<const T*>(&a);
+      const T* bp = reinterpret_cast<const T*>(&b);
+      const T* cp = reinterpret_cast<const T*>(&c);
+      const T* tp = reinterpret_cast<const T*>(&t);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float oi = static_cast<float>(ap[i]), ti = static_cast<float>(tp[i]);
+        e = fmaf(ti, oi, e);
+        d = fmaf(static_cast<float>(bp[i]), oi, fmaf(ti, static_cast<float>(cp[i]), d));
+      }
+    }
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) {
+      e += __shfl_xor_sync(0xffffffffu, e, off);
+      d += __shfl_xor_sync(0xffffffffu, d, off);
+    }
+    if (act && g == 0) {
+      eps[row] = e;
+      delta2[row] = d;
+    }
   }
 }
 
@@ -72,6 +114,35 @@ cudaError_t launch_delta(bool bf16, int D, const void* o, const void* dO, float*
     return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <typename T, int D>
+static void jvp_delta_t(const void* o, const void* dO, const void* to, const void* dto, float* eps, float* delta2,
+                        long long rows, cudaStream_t s) {
+  constexpr int RPB = 256 / (D / 8);
+  long long blocks = (rows + RPB - 1) / RPB;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  jvp_delta_kernel<T, D><<<blocks, 256, 0, s>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dO),
+                                                static_cast<const uint4*>(to), static_cast<const uint4*>(dto), eps,
+                                                delta2, rows);
+}
+
+cudaError_t launch_jvp_delta(bool bf16, int D, const void* o, const void* dO, const void* to, const void* dto,
+                             float* eps, float* delta2, long long rows, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+#define TA_JVP_DELTA(D_)                                                                     \
+  if (D == D_) {                                                                             \
+    if (bf16) jvp_delta_t<__nv_bfloat16, D_>(o, dO, to, dto, eps, delta2, rows, s);          \
+    else jvp_delta_t<__half, D_>(o, dO, to, dto, eps, delta2, rows, s);                      \
+    return cudaGetLastError();                                                               \
+  }
+  TA_JVP_DELTA(16)
+  TA_JVP_DELTA(32)
+  TA_JVP_DELTA(64)
+  TA_JVP_DELTA(128)
+#undef TA_JVP_DELTA
+  return cudaErrorInvalidValue;
 }
 
 __global__ void empty_rows_kernel(uint4* o, float* lse, uint4* to, long long rows, int vec_per_row) {

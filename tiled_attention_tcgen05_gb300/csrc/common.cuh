@@ -45,7 +45,9 @@ struct BwdArgs {
   void* dk2;  // piecewise only
   void* dv;
   const float* lse;
-  const float* delta;
+  const float* delta;  // backward of the JVP: <dO, O> + <dtO, tO>
+  const float* mu;     // backward of the JVP only: tL = rowsum(P o T)
+  const float* eps;    // backward of the JVP only: <dtO, O>
   int BH, M, N, P_SEQ;
   int causal;
   int w;

@@ -286,6 +286,153 @@ __global__ void __launch_bounds__(kF32Warps * 32) f32_dkdv_kernel(const float* _
   if constexpr (PW) store_row<E, D>(reinterpret_cast<float*>(a.dk2) + koff, gk2, a.sm_scale, lane);
 }
 
+// ------------------------------------------- backward of the JVP (fp32)
+// Gradients of <dO, O> + <dtO, tO> with respect to q, k, v; per (i, j), with
+// t = T - mu:  dT = P (dtO.v_j - eps_i),  dS = P (dO.v_j + dtO.tv_j - delta2_i)
+// + t dT,  dq_i += dS k_j + dT tk_j,  dk_j += dS q_i + dT tq_i,
+// dv_j += P dO_i + P t dtO_i  (dq and dk times sm_scale at the end).
+template <int D>
+__global__ void __launch_bounds__(256) f32_jvp_delta_kernel(const float* o, const float* dO, const float* to,
+                                                            const float* dto, float* eps, float* delta2,
+                                                            long long rows) {
+  constexpr int E = padded_d<D>() / 32;
+  const int lane = threadIdx.x & 31;
+  for (long long r = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)); r < rows;
+       r += static_cast<long long>(gridDim.x) * 8) {
+    float e1 = 0.f, e2 = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+      if (col_ok<D>(lane, e)) {
+        const long long x = r * D + lane + 32 * e;
+        e1 = fmaf(dto[x], o[x], e1);
+        e2 = fmaf(dO[x], o[x], fmaf(dto[x], to[x], e2));
+      }
+    e1 = warp_sum(e1);
+    e2 = warp_sum(e2);
+    if (lane == 0) {
+      eps[r] = e1;
+      delta2[r] = e2;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kF32Warps * 32) f32_jvp_dq_kernel(F32JvpPtrs P, BwdArgs a) {
+  constexpr int DP = padded_d<D>();
+  constexpr int E = DP / 32;
+  __shared__ float sK[kF32Tile * DP], sTK[kF32Tile * DP], sV[kF32Tile * DP], sTV[kF32Tile * DP];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int i = blockIdx.y * kF32Warps + warp;
+  const bool live = i < a.M;
+  const size_t qoff = (static_cast<size_t>(bh) * a.M + (live ? i : 0)) * D;
+  const size_t koff = static_cast<size_t>(bh) * a.N * D;
+  float qr[E], tqr[E], dor[E], dtor[E], g[E];
+  load_row<E, D>(qr, P.q + qoff, lane);
+  load_row<E, D>(tqr, P.tq + qoff, lane);
+  load_row<E, D>(dor, P.dO + qoff, lane);
+  load_row<E, D>(dtor, P.dtO + qoff, lane);
+#pragma unroll
+  for (int e = 0; e < E; ++e) g[e] = 0.f;
+  const size_t ri = static_cast<size_t>(bh) * a.M + (live ? i : 0);
+  const float L = live ? a.lse[ri] : 0.f, mu = live ? a.mu[ri] : 0.f;
+  const float eps = live ? a.eps[ri] : 0.f, d2 = live ? a.delta[ri] : 0.f;
+  int hi = a.N;
+  if (a.causal) {
+    const int last_row = min(a.M - 1, static_cast<int>(blockIdx.y) * kF32Warps + kF32Warps - 1);
+    hi = max(0, min(a.N, last_row + a.P_SEQ + 1));
+  }
+  const int lim = a.causal ? min(a.N - 1, i + a.P_SEQ) : a.N - 1;
+  for (int j0 = 0; j0 < hi; j0 += kF32Tile) {
+    __syncthreads();
+    stage<D>(sK, P.k + koff, j0, a.N);
+    stage<D>(sTK, P.tk + koff, j0, a.N);
+    stage<D>(sV, P.v + koff, j0, a.N);
+    stage<D>(sTV, P.tv + koff, j0, a.N);
+    __syncthreads();
+    if (!live) continue;
+    const int jn = min(kF32Tile, lim - j0 + 1);
+    for (int jj = 0; jj < jn; ++jj) {
+      const float* kr = sK + jj * DP;
+      const float* tkr = sTK + jj * DP;
+      const float p = expf(dot_lane<E>(qr, kr, lane) * a.sm_scale - L);
+      const float t = a.sm_scale * (dot_lane<E>(tqr, kr, lane) + dot_lane<E>(qr, tkr, lane)) - mu;
+      const float dtp = dot_lane<E>(dtor, sV + jj * DP, lane);
+      const float dpa = dot_lane<E>(dor, sV + jj * DP, lane) + dot_lane<E>(dtor, sTV + jj * DP, lane);
+      const float dT = p * (dtp - eps);
+      const float dS = fmaf(t, dT, p * (dpa - d2));
+#pragma unroll
+      for (int e = 0; e < E; ++e) g[e] = fmaf(dS, kr[lane + 32 * e], fmaf(dT, tkr[lane + 32 * e], g[e]));
+    }
+  }
+  if (!live) return;
+  store_row<E, D>(reinterpret_cast<float*>(a.dq) + qoff, g, a.sm_scale, lane);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kF32Warps * 32) f32_jvp_dkdv_kernel(F32JvpPtrs P, BwdArgs a) {
+  constexpr int DP = padded_d<D>();
+  constexpr int E = DP / 32;
+  __shared__ float sQ[kF32Tile * DP], sTQ[kF32Tile * DP], sDO[kF32Tile * DP], sDTO[kF32Tile * DP];
+  __shared__ float sL[kF32Tile], sMu[kF32Tile], sEps[kF32Tile], sD2[kF32Tile];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int j = blockIdx.y * kF32Warps + warp;
+  const bool live = j < a.N;
+  const size_t koff = (static_cast<size_t>(bh) * a.N + (live ? j : 0)) * D;
+  const size_t qoff = static_cast<size_t>(bh) * a.M * D;
+  float kr[E], tkr[E], vr[E], tvr[E], gk[E], gv[E];
+  load_row<E, D>(kr, P.k + koff, lane);
+  load_row<E, D>(tkr, P.tk + koff, lane);
+  load_row<E, D>(vr, P.v + koff, lane);
+  load_row<E, D>(tvr, P.tv + koff, lane);
+#pragma unroll
+  for (int e = 0; e < E; ++e) gk[e] = gv[e] = 0.f;
+  int lo = 0;
+  if (a.causal) lo = max(0, static_cast<int>(blockIdx.y) * kF32Warps - a.P_SEQ);
+  const int first = a.causal ? max(0, j - a.P_SEQ) : 0;
+  for (int i0 = (lo / kF32Tile) * kF32Tile; i0 < a.M; i0 += kF32Tile) {
+    __syncthreads();
+    stage<D>(sQ, P.q + qoff, i0, a.M);
+    stage<D>(sTQ, P.tq + qoff, i0, a.M);
+    stage<D>(sDO, P.dO + qoff, i0, a.M);
+    stage<D>(sDTO, P.dtO + qoff, i0, a.M);
+    for (int r = threadIdx.x; r < kF32Tile; r += blockDim.x) {
+      const bool in = i0 + r < a.M;
+      const size_t g = static_cast<size_t>(bh) * a.M + (in ? i0 + r : 0);
+      sL[r] = in ? a.lse[g] : INFINITY;
+      sMu[r] = in ? a.mu[g] : 0.f;
+      sEps[r] = in ? a.eps[g] : 0.f;
+      sD2[r] = in ? a.delta[g] : 0.f;
+    }
+    __syncthreads();
+    if (!live) continue;
+    const int ib = max(0, first - i0);
+    const int ie = min(kF32Tile, a.M - i0);
+    for (int ii = ib; ii < ie; ++ii) {
+      const float* qr = sQ + ii * DP;
+      const float* tqr = sTQ + ii * DP;
+      const float* dor = sDO + ii * DP;
+      const float* dtor = sDTO + ii * DP;
+      const float p = expf(dot_lane<E>(kr, qr, lane) * a.sm_scale - sL[ii]);
+      const float t = a.sm_scale * (dot_lane<E>(kr, tqr, lane) + dot_lane<E>(tkr, qr, lane)) - sMu[ii];
+      const float dtp = dot_lane<E>(vr, dtor, lane);
+      const float dpa = dot_lane<E>(vr, dor, lane) + dot_lane<E>(tvr, dtor, lane);
+      const float dT = p * (dtp - sEps[ii]);
+      const float dS = fmaf(t, dT, p * (dpa - sD2[ii]));
+      const float pt = p * t;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        gv[e] = fmaf(p, dor[lane + 32 * e], fmaf(pt, dtor[lane + 32 * e], gv[e]));
+        gk[e] = fmaf(dS, qr[lane + 32 * e], fmaf(dT, tqr[lane + 32 * e], gk[e]));
+      }
+    }
+  }
+  if (!live) return;
+  store_row<E, D>(reinterpret_cast<float*>(a.dv) + koff, gv, 1.f, lane);
+  store_row<E, D>(reinterpret_cast<float*>(a.dk) + koff, gk, a.sm_scale, lane);
+}
+
 // ---------------------------------------------------------------- host side
 template <int MODE, int D>
 static cudaError_t f32_fwd_t(const F32Ptrs& p, const FwdArgs& a, cudaStream_t s) {
@@ -346,6 +493,38 @@ cudaError_t launch_f32_bwd(int mode, int D, const F32Ptrs& p, const BwdArgs& a, 
   if (mode == kStd && D == 128) return f32_bwd_t<kStd, 128>(p, a, s);
   if (mode == kPiecewise && D == 64) return f32_bwd_t<kPiecewise, 64>(p, a, s);
   if (mode == kPiecewise && D == 128) return f32_bwd_t<kPiecewise, 128>(p, a, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_f32_jvp_delta(int D, const float* o, const float* dO, const float* to, const float* dto,
+                                 float* eps, float* delta2, long long rows, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  long long blocks = (rows + 7) / 8;
+  if (blocks > 65535ll * 8) blocks = 65535ll * 8;
+  if (D == 16) f32_jvp_delta_kernel<16><<<blocks, 256, 0, s>>>(o, dO, to, dto, eps, delta2, rows);
+  else if (D == 32) f32_jvp_delta_kernel<32><<<blocks, 256, 0, s>>>(o, dO, to, dto, eps, delta2, rows);
+  else if (D == 64) f32_jvp_delta_kernel<64><<<blocks, 256, 0, s>>>(o, dO, to, dto, eps, delta2, rows);
+  else if (D == 128) f32_jvp_delta_kernel<128><<<blocks, 256, 0, s>>>(o, dO, to, dto, eps, delta2, rows);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t f32_jvp_bwd_t(const F32JvpPtrs& p, const BwdArgs& a, cudaStream_t s) {
+  dim3 gq(a.BH, (a.M + kF32Warps - 1) / kF32Warps);
+  f32_jvp_dq_kernel<D><<<gq, kF32Warps * 32, 0, s>>>(p, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 gk(a.BH, (a.N + kF32Warps - 1) / kF32Warps);
+  f32_jvp_dkdv_kernel<D><<<gk, kF32Warps * 32, 0, s>>>(p, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_f32_jvp_bwd(int D, const F32JvpPtrs& p, const BwdArgs& a, cudaStream_t s) {
+  if (D == 16) return f32_jvp_bwd_t<16>(p, a, s);
+  if (D == 32) return f32_jvp_bwd_t<32>(p, a, s);
+  if (D == 64) return f32_jvp_bwd_t<64>(p, a, s);
+  if (D == 128) return f32_jvp_bwd_t<128>(p, a, s);
   return cudaErrorInvalidValue;
 }
 

@@ -30,6 +30,18 @@ cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& maps, con
                             cudaStream_t s);
 cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& maps, const BwdArgs& a, cudaStream_t s);
 
+// Backward of the JVP.  Maps of the eight [BH, S, D] 16-bit inputs with
+// 128-row boxes (stationary tiles) and with 64-row boxes (streamed steps).
+struct JvpBwdMaps {
+  CUtensorMap q128, tq128, do128, dto128, k128, tk128, v128, tv128;
+  CUtensorMap q64, tq64, do64, dto64, k64, tk64, v64, tv64;
+};
+// eps_i = <dtO_i, O_i>, delta2_i = <dO_i, O_i> + <dtO_i, tO_i> for BH*M rows.
+cudaError_t launch_jvp_delta(bool bf16, int D, const void* o, const void* dO, const void* to, const void* dto,
+                             float* eps, float* delta2, long long rows, cudaStream_t s);
+// keys = true: dK, dV (a.dk, a.dv); false: dQ (a.dq).  a.delta = delta2.
+cudaError_t launch_bwd_jvp(bool keys, bool bf16, int D, const JvpBwdMaps& maps, const BwdArgs& a, cudaStream_t s);
+
 // Fills O = 0, L = -inf (rows that see no key) for BH*M rows of D elements
 // of `esize` bytes.
 cudaError_t launch_empty_rows(int esize, int D, void* o, float* lse, void* to, long long rows, cudaStream_t s);
@@ -44,6 +56,13 @@ cudaError_t launch_f32_fwd(int mode, int D, const F32Ptrs& p, const FwdArgs& a, 
 cudaError_t launch_f32_delta(int D, const float* o, const float* dO, float* delta, long long rows,
                              cudaStream_t s);
 cudaError_t launch_f32_bwd(int mode, int D, const F32Ptrs& p, const BwdArgs& a, cudaStream_t s);
+// Backward of the JVP in fp32: dq, dk, dv from q, k, v, tq, tk, tv, dO, dtO.
+struct F32JvpPtrs {
+  const float *q, *k, *v, *tq, *tk, *tv, *dO, *dtO;
+};
+cudaError_t launch_f32_jvp_delta(int D, const float* o, const float* dO, const float* to, const float* dto,
+                                 float* eps, float* delta2, long long rows, cudaStream_t s);
+cudaError_t launch_f32_jvp_bwd(int D, const F32JvpPtrs& p, const BwdArgs& a, cudaStream_t s);
 
 // Merge of two partial attention states (forward and backward); dtype 0 =
 // fp16, 1 = bf16, 2 = fp32.  dl may be null (zero).
