@@ -297,6 +297,52 @@ def fp8_measure(ta, torch, si, dev, stream, w, bf16_peak, iters=10):
             "workload": "e5m2 forward, B1 H32 M=N=8192 D128 causal (L2 flushed before each timed launch)"}
 
 
+def jvp_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
+    """Times the JVP forward (attn_fwd_jvp with tL) and its backward
+    (attn_bwd_jvp) on the JVP workload's shape, [2, 8, 1024, 64] fp16, causal
+    and not, outside the step's timed region; L2 is flushed before each timed
+    call (the inputs, 2 MB a tensor, fit in it).  Algorithmic FLOPs: the JVP
+    forward is 3x the primal forward (6 matmul-equivalents of 2 M N D), the
+    backward of the JVP 15 matmul-equivalents (S, T, dtO V^T, dO V^T + dtO tV^T
+    and the nine gradient products), i.e. 7.5x the primal forward."""
+    B, H, M, D = 2, 8, 1024, 64
+    names = ("q", "k", "v", "tq", "tk", "tv", "do", "dto")
+    g = {n: t.to(dev) for n, t in si.attention_inputs(B, H, M, M, D, "f16", 4, names=names).items()}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {"workload": "JVP forward and its backward, B2 H8 M=N=1024 D64 fp16 (L2 flushed before each call)"}
+    for causal in (False, True):
+        fwd = lambda: ta.attn_fwd_jvp(*(g[n] for n in names[:6]), causal=causal, with_tlse=True, stream=stream)
+        o, lse, to, tlse = fwd()
+        ws = torch.empty(max(16, ta.load().attn_bwd_jvp_workspace_bytes(B, H, M, M, D, 0)), device=dev,
+                         dtype=torch.uint8)
+        bwd = lambda: ta.attn_bwd_jvp(*(g[n] for n in names[:6]), o, lse, to, tlse, g["do"], g["dto"],
+                                      causal=causal, ws=ws, stream=stream)
+        for _ in range(3):
+            fwd()
+            bwd()
+        torch.cuda.synchronize(dev)
+        res = {}
+        for label, fn in (("fwd", fwd), ("bwd", bwd)):
+            ms = 0.0
+            with torch.cuda.stream(stream):
+                for _ in range(iters):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+                    torch.cuda.synchronize(dev)
+                    ms += e0.elapsed_time(e1) / iters
+            res[label] = ms
+        f = flops_fwd(B, H, M, M, D, causal)
+        tf_f = 3 * f / (res["fwd"] * 1e-3) / 1e12
+        tf_b = 7.5 * f / (res["bwd"] * 1e-3) / 1e12
+        out["causal" if causal else "noncausal"] = {
+            "fwd_ms": res["fwd"], "bwd_ms": res["bwd"], "fwd_tflops": tf_f, "bwd_tflops": tf_b,
+            "fwd_frac": tf_f / bf16_peak, "bwd_frac": tf_b / bf16_peak}
+    return out
+
+
 # -------------------------------------------------------------- GPU arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -418,6 +464,7 @@ def run_ours(args, rank, world, local_rank):
 
     merge = merge_measure(ta, torch, dev, stream, o, lse, dq, g["do"], hbm_peak)
     fp8 = fp8_measure(ta, torch, si, dev, stream, w, bf16_peak)
+    jvp = jvp_measure(ta, torch, si, dev, stream, bf16_peak)
     if ta.sync_status(stream) != "TA_OK":
         raise RuntimeError("device error word set in the merge measurement")
 
@@ -450,6 +497,7 @@ def run_ours(args, rank, world, local_rank):
         "kernels": kernels,
         "merge": merge,
         "fp8_fwd": fp8,
+        "jvp": jvp,
         "cpu_baseline": {"value": cpu_f / cpu_secs / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),
                          "kind": "oracle",
                          "sample": "%d of 32 heads (b=0, h<%d), fwd+bwd, fp64 numpy, %.1f s"
