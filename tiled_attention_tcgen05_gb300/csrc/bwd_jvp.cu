@@ -11,9 +11,10 @@
 //   tP  = P o (T - mu),
 //   dQ = sm_scale (dS K + dT tK),  dK = sm_scale (dS^T Q + dT^T tQ),
 //   dV = P^T dO + tP^T dtO.
-// The tangents' own gradients (dtq, dtk, dtv) are the plain backward with dO
-// replaced by dtO (tO is linear in the tangents) and are computed by the
-// plain backward kernels.
+// The tangents' own gradients are the plain backward with dO replaced by
+// dtO (tO is linear in the tangents): dtq = sm_scale dT K, dtk = sm_scale
+// dT^T Q, dtv = P^T dtO.  At D <= 64 (TANG) these kernels accumulate them
+// too; at D = 128 TMEM has no room and the plain backward kernels run them.
 //
 // Two kernels from one template, each one CTA per 128-row stationary tile,
 // 320 threads:
@@ -28,12 +29,14 @@
 //              lane issues each K-loop of MMAs as a single asm block).
 //
 // TMEM (512 columns): four fp32 score buffers of 64 columns (S, T, dtP, dPa)
-// and the fp32 accumulators from column 256 (dV, dK or dQ).  The 16-bit MMA
-// operands are written back in place: a thread packs its 32 columns into the
-// first 16 columns of its own 32-column slice, so K-step kk (16 streamed
-// rows) of an operand sits at column 32 (kk / 2) + 8 (kk % 2) of its buffer.
-// Operands: KEYS keeps P, tP, dS, dT in the S, T, dtP, dPa buffers; the dQ
-// kernel keeps dS, dT in the S, T buffers.
+// and the fp32 accumulators from column 256 (dV, dK[, dtV, dtK] or
+// dQ[, dtQ]).  The 16-bit MMA operands are written back in place: a thread
+// packs its 32 columns into the first 16 columns of its own 32-column slice,
+// so K-step kk (16 streamed rows) of an operand sits at column
+// 32 (kk / 2) + 8 (kk % 2) of its buffer.
+// Operands: P and tP (KEYS only) in the S and T buffers, dS and dT in the
+// dtP and dPa buffers.  The next step's S and T go into their buffers as
+// soon as those are free, under the current step's element-wise work.
 #include "bwd_common.cuh"
 #include "common.cuh"
 #include "launch.h"
@@ -61,6 +64,10 @@ struct JvpBwdCfg {
   static_assert(STAGES >= 1, "tiles do not fit in shared memory");
   static_assert(COL_ACC + 2 * D <= 512, "TMEM overflow");
 };
+
+// The tangents' gradients fit beside the others (4 D accumulator columns).
+template <int D>
+constexpr bool jvp_tangents_fit() { return 256 + 4 * D <= 512; }
 
 template <int D>
 __device__ __forceinline__ void jvp_load(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh,
@@ -108,7 +115,7 @@ __device__ __forceinline__ void pack16(const float* x, uint32_t (&o)[8]) {
   for (int e = 0; e < 8; ++e) o[e] = pack2<BF>(x[2 * e], x[2 * e + 1]);
 }
 
-template <typename T, bool KEYS, int D>
+template <typename T, bool KEYS, int D, bool TANG>
 __global__ void __launch_bounds__(kJvpThreads, 1)
     attn_bwd_jvp_kernel(const __grid_constant__ CUtensorMap tx0, const __grid_constant__ CUtensorMap tx1,
                         const __grid_constant__ CUtensorMap tx2, const __grid_constant__ CUtensorMap tx3,
@@ -118,10 +125,11 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
   using C = JvpBwdCfg<D>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
+  static_assert(!TANG || jvp_tangents_fit<D>(), "no TMEM room for the tangents' gradients");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_x, bar_y[STAGES], bar_yempty[STAGES];
-  __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_p, bar_ops, bar_done;
+  __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_p, bar_sfree, bar_ops, bar_done;
   // KEYS: per streamed query, L log2(e), mu, eps, delta2
   __shared__ __align__(16) float sRow[KEYS ? STAGES : 1][4][kJR];
   __shared__ uint32_t tmem_slot;
@@ -163,6 +171,7 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
     mbar_init(&bar_s, 1);
     mbar_init(&bar_dp, 1);
     mbar_init(&bar_p, kJvpRowWarps);
+    mbar_init(&bar_sfree, kJvpRowWarps);
     mbar_init(&bar_ops, kJvpRowWarps);
     mbar_init(&bar_done, 1);
     fence_mbar_init();
@@ -231,39 +240,74 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
       constexpr uint32_t idesc_g = idesc_f16(kBM, D, BF, false, true);     // M = stationary, N = D
       const uint32_t xs0 = smem_u32(sX(0)), xs1 = smem_u32(sX(1)), xs2 = smem_u32(sX(2)), xs3 = smem_u32(sX(3));
       bool ok = warp_wait(&bar_x, 0, ctl, kErrTimeoutTma);
-      for (int u = 0; ok && u < nu; ++u) {
-        const int st = u % STAGES;
-        if (!(ok = warp_wait(&bar_y[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
-        tc_fence_after();
-        const uint32_t ys0 = smem_u32(sY(st, 0)), ys1 = smem_u32(sY(st, 1)), ys2 = smem_u32(sY(st, 2)),
-                       ys3 = smem_u32(sY(st, 3));
-        const uint32_t first = u > 0 ? 1u : 0u;
-        // S = X0 Y0^T; T = X1 Y0^T + X0 Y1^T (K tQ^T + tK Q^T, or tQ K^T + Q tK^T)
-        mma_xyT<D>(tmem + C::COL_S, xs0, ys0, idesc_s, 0u);
-        mma_xyT<D>(tmem + C::COL_T, xs1, ys0, idesc_s, 0u);
-        mma_xyT<D>(tmem + C::COL_T, xs0, ys1, idesc_s, 1u);
+      auto ys = [&](int st, int i) { return smem_u32(sY(st, i)); };
+      // S = X0 Y0^T; T = X1 Y0^T + X0 Y1^T (K Q^T, tK Q^T + K tQ^T, or Q K^T, tQ K^T + Q tK^T)
+      auto scores_st = [&](int st) {
+        mma_xyT<D>(tmem + C::COL_S, xs0, ys(st, 0), idesc_s, 0u);
+        mma_xyT<D>(tmem + C::COL_T, xs1, ys(st, 0), idesc_s, 0u);
+        mma_xyT<D>(tmem + C::COL_T, xs0, ys(st, 1), idesc_s, 1u);
         commit_el(&bar_s);
-        if constexpr (KEYS) mma_xyT<D>(tmem + C::COL_DTP, xs2, ys3, idesc_s, 0u);  // dtP^T = V dtO^T
-        else mma_xyT<D>(tmem + C::COL_DTP, xs3, ys2, idesc_s, 0u);                 // dtP = dtO V^T
-        mma_xyT<D>(tmem + C::COL_DPA, xs2, ys2, idesc_s, 0u);  // dPa = dO V^T + dtO tV^T (or transposed)
-        mma_xyT<D>(tmem + C::COL_DPA, xs3, ys3, idesc_s, 1u);
+      };
+      // dtP = V dtO^T (or dtO V^T); dPa = V dO^T + tV dtO^T (or dO V^T + dtO tV^T)
+      auto scores_dp = [&](int st) {
+        if constexpr (KEYS) mma_xyT<D>(tmem + C::COL_DTP, xs2, ys(st, 3), idesc_s, 0u);
+        else mma_xyT<D>(tmem + C::COL_DTP, xs3, ys(st, 2), idesc_s, 0u);
+        mma_xyT<D>(tmem + C::COL_DPA, xs2, ys(st, 2), idesc_s, 0u);
+        mma_xyT<D>(tmem + C::COL_DPA, xs3, ys(st, 3), idesc_s, 1u);
         commit_el(&bar_dp);
+      };
+      // With two or more stages the next step's S and T are issued as soon as
+      // their buffers are free (after dV's MMAs read P and tP, or once the dQ
+      // kernel's threads hold S and T in registers), so they run under the
+      // element-wise phase; with one stage its data arrives only after the
+      // current step's last MMA.
+      constexpr bool kEarly = STAGES >= 2;
+      if (ok) ok = warp_wait(&bar_y[0], 0, ctl, kErrTimeoutTma);
+      if (ok) {
+        tc_fence_after();
+        scores_st(0);
+        scores_dp(0);
+      }
+      for (int u = 0; ok && u < nu; ++u) {
+        const int st = u % STAGES, st1 = (u + 1) % STAGES;
+        const bool more = u + 1 < nu;
+        const uint32_t first = u > 0 ? 1u : 0u;
         if constexpr (KEYS) {
           if (!(ok = warp_wait(&bar_p, u & 1, ctl, kErrTimeoutSoftmax))) break;
           tc_fence_after();
-          mma_aY<D>(tmem + C::COL_ACC, tmem + C::COL_S, ys2, idesc_g, first);  // dV += P^T dO
-          mma_aY<D>(tmem + C::COL_ACC, tmem + C::COL_T, ys3, idesc_g, 1u);     // dV += tP^T dtO
+          mma_aY<D>(tmem + C::COL_ACC, tmem + C::COL_S, ys(st, 2), idesc_g, first);  // dV += P^T dO
+          mma_aY<D>(tmem + C::COL_ACC, tmem + C::COL_T, ys(st, 3), idesc_g, 1u);     // dV += tP^T dtO
+          if constexpr (TANG) mma_aY<D>(tmem + C::COL_ACC + 2 * D, tmem + C::COL_S, ys(st, 3), idesc_g, first);  // dtV
+        } else if constexpr (kEarly) {
+          if (!(ok = warp_wait(&bar_sfree, u & 1, ctl, kErrTimeoutSoftmax))) break;
+          tc_fence_after();
+        }
+        if (kEarly && more) {
+          if (!(ok = warp_wait(&bar_y[st1], ((u + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+          tc_fence_after();
+          scores_st(st1);
         }
         if (!(ok = warp_wait(&bar_ops, u & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
+        // dS and dT sit in the dtP and dPa buffers
         if constexpr (KEYS) {
-          mma_aY<D>(tmem + C::COL_ACC + D, tmem + C::COL_DTP, ys0, idesc_g, first);  // dK += dS^T Q
-          mma_aY<D>(tmem + C::COL_ACC + D, tmem + C::COL_DPA, ys1, idesc_g, 1u);     // dK += dT^T tQ
+          mma_aY<D>(tmem + C::COL_ACC + D, tmem + C::COL_DTP, ys(st, 0), idesc_g, first);  // dK += dS^T Q
+          mma_aY<D>(tmem + C::COL_ACC + D, tmem + C::COL_DPA, ys(st, 1), idesc_g, 1u);     // dK += dT^T tQ
+          if constexpr (TANG) mma_aY<D>(tmem + C::COL_ACC + 3 * D, tmem + C::COL_DPA, ys(st, 0), idesc_g, first);  // dtK
         } else {
-          mma_aY<D>(tmem + C::COL_ACC, tmem + C::COL_S, ys0, idesc_g, first);  // dQ += dS K
-          mma_aY<D>(tmem + C::COL_ACC, tmem + C::COL_T, ys1, idesc_g, 1u);     // dQ += dT tK
+          mma_aY<D>(tmem + C::COL_ACC, tmem + C::COL_DTP, ys(st, 0), idesc_g, first);  // dQ += dS K
+          mma_aY<D>(tmem + C::COL_ACC, tmem + C::COL_DPA, ys(st, 1), idesc_g, 1u);     // dQ += dT tK
+          if constexpr (TANG) mma_aY<D>(tmem + C::COL_ACC + D, tmem + C::COL_DPA, ys(st, 0), idesc_g, first);  // dtQ
         }
         commit_el(&bar_yempty[st]);
+        if (more) {
+          if (!kEarly) {
+            if (!(ok = warp_wait(&bar_y[st1], ((u + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+            tc_fence_after();
+            scores_st(st1);
+          }
+          scores_dp(st1);
+        }
       }
       if (ok) commit_el(&bar_done);
     }
@@ -297,6 +341,11 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
       tmem_ld_x32(lane_addr + C::COL_T + 32 * h, tr);
       tmem_ld_wait(sr);
       tmem_ld_wait(tr);
+      if constexpr (!KEYS) {  // S and T are in registers: their buffers may take the next step's
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_sfree);
+      }
       float p[32], tm[32];  // P and T - mu of the thread's 32 columns
       if constexpr (KEYS) {
         const float4* L4 = reinterpret_cast<const float4*>(&sRow[st][0][32 * h]);
@@ -383,8 +432,8 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
         uint32_t pks[8], pkt[8];
         pack16<BF>(dS, pks);
         pack16<BF>(dT, pkt);
-        tmem_st_x8(lane_addr + (KEYS ? C::COL_DTP : C::COL_S) + 32 * h + 8 * cc, pks);
-        tmem_st_x8(lane_addr + (KEYS ? C::COL_DPA : C::COL_T) + 32 * h + 8 * cc, pkt);
+        tmem_st_x8(lane_addr + C::COL_DTP + 32 * h + 8 * cc, pks);
+        tmem_st_x8(lane_addr + C::COL_DPA + 32 * h + 8 * cc, pkt);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -408,10 +457,26 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
         zero_half<T, D>(dv, dc, args.dg);
         zero_half<T, D>(dk, dc, args.dg);
       }
+      if constexpr (TANG) {
+        T* dtv = reinterpret_cast<T*>(args.dtv) + off;
+        T* dtk = reinterpret_cast<T*>(args.dtk) + off;
+        if (live) {
+          epilogue_half<T, D>(lane_addr + C::COL_ACC + 2 * D, dtv, dc, st_row, true, 1.f, args.dg);
+          epilogue_half<T, D>(lane_addr + C::COL_ACC + 3 * D, dtk, dc, st_row, true, args.sm_scale, args.dg);
+        } else if (st_row) {
+          zero_half<T, D>(dtv, dc, args.dg);
+          zero_half<T, D>(dtk, dc, args.dg);
+        }
+      }
     } else {
       T* dq = reinterpret_cast<T*>(args.dq) + off;
       if (live) epilogue_half<T, D>(lane_addr + C::COL_ACC, dq, dc, st_row, true, args.sm_scale, args.dg);
       else if (st_row) zero_half<T, D>(dq, dc, args.dg);
+      if constexpr (TANG) {
+        T* dtq = reinterpret_cast<T*>(args.dtq) + off;
+        if (live) epilogue_half<T, D>(lane_addr + C::COL_ACC + D, dtq, dc, st_row, true, args.sm_scale, args.dg);
+        else if (st_row) zero_half<T, D>(dtq, dc, args.dg);
+      }
     }
   }
 
@@ -424,7 +489,7 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
 template <typename T, bool KEYS, int D>
 static cudaError_t launch_jvp_bwd_t(const JvpBwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = JvpBwdCfg<D>;
-  auto kern = attn_bwd_jvp_kernel<T, KEYS, D>;
+  auto kern = attn_bwd_jvp_kernel<T, KEYS, D, jvp_tangents_fit<D>()>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -444,6 +509,8 @@ static cudaError_t launch_jvp_bwd_t(const JvpBwdMaps& m, const BwdArgs& a, cudaS
   }
   return cudaGetLastError();
 }
+
+bool bwd_jvp_has_tangents(int D) { return D == 64 ? jvp_tangents_fit<64>() : jvp_tangents_fit<128>(); }
 
 cudaError_t launch_bwd_jvp(bool keys, bool bf16, int D, const JvpBwdMaps& m, const BwdArgs& a, cudaStream_t s) {
 #define TA_JVP_BWD(K_, D_) \

@@ -48,6 +48,9 @@ struct BwdArgs {
   const float* delta;  // backward of the JVP: <dO, O> + <dtO, tO>
   const float* mu;     // backward of the JVP only: tL = rowsum(P o T)
   const float* eps;    // backward of the JVP only: <dtO, O>
+  void* dtq;           // backward of the JVP at D <= 64: the tangents' gradients
+  void* dtk;
+  void* dtv;
   int BH, M, N, P_SEQ;
   int causal;
   int w;

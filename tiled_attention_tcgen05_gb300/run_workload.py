@@ -5,8 +5,10 @@ number of steps: the command line used for profiling (ncu) and timing runs.
 
 Workloads (synth_inputs.WORKLOADS): 1 fwd+bwd fp16 B1 H2 S128 D64 non-causal;
 2 fwd+bwd bf16 causal B4 H16 S2048 D128; 3 fwd+bwd bf16 causal B1 H32 S8192
-D128; 4 fwd+JVP fp16 B2 H8 S1024 D64 (--causal 0/1); 5 piecewise fwd+bwd bf16
-causal B2 H16 S4096 D64 w=512.  Prints the mean milliseconds per step.
+D128; 4 JVP forward (with tL) and the backward of the JVP, fp16 B2 H8 S1024
+D64 (--causal 0/1); 5 piecewise fwd+bwd bf16 causal B2 H16 S4096 D64 w=512.
+--shape B,H,S,D replaces the workload's sizes.  Prints the mean milliseconds
+per step.
 """
 from __future__ import annotations
 
@@ -22,19 +24,25 @@ import synth_inputs as si  # noqa: E402
 import tiled_attention_tcgen05_gb300 as ta  # noqa: E402
 
 
-def make_step(wid: int, causal_override=None):
+def make_step(wid: int, causal_override=None, shape=None):
     w = si.WORKLOADS[wid]
     B, H, M, N, D, dt = w["B"], w["H"], w["M"], w["N"], w["D"], w["dtype"]
     causal = w["causal"] if causal_override is None else bool(causal_override)
+    if shape is not None:
+        B, H, M, D = shape
+        N = M
     if w["mode"] == "jvp":
-        names = ("q", "k", "v", "tq", "tk", "tv")
+        names = ("q", "k", "v", "tq", "tk", "tv", "do", "dto")
     elif w["mode"] == "piecewise":
         names = ("q1", "k1", "q2", "k2", "v", "do")
     else:
         names = ("q", "k", "v", "do")
     x = {n: t.cuda() for n, t in si.attention_inputs(B, H, M, N, D, dt, wid, names=names).items()}
     if w["mode"] == "jvp":
-        return lambda: ta.attn_fwd_jvp(*(x[n] for n in names), causal=bool(causal))
+        def jvp_step():
+            o, lse, to, tlse = ta.attn_fwd_jvp(*(x[n] for n in names[:6]), causal=bool(causal), with_tlse=True)
+            ta.attn_bwd_jvp(*(x[n] for n in names[:6]), o, lse, to, tlse, x["do"], x["dto"], causal=bool(causal))
+        return jvp_step
     if w["mode"] == "piecewise":
         def step():
             o, lse = ta.piecewise_fwd(x["q1"], x["k1"], x["q2"], x["k2"], x["v"], w["w"], causal)
@@ -53,9 +61,11 @@ def main():
     ap.add_argument("--steps", type=int, default=2)
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--causal", type=int, default=None)
+    ap.add_argument("--shape", type=str, default=None, help="B,H,S,D instead of the workload's own (M = N = S)")
     a = ap.parse_args()
     ta.load()
-    step = make_step(a.workload, a.causal)
+    shape = tuple(int(x) for x in a.shape.split(",")) if a.shape else None
+    step = make_step(a.workload, a.causal, shape)
     for _ in range(a.warmup):
         step()
     torch.cuda.synchronize()
