@@ -78,9 +78,9 @@ def test_backward_workspace_and_validation(lib):
     assert st == INVALID  # null workspace
     st = lib.attn_bwd(*p[:9], vp(0x2008), 1024, 1, 1, 128, 128, 64, BF16, 1, -1.0, vp(0))
     assert st == ALIGNMENT
-    # piecewise backward keeps three D-wide accumulators in TMEM: D = 64 only
+    # a head size outside {16, 32, 64, 128} is refused before any launch
     q = [vp(16 * (i + 1)) for i in range(14)]
-    st = lib.piecewise_bwd(*q, 1 << 20, 1, 1, 128, 128, 128, BF16, 1, -1.0, 64, vp(0))
+    st = lib.piecewise_bwd(*q, 1 << 20, 1, 1, 128, 128, 96, BF16, 1, -1.0, 64, vp(0))
     assert st == UNSUPPORTED
 
 

@@ -611,9 +611,6 @@ ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const vo
   Problem p;
   ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
   if (st != TA_OK) return st;
-  // TMEM holds S, dP, dV, dK1 and dK2 of a 128-key tile only for D <= 64
-  // (the fp32 mode has no such limit).
-  if (D > 64 && dt != TA_F32) return TA_ERR_UNSUPPORTED;
   if (p.BH == 0 || (M == 0 && N == 0)) return TA_OK;
   if (M == 0) st = check_ptrs({dk1, dk2, dv});
   else if (N == 0) st = check_ptrs({o, dO, dq1, dq2, ws});

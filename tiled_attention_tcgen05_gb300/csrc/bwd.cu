@@ -98,7 +98,10 @@ __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_
 // ======================================================================
 //                        dK, dV (key-stationary)
 // ======================================================================
-template <int MODE, int D>
+// PART selects the outputs of the key-stationary kernel: -1 all of them; for
+// piecewise D = 128, where TMEM cannot hold dV, dK1 and dK2 beside the score
+// buffers, two launches: 0 = dV and dK1, 1 = dK2 alone.
+template <int MODE, int D, int PART = -1>
 struct DkdvCfg {
   static constexpr int BLK = kBM * 128;
   static constexpr int TILE = (D / 64) * BLK;
@@ -109,18 +112,21 @@ struct DkdvCfg {
   static constexpr int ST_FIT = (kSmemMax - RESERVE - NRES * TILE) / STAGE;
   static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
   static constexpr int SMEM = NRES * TILE + STAGES * STAGE + 1024;
-  static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D, COL_DK2 = 256 + 2 * D;
+  static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D;
+  static constexpr uint32_t COL_DK2 = (PART == 1) ? 256 : 256 + 2 * D;
   static_assert(STAGES >= 1, "tile does not fit in shared memory");
-  static_assert(COL_DK2 + (MODE == kPiecewise ? D : 0) <= 512, "TMEM overflow");
+  static_assert((PART == 1 ? 256 + D : PART == 0 ? 256 + 2 * D : COL_DK2 + (MODE == kPiecewise ? D : 0)) <= 512,
+                "TMEM overflow");
 };
 
-template <typename T, int MODE, int D>
+template <typename T, int MODE, int D, int PART>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
                          const BwdArgs args) {
-  using C = DkdvCfg<MODE, D>;
+  using C = DkdvCfg<MODE, D, PART>;
+  constexpr bool kDV = PART != 1, kDK1 = PART != 1, kDK2 = PART != 0;  // outputs of this launch
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
   constexpr bool PW = (MODE == kPiecewise);
@@ -264,20 +270,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         commit_el(&bar_dp);
         if (!(ok = warp_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_tY<D>(tmem + C::COL_DV, tmem + C::COL_A, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
+        if constexpr (kDV) mma_tY<D>(tmem + C::COL_DV, tmem + C::COL_A, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
         if constexpr (!PW) {
           mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, u > 0);  // dK += dS^T Q
         } else {
-          if (cls == kNearB) {
+          if ((cls & kNearB) && kDK1) {
             mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
             acc1 = true;
-          } else if (cls == kFarB) {
-            mma_tY<D>(tmem + C::COL_DK2, tmem + C::COL_B, smem_u32(sQ2(st)), idesc_g, acc2);
+          }
+          if ((cls & kFarB) && kDK2) {  // the far part of dS: COL_B when the whole tile is far
+            const uint32_t src = (cls == kFarB) ? C::COL_B : C::COL_A + 32;
+            mma_tY<D>(tmem + C::COL_DK2, tmem + src, smem_u32(sQ2(st)), idesc_g, acc2);
             acc2 = true;
-          } else {
-            mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
-            mma_tY<D>(tmem + C::COL_DK2, tmem + C::COL_A + 32, smem_u32(sQ2(st)), idesc_g, acc2);
-            acc1 = acc2 = true;
           }
         }
         commit_el(&bar_qempty[st]);
@@ -399,18 +403,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     T* dk = reinterpret_cast<T*>(args.dk) + off;
     const int dc = hc * (D / 2);  // this thread's half of the D columns
     if (live) {
-      epilogue_half<T, D>(lane_addr + C::COL_DV, dv, dc, st_row, true, 1.f, args.dg);
+      if constexpr (kDV) epilogue_half<T, D>(lane_addr + C::COL_DV, dv, dc, st_row, true, 1.f, args.dg);
       if constexpr (!PW) {
         epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, true, args.sm_scale, args.dg);
       } else {
         T* dk2 = reinterpret_cast<T*>(args.dk2) + off;
-        epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, touched1, args.sm_scale, args.dg);
-        epilogue_half<T, D>(lane_addr + C::COL_DK2, dk2, dc, st_row, touched2, args.sm_scale, args.dg);
+        if constexpr (kDK1)
+          epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, touched1, args.sm_scale, args.dg);
+        if constexpr (kDK2)
+          epilogue_half<T, D>(lane_addr + C::COL_DK2, dk2, dc, st_row, touched2, args.sm_scale, args.dg);
       }
     } else if (st_row) {
-      zero_half<T, D>(dv, dc, args.dg);
-      zero_half<T, D>(dk, dc, args.dg);
-      if constexpr (PW) zero_half<T, D>(reinterpret_cast<T*>(args.dk2) + off, dc, args.dg);
+      if constexpr (kDV) zero_half<T, D>(dv, dc, args.dg);
+      if constexpr (kDK1) zero_half<T, D>(dk, dc, args.dg);
+      if constexpr (PW && kDK2) zero_half<T, D>(reinterpret_cast<T*>(args.dk2) + off, dc, args.dg);
     }
   }
 
@@ -1346,10 +1352,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-template <typename T, int MODE, int D>
+template <typename T, int MODE, int D, int PART = -1>
 static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
-  using C = DkdvCfg<MODE, D>;
-  auto kern = attn_bwd_dkdv_kernel<T, MODE, D>;
+  using C = DkdvCfg<MODE, D, PART>;
+  auto kern = attn_bwd_dkdv_kernel<T, MODE, D, PART>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -1398,6 +1404,13 @@ cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& m, const 
   if (mode == kStd && D == 64) return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 64>(m, a, s) : launch_dkdv_std_t<__half, 64>(m, a, s);
   if (mode == kStd && D == 128) return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 128>(m, a, s) : launch_dkdv_std_t<__half, 128>(m, a, s);
   if (mode == kPiecewise && D == 64) return bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dkdv_t<__half, kPiecewise, 64>(m, a, s);
+  if (mode == kPiecewise && D == 128) {  // dV and dK1, then dK2
+    cudaError_t e = bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 128, 0>(m, a, s)
+                         : launch_dkdv_t<__half, kPiecewise, 128, 0>(m, a, s);
+    if (e != cudaSuccess) return e;
+    return bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 128, 1>(m, a, s)
+                : launch_dkdv_t<__half, kPiecewise, 128, 1>(m, a, s);
+  }
   return cudaErrorNotSupported;
 }
 
@@ -1421,6 +1434,7 @@ cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& m, const Bw
   if (mode == kStd && D == 64) return bf16 ? launch_dq_std_t<__nv_bfloat16, 64>(m, a, s) : launch_dq_std_t<__half, 64>(m, a, s);
   if (mode == kStd && D == 128) return bf16 ? launch_dq_std_t<__nv_bfloat16, 128>(m, a, s) : launch_dq_std_t<__half, 128>(m, a, s);
   if (mode == kPiecewise && D == 64) return bf16 ? launch_dq_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dq_t<__half, kPiecewise, 64>(m, a, s);
+  if (mode == kPiecewise && D == 128) return bf16 ? launch_dq_t<__nv_bfloat16, kPiecewise, 128>(m, a, s) : launch_dq_t<__half, kPiecewise, 128>(m, a, s);
   return cudaErrorNotSupported;
 }
 
