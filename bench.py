@@ -343,6 +343,49 @@ def jvp_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
     return out
 
 
+def configs_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
+    """Times one fwd+bwd step (forward then backward, inputs resident) on the
+    other workloads: 1 (B1 H2 S128 D64 fp16, non-causal), 2 (B4 H16 S2048 D128
+    bf16 causal) and 5 (piecewise, B2 H16 S4096 D64 bf16 causal, w = 512).
+    L2 is flushed before each timed step.  FLOPs are the standard count
+    (4 M N D per head forward, x 3.5 for forward + backward, x 0.5 causal); the
+    piecewise path's second score products on straddling tiles are overhead."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    for wid in (1, 2, 5):
+        w = si.WORKLOADS[wid]
+        B, H, M, N, D, causal = w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"]
+        pw = w["mode"] == "piecewise"
+        names = ("q1", "k1", "q2", "k2", "v", "do") if pw else ("q", "k", "v", "do")
+        g = {n: t.to(dev) for n, t in si.attention_inputs(B, H, M, N, D, w["dtype"], wid, names=names).items()}
+        if pw:
+            def fn():
+                o, lse = ta.piecewise_fwd(g["q1"], g["k1"], g["q2"], g["k2"], g["v"], w["w"], causal, stream=stream)
+                ta.piecewise_bwd(g["q1"], g["k1"], g["q2"], g["k2"], g["v"], o, lse, g["do"], w["w"], causal,
+                                 stream=stream)
+        else:
+            def fn():
+                o, lse = ta.attn_fwd(g["q"], g["k"], g["v"], causal, stream=stream)
+                ta.attn_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal, stream=stream)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        ms = 0.0
+        with torch.cuda.stream(stream):
+            for _ in range(iters):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ms += e0.elapsed_time(e1) / iters
+        f = flops_fwd(B, H, M, N, D, causal) * 3.5
+        tf = f / (ms * 1e-3) / 1e12
+        out[str(wid)] = {"workload": w["name"], "ms_per_step": ms, "tflops": tf, "frac": tf / bf16_peak}
+    return out
+
+
 # -------------------------------------------------------------- GPU arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -509,6 +552,7 @@ def run_ours(args, rank, world, local_rank):
     merge = merge_measure(ta, torch, dev, stream, o, lse, dq, g["do"], hbm_peak)
     fp8 = fp8_measure(ta, torch, si, dev, stream, w, bf16_peak)
     jvp = jvp_measure(ta, torch, si, dev, stream, bf16_peak)
+    other = configs_measure(ta, torch, si, dev, stream, bf16_peak)
     if ta.sync_status(stream) != "TA_OK":
         raise RuntimeError("device error word set in the merge measurement")
 
@@ -544,6 +588,7 @@ def run_ours(args, rank, world, local_rank):
         "merge": merge,
         "fp8_fwd": fp8,
         "jvp": jvp,
+        "other_workloads": other,
         "cpu_baseline": {"value": cpu_f / cpu_secs / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),
                          "kind": "oracle",
                          "sample": "%d of 32 heads (b=0, h<%d), fwd+bwd, fp64 numpy, %.1f s"

@@ -11,8 +11,9 @@
 //              issues each K-loop of MMAs as a single asm block).
 // Per key tile t:  S = Q K_t^T (tcgen05.mma, A and B from shared memory) ->
 // softmax writes P (16-bit, packed two per TMEM column) over S -> O += P V_t
-// with P read straight from TMEM.  Standard mode double-buffers S so the
-// next QK^T overlaps the current softmax.
+// with P read straight from TMEM.  The standard and piecewise modes
+// double-buffer S so the next QK^T overlaps the current softmax; a piecewise
+// tile that needs both score products puts S(q2, k2) in a third buffer.
 //
 // Page sources: "Triton fused attention tutorial, updated with JVP support",
 // _attn_fwd / _attn_fwd_inner (online exp2 softmax with running max and sum,
@@ -47,14 +48,18 @@ struct FwdCfg {
   static constexpr int RESERVE = 2048;    // alignment slack + static shared memory
   static constexpr int ST_FIT = (kSmemMax - RESERVE - NQ * TILE) / STAGE;
   static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
-  static constexpr int NBUF = (MODE == kStd) ? 2 : 1;
+  // Two S buffers let QK^T(t + 1) run before P V(t); that needs a second
+  // K/V stage (tile t + 1's keys arrive while tile t's values are in use).
+  static constexpr int NBUF = (MODE == kJvp || STAGES < 2) ? 1 : 2;
   static constexpr int SMEM = NQ * TILE + STAGES * STAGE + 1024;
-  static constexpr uint32_t COL_S0 = 0;    // S (buffer 0) | piecewise S(q1,k1) | jvp S
-  static constexpr uint32_t COL_S1 = 128;  // S (buffer 1) | piecewise S(q2,k2) | jvp T
+  static constexpr uint32_t COL_S0 = 0;    // S (buffer 0) | jvp S
+  static constexpr uint32_t COL_S1 = 128;  // S (buffer 1) | jvp T
   static constexpr uint32_t COL_O = 256;
   static constexpr uint32_t COL_U = 256 + D;  // jvp tangent accumulator
+  static constexpr uint32_t COL_X = 256 + D;  // piecewise: S(q2, k2) of a tile that needs both products
   static_assert(STAGES >= 1, "tile does not fit in shared memory");
   static_assert(COL_U + (MODE == kJvp ? D : 0) <= 512, "TMEM overflow");
+  static_assert(MODE != kPiecewise || COL_X + 128 <= 512, "TMEM overflow");
 };
 
 enum : int { kNear = 1, kFar = 2 };
@@ -279,8 +284,23 @@ __global__ void __launch_bounds__(192, 1)
           mma_qk<D>(tmem + (b ? C::COL_S1 : C::COL_S0), aQ, aK, idesc_qk, false);
         } else if constexpr (MODE == kPiecewise) {
           const int cls = pw_class(q0, t * kBN, args.P_SEQ, args.w);
-          if (cls & kNear) mma_qk<D>(tmem + C::COL_S0, aQ, aK, idesc_qk, false);
-          if (cls & kFar) mma_qk<D>(tmem + C::COL_S1, aQ2, smem_u32(sKt(st, 1)), idesc_qk, false);
+          const uint32_t sb = tmem + (b ? C::COL_S1 : C::COL_S0);
+          if (cls == kNear) {
+            mma_qk<D>(sb, aQ, aK, idesc_qk, false);
+          } else if (cls == kFar) {
+            mma_qk<D>(sb, aQ2, smem_u32(sKt(st, 1)), idesc_qk, false);
+          } else {
+            // the previous tile's softmax must be done with the third buffer
+            if (t > 0 && pw_class(q0, (t - 1) * kBN, args.P_SEQ, args.w) == (kNear | kFar)) {
+              if (!warp_wait(&bar_p[(t - 1) % NBUF], ((t - 1) / NBUF) & 1, ctl, kErrTimeoutSoftmax)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            mma_qk<D>(sb, aQ, aK, idesc_qk, false);
+            mma_qk<D>(tmem + C::COL_X, aQ2, smem_u32(sKt(st, 1)), idesc_qk, false);
+          }
         } else {
           mma_qk<D>(tmem + C::COL_S0, aQ, aK, idesc_qk, false);
           // T = tq K^T + q tk^T (the sm_scale factor is applied by the softmax)
@@ -315,9 +335,8 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t s_col = (NBUF == 2 && b) ? C::COL_S1 : C::COL_S0;
       int cls = kNear;
       if constexpr (MODE == kPiecewise) cls = pw_class(q0, k0, args.P_SEQ, args.w);
-      const uint32_t first_col = (MODE == kPiecewise && cls == kFar) ? C::COL_S1 : s_col;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + first_col + 32 * c, TA_CHUNK(s, c));
+      for (int c = 0; c < 4; ++c) tmem_ld_x32(lane_addr + s_col + 32 * c, TA_CHUNK(s, c));
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld_wait(TA_CHUNK(s, c));
       // raw scores; sm_scale * log2(e) > 0 is applied inside the exponent FMA
@@ -331,7 +350,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t s2[32];
-            tmem_ld_x32(lane_addr + C::COL_S1 + 32 * c, s2);
+            tmem_ld_x32(lane_addr + C::COL_X + 32 * c, s2);
             tmem_ld_wait(s2);
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -378,7 +397,7 @@ __global__ void __launch_bounds__(192, 1)
       const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
       l = l * alpha + rs;
       // P (16-bit, two per column) over the first 64 columns of the S buffer
-      const uint32_t p_col = (MODE == kStd) ? s_col : C::COL_S0;
+      const uint32_t p_col = s_col;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
