@@ -80,7 +80,7 @@ __device__ __forceinline__ void mma_abT(uint32_t d_tmem, uint32_t a_smem, uint32
 // d (+)= X Y: X is 128 x 128 16-bit in TMEM whose K-steps 0-3 sit at columns
 // x + [0, 32) and K-steps 4-7 at x + [64, 96) (the two column halves); Y is a
 // 128-row x D tile in smem read as an MN-major B operand (rows = K).
-template <int D>
+template <int D, int HS = 64>  // HS: TMEM column offset of the second half's K-steps
 __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
                                        bool accumulate) {
   const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
@@ -88,7 +88,7 @@ __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_
   uint64_t b[8];
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    a[kk] = x_tmem + (kk & 3) * 8 + (kk >> 2) * 64;
+    a[kk] = x_tmem + (kk & 3) * 8 + (kk >> 2) * HS;
     b[kk] = dy + static_cast<uint64_t>((kk * 16 * 128) >> 4);
   }
   mma_ts_n<8>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
@@ -114,6 +114,11 @@ struct DkdvCfg {
   static constexpr int SMEM = NRES * TILE + STAGES * STAGE + 1024;
   static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D;
   static constexpr uint32_t COL_DK2 = (PART == 1) ? 256 : 256 + 2 * D;
+  // Piecewise, all outputs, with 64 spare columns for P^T (D = 64) and two
+  // query stages: P^T lives there, so S^T's buffer frees as soon as the
+  // softmax holds S^T in registers and the next tile's score MMA can start.
+  static constexpr bool EARLY = (MODE == kPiecewise) && (PART == -1) && (256 + 3 * D + 64 <= 512) && STAGES >= 2;
+  static constexpr uint32_t COL_P = 256 + 3 * D;
   static_assert(STAGES >= 1, "tile does not fit in shared memory");
   static_assert((PART == 1 ? 256 + D : PART == 0 ? 256 + 2 * D : COL_DK2 + (MODE == kPiecewise ? D : 0)) <= 512,
                 "TMEM overflow");
@@ -134,6 +139,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_kv, bar_q[STAGES], bar_qempty[STAGES];
   __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_consumed, bar_ds, bar_done;
+  __shared__ __align__(8) uint64_t bar_sfree, bar_pfree;  // EARLY: S^T in registers; P^T read by dV
   __shared__ __align__(16) float sL[STAGES][kBM];      // L * log2(e) of the tile's queries
   __shared__ __align__(16) float sDelta[STAGES][kBM];  // delta of the tile's queries
   __shared__ uint32_t tmem_slot;
@@ -170,6 +176,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_consumed, kRowWarps);
     mbar_init(&bar_ds, kRowWarps);
     mbar_init(&bar_done, 1);
+    mbar_init(&bar_sfree, kRowWarps);
+    mbar_init(&bar_pfree, 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -245,7 +253,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = warp_wait(&bar_kv, 0, ctl, kErrTimeoutTma);
       bool acc1 = false, acc2 = false;
       int nstr = 0;
-      for (int u = 0; ok && u < nq; ++u) {
+      if constexpr (C::EARLY) {
+        auto cls_of = [&](int u) { return pw_class_b((i0 + u) * kBM, k0, args.P_SEQ, args.w); };
+        // S^T(u), its near (or only) product, into COL_A; bar_s unless the tile needs both
+        auto issue_s1 = [&](int u, int st) {
+          const int cls = cls_of(u);
+          if (cls == kFarB) mma_abT<D>(tmem + C::COL_A, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
+          else mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(st)), idesc_s);
+          if (cls != (kNearB | kFarB)) commit_el(&bar_s);
+        };
+        bool s_issued = false;  // S^T(u) went out early, under tile u - 1
+        for (int u = 0; ok && u < nq; ++u) {
+          const int st = u % STAGES;
+          const int cls = cls_of(u);
+          if (!s_issued) {
+            if (!(ok = warp_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+            tc_fence_after();
+            issue_s1(u, st);
+          }
+          if (cls == (kNearB | kFarB)) {
+            mma_abT<D>(tmem + C::COL_B, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
+            commit_el(&bar_s);
+            if (!(ok = warp_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
+            tc_fence_after();
+            ++nstr;
+          }
+          mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(st)), idesc_s);  // dP^T = V dO^T
+          commit_el(&bar_dp);
+          s_issued = false;
+          // a tile that needs both products keeps its far dS^T in COL_A: no early S^T after it
+          if (u + 1 < nq && cls != (kNearB | kFarB)) {
+            const int st1 = (u + 1) % STAGES;
+            if (!(ok = warp_wait(&bar_sfree, u & 1, ctl, kErrTimeoutSoftmax))) break;
+            if (!(ok = warp_wait(&bar_q[st1], ((u + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
+            tc_fence_after();
+            issue_s1(u + 1, st1);
+            s_issued = true;
+          }
+          if (!(ok = warp_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
+          tc_fence_after();
+          mma_tY<D, 32>(tmem + C::COL_DV, tmem + C::COL_P, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
+          commit_el(&bar_pfree);
+          if (cls & kNearB) {
+            mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
+            acc1 = true;
+          }
+          if (cls & kFarB) {
+            const uint32_t src = (cls == kFarB) ? C::COL_B : C::COL_A + 32;
+            mma_tY<D>(tmem + C::COL_DK2, tmem + src, smem_u32(sQ2(st)), idesc_g, acc2);
+            acc2 = true;
+          }
+          commit_el(&bar_qempty[st]);
+        }
+        if (ok) commit_el(&bar_done);
+      }
+      for (int u = 0; !C::EARLY && ok && u < nq; ++u) {
         const int st = u % STAGES;
         const int q0 = (i0 + u) * kBM;
         if (!(ok = warp_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
@@ -286,7 +348,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         commit_el(&bar_qempty[st]);
       }
-      if (ok) commit_el(&bar_done);
+      if (!C::EARLY && ok) commit_el(&bar_done);
     }
   } else {
     // ------------------------------------------- key-row softmax gradient
@@ -324,6 +386,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (cb + 32 * c + e >= fl) s[32 * c + e] = s2[e];
         }
       }
+      if constexpr (C::EARLY) {  // S^T is in registers: its buffer may take the next tile's
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_sfree);
+      }
       // L * log2(e) of the 64 queries, four per vector load
       const float4* L4 = reinterpret_cast<const float4*>(&sL[st][cb]);
       float p[64];
@@ -342,12 +409,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c = 0; c < 64; ++c)
           if (c < lo) p[c] = 0.f;
       }
+      if constexpr (C::EARLY) {  // P^T goes to its own columns once dV(u - 1) has read them
+        if (u > 0 && !(ok = warp_wait(&bar_pfree, (u - 1) & 1, ctl, kErrTimeoutMma))) break;
+        tc_fence_after();
+      }
+      const uint32_t p_col = C::EARLY ? C::COL_P + 32 * hc : C::COL_A + cb;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack2<BF>(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
-        tmem_st_x16(lane_addr + C::COL_A + cb + 16 * c, pk);
+        tmem_st_x16(lane_addr + p_col + 16 * c, pk);
       }
       if (cls == (kNearB | kFarB)) {
         tmem_st_wait();
