@@ -93,3 +93,29 @@ def test_binding_fails_loudly_without_library(tmp_path):
             ta.load(str(tmp_path / "missing.so"))
     finally:
         ta._lib = saved
+
+
+def test_jvp_backward_workspace_and_validation(lib):
+    """attn_bwd_jvp: workspace size (eps and delta2 rows) and the argument
+    checks that run before any launch."""
+    vp = ctypes.c_void_p
+    assert lib.attn_bwd_jvp_workspace_bytes(2, 8, 1024, 1024, 64, F16) == 2 * 16 * 1024 * 4
+    assert lib.attn_bwd_jvp_workspace_bytes(1, 1, 3, 3, 64, F16) == 512
+    assert lib.attn_bwd_jvp_workspace_bytes(0, 1, 3, 3, 64, F16) == 0
+    p = [vp(16 * (i + 1)) for i in range(18)]
+
+    def call(ptrs, ws, nbytes, D=64, dt=F16, M=128, N=128):
+        return lib.attn_bwd_jvp(*ptrs, ws, nbytes, 1, 1, M, N, D, dt, 1, -1.0, vp(0))
+
+    nws = 1 << 20
+    assert call(p, vp(0x4000), nws, D=96) == UNSUPPORTED
+    assert call(p, vp(0x4000), nws, dt=5) == UNSUPPORTED
+    assert call(p, vp(0), nws) == INVALID                  # null workspace
+    assert call(p, vp(0x4000), 16) == INVALID              # workspace too small
+    no_tl = list(p)
+    no_tl[9] = vp(0)                                        # tlse is required
+    assert call(no_tl, vp(0x4000), nws) == INVALID
+    misaligned = list(p)
+    misaligned[11] = vp(0x2008)                             # dtO
+    assert call(misaligned, vp(0x4000), nws) == ALIGNMENT
+    assert lib.attn_bwd_jvp(*p, vp(0x4000), nws, 0, 1, 128, 128, 64, F16, 1, -1.0, vp(0)) == OK  # B = 0
