@@ -18,6 +18,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -84,12 +85,22 @@ def peak_value(peaks, key):
     return FALLBACK_PEAKS.get(key)
 
 
+def _code_only(text):
+    """C++/CUDA source without its comments and blank lines (string literals in
+    these sources hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash():
+    """Hash of the kernel sources' code (comments excluded), the key under
+    which profiles/traffic.json records the DRAM counters it was taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tiled_attention_tcgen05_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -36,6 +36,14 @@
 // 16-bit results (64 values = 32 packed columns) at [64h, 64h + 32) and, for
 // the far half of a straddling piecewise tile, at [64h + 32, 64h + 64).  The
 // gradient MMAs read the packed operand's 8-column K-steps from both halves.
+//
+// The standard mode runs the specialised attn_bwd_dkdv_std_kernel /
+// attn_bwd_dq_std_kernel further down.  Of the generic kernels, the
+// piecewise mode overlaps more at D = 64, where TMEM has room: dK/dV keeps
+// P^T in its last 64 columns so the next query tile's S^T starts as soon as
+// the softmax holds S^T in registers, and dQ alternates two S buffers.  At
+// D = 128 the piecewise dK/dV pass runs as two launches (dV and dK1, then
+// dK2) because TMEM cannot hold all three accumulators beside S^T and dP^T.
 #include "bwd_common.cuh"
 #include "common.cuh"
 #include "launch.h"
