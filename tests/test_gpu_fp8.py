@@ -66,3 +66,22 @@ def test_fp8_rejects_unsupported_shapes(gpu_lib):
     k32 = torch.zeros(1, 1, 128, 32, device="cuda", dtype=f8)
     with pytest.raises(ta.TAError):
         ta.attn_fwd_fp8(q32, k32, torch.zeros(1, 1, 32, 128, device="cuda", dtype=f8))
+
+
+def test_fp8_forward_benchmark_shape_sampled_heads(gpu_lib):
+    """B1 H32 M=N=8192 D128 causal, the shape and launch bench.py times:
+    first and last heads against the rounding bound."""
+    B, H, M, D = 1, 32, 8192, 128
+    q, k, v, o, lse = _run(gpu_lib, B, H, M, M, D, True, 52)
+    s = oracle.default_scale(D)
+    keep = oracle.allowed_mask(M, M, True)
+    for h in (0, H - 1):
+        qf, kf, vf = (t[0, h].to(torch.float64).numpy() for t in (q, k, v))
+        O, L = oracle.attention_fwd(qf, kf, vf, True)
+        S = np.where(keep, s * qf @ kf.T, -np.inf)
+        P = np.exp(S - L[:, None])
+        bound = U * (1 + U) * (P @ np.abs(vf)) + U * np.abs(O) + 1e-6
+        err = np.abs(o[0, h] - O)
+        assert np.all(err <= bound), f"max excess {np.max(err - bound):.3e} at head {h}"
+        assert err.mean() < 0.03, err.mean()
+        np.testing.assert_allclose(lse[0, h], L, atol=1e-3)

@@ -84,3 +84,22 @@ def test_merge_empty_and_bad_arguments(gpu_lib):
     lx = torch.zeros(1, 1, 8, device=dev, dtype=torch.float32)
     with pytest.raises(ta.TAError):
         ta.merge_fwd(x, lx, x, lx)  # D = 96 is not supported
+
+
+def test_merge_benchmark_shape(gpu_lib):
+    """B1 H32 M8192 D128 bf16, the shape bench.py times: every element of the
+    forward and the backward (with dL)."""
+    ta = gpu_lib
+    B, H, M, D = 1, 32, 8192, 128
+    o1, l1, o2, l2 = _states(B, H, M, D, "bf16", 43)
+    do = si.randn((B, H, M, D), "bf16", si.seed_for(43, 4))
+    dl = si.randn((B, H, M), "f32", si.seed_for(43, 5))
+    g = [t.cuda() for t in (o1, l1, o2, l2, do, dl)]
+    o, lse = ta.merge_fwd(g[0], g[1], g[2], g[3])
+    grads = ta.merge_bwd(*g)
+    assert ta.sync_status() == "TA_OK"
+    O, L = oracle.lse_merge_fwd_bhsd(o1, l1, o2, l2)
+    compare("O", o, O, o_tol("bf16"))
+    compare("L", lse, L, 1e-5)
+    for name, got, r in zip(("dO1", "dL1", "dO2", "dL2"), grads, oracle.lse_merge_bwd_bhsd(o1, l1, o2, l2, do, dl)):
+        compare(name, got, r, TOL["grad"] if name.startswith("dO") else 1e-4)
