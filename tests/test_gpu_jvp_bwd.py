@@ -1,7 +1,8 @@
 """GPU parity of the backward of the JVP (attn_bwd_jvp) through the C ABI
 against the fp64 oracle: the gradients of <dO, O> + <dtO, tO> with respect to
 q, k, v and the tangents.  16-bit cases compare every element at the
-gradient tolerance (max_abs 5e-2, unit-normal inputs); the fp32 mode at 1e-4.
+tolerance derived for it (max_abs 5e-2 fp16, 1e-1 bf16, unit-normal inputs;
+see jvp_grad_tol); the fp32 mode at 1e-4.
 The forward outputs (o, lse, to, tlse) are the GPU's own attn_fwd_jvp."""
 import numpy as np
 import pytest
@@ -9,7 +10,7 @@ import torch
 
 import oracle
 import synth_inputs as si
-from _parity import TOL, compare, inputs, sample_heads
+from _parity import TOL, compare, inputs, jvp_grad_tol, sample_heads
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +45,7 @@ def test_jvp_backward_small(gpu_lib, B, H, M, N, D, dtype, causal):
     grads = _run(gpu_lib, g, causal)
     ref = oracle.attention_jvp_bwd_bhsd(*(cpu[n] for n in NAMES), causal)
     for name, got, r in zip(GRADS, grads, ref):
-        compare(name, got, r, TOL["grad"])
+        compare(name, got, r, jvp_grad_tol(dtype))
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -57,7 +58,7 @@ def test_jvp_backward_fp16_b2_h8_s1024_d64(gpu_lib, causal):
     ref = oracle.attention_jvp_bwd_bhsd(*(cpu[n] for n in NAMES), causal, heads=heads)
     for name, got, r in zip(GRADS, grads, ref):
         compare(name, np.stack([got[b, h].float().cpu().numpy() for b, h in heads]),
-                np.stack([r[b, h] for b, h in heads]), TOL["grad"])
+                np.stack([r[b, h] for b, h in heads]), jvp_grad_tol("f16"))
 
 
 @pytest.mark.parametrize("B,H,M,N,D,causal", [(1, 2, 128, 128, 64, False), (1, 1, 200, 333, 128, True),
