@@ -526,22 +526,28 @@ __global__ void __launch_bounds__(192, 1)
 // K and V have separate rings: a K tile is released as soon as both score
 // MMAs that read it have finished, so the K ring runs further ahead of the
 // MMAs than a joint K/V ring of the same size could.
-template <int D>
+template <int D, bool PW = false>
 struct Fwd2Cfg {
   static constexpr int BLK = kBM * 128;
   static constexpr int TILE = (D / 64) * BLK;
-  static constexpr int KST = (D == 128) ? 3 : 4;  // K ring depth
-  static constexpr int VST = (D == 128) ? 2 : 4;  // V ring depth
-  static constexpr int SMEM = (2 + KST + VST) * TILE + 1024;
+  // piecewise: Q1 and Q2 of both query tiles resident, K1 and K2 per K stage,
+  // and a third 128-column score buffer for S(q2, k2) of a tile that needs both
+  static constexpr int NQ = PW ? 4 : 2;
+  static constexpr int NK = PW ? 2 : 1;
+  static constexpr int KST = PW ? 3 : (D == 128) ? 3 : 4;  // K ring depth
+  static constexpr int VST = PW ? 3 : (D == 128) ? 2 : 4;  // V ring depth
+  static constexpr int SMEM = (NQ + NK * KST + VST) * TILE + 1024;
+  static constexpr uint32_t COL_X = 256 + 2 * D;
   static_assert(SMEM + 2048 <= kSmemMax, "tiles do not fit in shared memory");
-  static_assert(256 + 2 * D <= 512, "TMEM overflow");
+  static_assert(256 + 2 * D + (PW ? 128 : 0) <= 512, "TMEM overflow");
 };
 
-template <typename T, int D>
+template <typename T, int D, bool PW>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
-  using C = Fwd2Cfg<D>;
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q2,
+                     const __grid_constant__ CUtensorMap tm_k2, const FwdArgs args) {
+  using C = Fwd2Cfg<D, PW>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int KST = C::KST, VST = C::VST;
 
@@ -549,6 +555,7 @@ __global__ void __launch_bounds__(320, 1)
   __shared__ __align__(8) uint64_t bar_q;
   __shared__ __align__(8) uint64_t bar_k[KST], bar_kempty[KST], bar_v[VST], bar_vempty[VST];
   __shared__ __align__(8) uint64_t bar_s[2], bar_p[2], bar_o[2], bar_ofinal;
+  __shared__ __align__(8) uint64_t bar_xfree;  // piecewise: the third score buffer has been read
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -565,9 +572,11 @@ __global__ void __launch_bounds__(320, 1)
   const int nt = n_t[1] > n_t[0] ? n_t[1] : n_t[0];
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = base;  // tile 0 at sQ, tile 1 at sQ + TILE
-  auto sK = [&](int st) { return base + (2 + st) * C::TILE; };
-  auto sV = [&](int st) { return base + (2 + KST + st) * C::TILE; };
+  uint8_t* sQ = base;  // tile 0 at sQ, tile 1 at sQ + TILE (piecewise: then Q2 of both)
+  auto sK = [&](int st) { return base + (C::NQ + C::NK * st) * C::TILE; };  // K | K1 (+ K2 next)
+  auto sV = [&](int st) { return base + (C::NQ + C::NK * KST + st) * C::TILE; };
+  // piecewise: which score products query tile w needs for key tile t
+  auto cls_of = [&](int w, int t) { return pw_class(q0 + w * kBM, t * kBN, args.P_SEQ, args.w); };
 
   WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
   if (threadIdx.x == 0) {
@@ -587,6 +596,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bar_o[w], 1);
     }
     mbar_init(&bar_ofinal, 1);
+    mbar_init(&bar_xfree, 4);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -612,9 +622,13 @@ __global__ void __launch_bounds__(320, 1)
       if (is_k) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
-        mbar_expect_tx(&bar_q, 2 * C::TILE);
+        mbar_expect_tx(&bar_q, C::NQ * C::TILE);
         load_tile<D>(sQ, &tm_q, &bar_q, q0, bh);
         load_tile<D>(sQ + C::TILE, &tm_q, &bar_q, q0 + kBM, bh);
+        if constexpr (PW) {
+          load_tile<D>(sQ + 2 * C::TILE, &tm_q2, &bar_q, q0, bh);
+          load_tile<D>(sQ + 3 * C::TILE, &tm_q2, &bar_q, q0 + kBM, bh);
+        }
       } else {
         tma_prefetch_desc(&tm_v);
       }
@@ -622,8 +636,17 @@ __global__ void __launch_bounds__(320, 1)
       for (int t = 0; t < nt; ++t) {
         const int st = t % depth;
         if (t >= depth && !mbar_wait(&empty[st], ((t / depth) - 1) & 1, ctl, kErrTimeoutMma)) break;
-        mbar_expect_tx(&full[st], C::TILE);
-        load_tile<D>(is_k ? sK(st) : sV(st), map, &full[st], t * kBN, bh);
+        if (PW && is_k) {  // K1 if either query tile needs a near product, K2 if either needs a far one
+          int need = 0;
+          for (int w = 0; w < 2; ++w)
+            if (t < n_t[w]) need |= cls_of(w, t);
+          mbar_expect_tx(&full[st], (((need & kNear) ? 1 : 0) + ((need & kFar) ? 1 : 0)) * C::TILE);
+          if (need & kNear) load_tile<D>(sK(st), &tm_k, &full[st], t * kBN, bh);
+          if (need & kFar) load_tile<D>(sK(st) + C::TILE, &tm_k2, &full[st], t * kBN, bh);
+        } else {
+          mbar_expect_tx(&full[st], C::TILE);
+          load_tile<D>(is_k ? sK(st) : sV(st), map, &full[st], t * kBN, bh);
+        }
         issued = t + 1;
       }
       int zero = 0;
@@ -638,14 +661,36 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t idesc_qk = idesc_f16(kBM, kBN, BF, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(kBM, D, BF, false, true);
       const uint32_t aQ[2] = {smem_u32(sQ), smem_u32(sQ) + C::TILE};
+      int nx = 0;  // piecewise: uses of the third score buffer so far
+      // S of query tile w against key tile t (stage sk); false if a wait ran out
+      auto issue_s = [&](int w, int t, int sk) -> bool {
+        if constexpr (!PW) {
+          mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(sk)), idesc_qk, false);
+        } else {
+          const int cls = cls_of(w, t);
+          const uint32_t aK1 = smem_u32(sK(sk)), aK2 = aK1 + C::TILE, aQ2 = aQ[w] + 2 * C::TILE;
+          if (cls == kNear) {
+            mma_qk<D>(tmem + col_s[w], aQ[w], aK1, idesc_qk, false);
+          } else if (cls == kFar) {
+            mma_qk<D>(tmem + col_s[w], aQ2, aK2, idesc_qk, false);
+          } else {  // S(q1, k1) in its own buffer, S(q2, k2) in the shared third one
+            if (nx > 0) {
+              if (!warp_wait(&bar_xfree, (nx - 1) & 1, ctl, kErrTimeoutSoftmax)) return false;
+              tc_fence_after();
+            }
+            ++nx;
+            mma_qk<D>(tmem + col_s[w], aQ[w], aK1, idesc_qk, false);
+            mma_qk<D>(tmem + C::COL_X, aQ2, aK2, idesc_qk, false);
+          }
+        }
+        commit_el(&bar_s[w]);
+        return true;
+      };
       bool ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma) && warp_wait(&bar_k[0], 0, ctl, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
-        for (int w = 0; w < 2; ++w)
-          if (n_t[w] > 0) {
-            mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(0)), idesc_qk, false);
-            commit_el(&bar_s[w]);
-          }
+        for (int w = 0; ok && w < 2; ++w)
+          if (n_t[w] > 0) ok = issue_s(w, 0, 0);
       }
       if (ok) commit_el(&bar_kempty[0]);  // K tile 0 is consumed once both score MMAs finish
       for (int t = 0; ok && t < nt; ++t) {
@@ -662,8 +707,7 @@ __global__ void __launch_bounds__(320, 1)
             commit_el(&bar_o[w]);
           }
           if (next && t + 1 < n_t[w]) {
-            mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(sk1)), idesc_qk, false);
-            commit_el(&bar_s[w]);
+            if (!(ok = issue_s(w, t + 1, sk1))) break;
           }
         }
         if (!ok) break;
@@ -694,6 +738,24 @@ __global__ void __launch_bounds__(320, 1)
       float x[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) x[j] = __uint_as_float(s[j]);
+      if constexpr (PW) {
+        if (cls_of(w, t) == (kNear | kFar)) {
+          // far iff key k0 + c satisfies row + P_SEQ - (k0 + c) >= w: take S(q2, k2) there
+          const long long pwl = (long long)row + args.P_SEQ - k0 - args.w;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t s2[32];
+            tmem_ld_x32(lane_addr + C::COL_X + 32 * c, s2);
+            tmem_ld_wait(s2);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (32 * c + j <= pwl) x[32 * c + j] = __uint_as_float(s2[j]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_xfree);
+        }
+      }
       if ((args.causal && k0 + kBN - 1 > tq0 + args.P_SEQ) || (k0 + kBN > args.N)) {
         int lim = args.N - 1 - k0;
         if (args.causal) lim = min(lim, row + args.P_SEQ - k0);
@@ -807,10 +869,10 @@ static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStrea
   return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool PW = false>
 static cudaError_t launch_fwd2_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
-  using C = Fwd2Cfg<D>;
-  auto kern = attn_fwd2_kernel<T, D>;
+  using C = Fwd2Cfg<D, PW>;
+  auto kern = attn_fwd2_kernel<T, D, PW>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -820,7 +882,7 @@ static cudaError_t launch_fwd2_t(const FwdMaps& maps, const FwdArgs& a, cudaStre
   const long long pairs = (a.M + 2 * kBM - 1) / (2 * kBM);
   const long long blocks = pairs * a.BH;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, a);
+  kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, a);
   return cudaGetLastError();
 }
 
@@ -829,11 +891,12 @@ cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const Fw
     if (D == 64) return bf16 ? launch_fwd2_t<__nv_bfloat16, 64>(maps, a, s) : launch_fwd2_t<__half, 64>(maps, a, s);
     if (D == 128) return bf16 ? launch_fwd2_t<__nv_bfloat16, 128>(maps, a, s) : launch_fwd2_t<__half, 128>(maps, a, s);
   }
+  if (mode == kPiecewise && D == 64)  // two query tiles per CTA; TMEM has room for the third score buffer
+    return bf16 ? launch_fwd2_t<__nv_bfloat16, 64, true>(maps, a, s) : launch_fwd2_t<__half, 64, true>(maps, a, s);
 #define TA_FWD_CASE(MODE_, D_)                                                          \
   if (mode == MODE_ && D == D_)                                                         \
     return bf16 ? launch_fwd_t<__nv_bfloat16, MODE_, D_>(maps, a, s)                    \
                 : launch_fwd_t<__half, MODE_, D_>(maps, a, s);
-  TA_FWD_CASE(kPiecewise, 64)
   TA_FWD_CASE(kPiecewise, 128)
   TA_FWD_CASE(kJvp, 64)
   TA_FWD_CASE(kJvp, 128)
