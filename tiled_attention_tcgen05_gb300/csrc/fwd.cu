@@ -516,7 +516,8 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ======================================================================
-//   Standard forward, two query tiles per CTA (ping-pong softmax groups)
+//   Two query tiles per CTA (ping-pong softmax groups): the standard
+//   forward, and the piecewise forward at D = 64
 // ======================================================================
 // One CTA owns query rows [q0, q0 + 256) of one head as two 128-row tiles
 // that share every K/V tile.  Warps 0-3 run the softmax of tile 0, warps 4-7
@@ -526,6 +527,11 @@ __global__ void __launch_bounds__(192, 1)
 // K and V have separate rings: a K tile is released as soon as both score
 // MMAs that read it have finished, so the K ring runs further ahead of the
 // MMAs than a joint K/V ring of the same size could.
+// Piecewise (PW): Q1 and Q2 of both tiles stay resident and a K stage holds
+// K1 and/or K2 as the two tiles' classes need; a tile whose keys are all
+// near (or all far) runs one score MMA, one that straddles the distance w
+// runs S(q1, k1) into its own buffer and S(q2, k2) into a third buffer that
+// the two tiles share (its reader's arrival on bar_xfree releases it).
 template <int D, bool PW = false>
 struct Fwd2Cfg {
   static constexpr int BLK = kBM * 128;
