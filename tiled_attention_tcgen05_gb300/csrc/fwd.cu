@@ -548,11 +548,12 @@ struct Fwd2Cfg {
   static_assert(256 + 2 * D + (PW ? 128 : 0) <= 512, "TMEM overflow");
 };
 
+// The kernel body; the standard entry point below takes three tensor maps,
+// the piecewise one five.  The maps arrive by reference to the __grid_constant__
+// kernel parameters, whose addresses the TMA instructions take.
 template <typename T, int D, bool PW>
-__global__ void __launch_bounds__(320, 1)
-    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q2,
-                     const __grid_constant__ CUtensorMap tm_k2, const FwdArgs args) {
+__device__ __forceinline__ void fwd2_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                          const CUtensorMap& tm_q2, const CUtensorMap& tm_k2, const FwdArgs args) {
   using C = Fwd2Cfg<D, PW>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int KST = C::KST, VST = C::VST;
@@ -602,7 +603,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&bar_o[w], 1);
     }
     mbar_init(&bar_ofinal, 1);
-    mbar_init(&bar_xfree, 4);
+    if constexpr (PW) mbar_init(&bar_xfree, 4);
     fence_mbar_init();
   }
   if (warp == 9) {
@@ -695,8 +696,15 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma) && warp_wait(&bar_k[0], 0, ctl, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
-        for (int w = 0; ok && w < 2; ++w)
-          if (n_t[w] > 0) ok = issue_s(w, 0, 0);
+        for (int w = 0; w < 2; ++w)
+          if (n_t[w] > 0) {
+            if constexpr (PW) {
+              if (ok) ok = issue_s(w, 0, 0);
+            } else {
+              mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(0)), idesc_qk, false);
+              commit_el(&bar_s[w]);
+            }
+          }
       }
       if (ok) commit_el(&bar_kempty[0]);  // K tile 0 is consumed once both score MMAs finish
       for (int t = 0; ok && t < nt; ++t) {
@@ -713,7 +721,12 @@ __global__ void __launch_bounds__(320, 1)
             commit_el(&bar_o[w]);
           }
           if (next && t + 1 < n_t[w]) {
-            if (!(ok = issue_s(w, t + 1, sk1))) break;
+            if constexpr (PW) {
+              if (!(ok = issue_s(w, t + 1, sk1))) break;
+            } else {  // the standard path keeps the MMA warp's loop as lean as possible
+              mma_qk<D>(tmem + col_s[w], aQ[w], smem_u32(sK(sk1)), idesc_qk, false);
+              commit_el(&bar_s[w]);
+            }
           }
         }
         if (!ok) break;
@@ -859,6 +872,21 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
+template <typename T, int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+  fwd2_body<T, D, false>(tm_q, tm_k, tm_v, tm_q, tm_k, args);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_fwd2_pw_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_k1,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q2,
+                        const __grid_constant__ CUtensorMap tm_k2, const FwdArgs args) {
+  fwd2_body<T, D, true>(tm_q1, tm_k1, tm_v, tm_q2, tm_k2, args);
+}
+
 // ---------------------------------------------------------------- host side
 template <typename T, int MODE, int D>
 static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
@@ -878,17 +906,27 @@ static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStrea
 template <typename T, int D, bool PW = false>
 static cudaError_t launch_fwd2_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
   using C = Fwd2Cfg<D, PW>;
-  auto kern = attn_fwd2_kernel<T, D, PW>;
   static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   const long long pairs = (a.M + 2 * kBM - 1) / (2 * kBM);
   const long long blocks = pairs * a.BH;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, a);
+  if constexpr (PW) {
+    auto kern = attn_fwd2_pw_kernel<T, D>;
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, a);
+  } else {
+    auto kern = attn_fwd2_kernel<T, D>;
+    if (!attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+      if (e != cudaSuccess) return e;
+      attr_set = true;
+    }
+    kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, a);
+  }
   return cudaGetLastError();
 }
 
