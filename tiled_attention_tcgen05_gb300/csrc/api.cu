@@ -324,8 +324,8 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
 // Backward of the JVP.  The workspace holds eps = <dtO, O> and
 // delta2 = <dO, O> + <dtO, tO> per query row.  The tangents' gradients are the
 // plain backward with dO := dtO (whose delta is eps): the JVP kernels form
-// them alongside the primal gradients at D <= 64 and the plain backward
-// kernels at D = 128.
+// them alongside the primal gradients where TMEM has room (dtK and dtV at
+// D <= 64, dtQ at every D), the plain backward's dK/dV kernel otherwise.
 static ta_status run_bwd_jvp(const Problem& p, const void* q, const void* k, const void* v, const void* tq,
                              const void* tk, const void* tv, const void* o, const float* lse, const void* to,
                              const float* tlse, const void* dO, const void* dtO, void* dq, void* dk, void* dv,
@@ -400,8 +400,9 @@ static ta_status run_bwd_jvp(const Problem& p, const void* q, const void* k, con
          make_map(n64[i], nrows[i], p.BH, p.N, p.D, p.bf16, 64);
   if (!ok) return TA_ERR_CUDA;
   const int kd = kernel_d(p.D);
-  if (bwd_jvp_has_tangents(kd)) {  // the JVP kernels write the tangents' gradients too
-    ap.dtq = dtq;
+  // the JVP kernels write the tangents' gradients too where TMEM has room;
+  // otherwise the plain backward of dtO computes them
+  if (bwd_jvp_has_tangents(true, kd)) {
     ap.dtk = dtk;
     ap.dtv = dtv;
   } else {
@@ -409,6 +410,10 @@ static ta_status run_bwd_jvp(const Problem& p, const void* q, const void* k, con
     e = launch_bwd_dkdv(kStd, p.bf16, kd, maps, at, s);
     prof_end(s);
     if (e != cudaSuccess) return TA_ERR_CUDA;
+  }
+  if (bwd_jvp_has_tangents(false, kd)) {
+    ap.dtq = dtq;
+  } else {
     prof_begin("attn_bwd_jvp_tangents_dq", s);
     e = launch_bwd_dq(kStd, p.bf16, kd, maps, at, s);
     prof_end(s);

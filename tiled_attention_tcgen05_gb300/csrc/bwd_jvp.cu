@@ -13,8 +13,9 @@
 //   dV = P^T dO + tP^T dtO.
 // The tangents' own gradients are the plain backward with dO replaced by
 // dtO (tO is linear in the tangents): dtq = sm_scale dT K, dtk = sm_scale
-// dT^T Q, dtv = P^T dtO.  At D <= 64 (TANG) these kernels accumulate them
-// too; at D = 128 TMEM has no room and the plain backward kernels run them.
+// dT^T Q, dtv = P^T dtO.  These kernels accumulate them too (TANG) where
+// TMEM has room: dtK and dtV at D <= 64, dtQ at every D; otherwise the plain
+// backward's key-stationary kernel computes dtK and dtV.
 //
 // Two kernels from one template, each one CTA per 128-row stationary tile,
 // 320 threads:
@@ -65,9 +66,11 @@ struct JvpBwdCfg {
   static_assert(COL_ACC + 2 * D <= 512, "TMEM overflow");
 };
 
-// The tangents' gradients fit beside the others (4 D accumulator columns).
-template <int D>
-constexpr bool jvp_tangents_fit() { return 256 + 4 * D <= 512; }
+// The tangents' gradients fit beside the others: dV, dK, dtV, dtK (4 D
+// accumulator columns) in the key-stationary kernel, dQ, dtQ (2 D) in the
+// query-stationary one.
+template <int D, bool KEYS>
+constexpr bool jvp_tangents_fit() { return 256 + (KEYS ? 4 : 2) * D <= 512; }
 
 template <int D>
 __device__ __forceinline__ void jvp_load(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh,
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
   using C = JvpBwdCfg<D>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
-  static_assert(!TANG || jvp_tangents_fit<D>(), "no TMEM room for the tangents' gradients");
+  static_assert(!TANG || jvp_tangents_fit<D, KEYS>(), "no TMEM room for the tangents' gradients");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_x, bar_y[STAGES], bar_yempty[STAGES];
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
 template <typename T, bool KEYS, int D>
 static cudaError_t launch_jvp_bwd_t(const JvpBwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = JvpBwdCfg<D>;
-  auto kern = attn_bwd_jvp_kernel<T, KEYS, D, jvp_tangents_fit<D>()>;
+  auto kern = attn_bwd_jvp_kernel<T, KEYS, D, jvp_tangents_fit<D, KEYS>()>;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -510,7 +513,10 @@ static cudaError_t launch_jvp_bwd_t(const JvpBwdMaps& m, const BwdArgs& a, cudaS
   return cudaGetLastError();
 }
 
-bool bwd_jvp_has_tangents(int D) { return D == 64 ? jvp_tangents_fit<64>() : jvp_tangents_fit<128>(); }
+bool bwd_jvp_has_tangents(bool keys, int D) {
+  if (keys) return D == 64 ? jvp_tangents_fit<64, true>() : jvp_tangents_fit<128, true>();
+  return D == 64 ? jvp_tangents_fit<64, false>() : jvp_tangents_fit<128, false>();
+}
 
 cudaError_t launch_bwd_jvp(bool keys, bool bf16, int D, const JvpBwdMaps& m, const BwdArgs& a, cudaStream_t s) {
 #define TA_JVP_BWD(K_, D_) \

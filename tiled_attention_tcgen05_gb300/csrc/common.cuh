@@ -48,7 +48,7 @@ struct BwdArgs {
   const float* delta;  // backward of the JVP: <dO, O> + <dtO, tO>
   const float* mu;     // backward of the JVP only: tL = rowsum(P o T)
   const float* eps;    // backward of the JVP only: <dtO, O>
-  void* dtq;           // backward of the JVP at D <= 64: the tangents' gradients
+  void* dtq;           // backward of the JVP: the tangents' gradients (where TMEM has room)
   void* dtk;
   void* dtv;
   int BH, M, N, P_SEQ;

@@ -40,9 +40,9 @@ struct JvpBwdMaps {
 cudaError_t launch_jvp_delta(bool bf16, int D, const void* o, const void* dO, const void* to, const void* dto,
                              float* eps, float* delta2, long long rows, cudaStream_t s);
 // keys = true: dK, dV (a.dk, a.dv); false: dQ (a.dq).  a.delta = delta2.
-// When bwd_jvp_has_tangents(D) the same launches also write the tangents'
-// gradients (a.dtk, a.dtv; a.dtq).
-bool bwd_jvp_has_tangents(int D);
+// When bwd_jvp_has_tangents(keys, D) the same launch also writes the
+// tangents' gradients (keys: a.dtk, a.dtv; otherwise a.dtq).
+bool bwd_jvp_has_tangents(bool keys, int D);
 cudaError_t launch_bwd_jvp(bool keys, bool bf16, int D, const JvpBwdMaps& maps, const BwdArgs& a, cudaStream_t s);
 
 // Fills O = 0, L = -inf (rows that see no key) for BH*M rows of D elements
