@@ -272,3 +272,53 @@ def test_fp32_mode_piecewise(gpu_lib, D, w):
     compare("L", lse, L, F32_TOL)
     for name, got, r in zip(("dq1", "dk1", "dq2", "dk2", "dv"), grads, ref):
         compare(name, got, r, F32_TOL)
+
+
+# ------------------------------------------------------- wide score range
+@pytest.mark.parametrize("M,N,D,dtype,causal,scale", [(512, 512, 128, "bf16", True, 1.0),
+                                                      (384, 640, 64, "f16", False, 2.0),
+                                                      (300, 300, 64, "bf16", True, 2.0)])
+def test_large_scores_exercise_the_rescale(gpu_lib, M, N, D, dtype, causal, scale):
+    """sm_scale 1 or 2 instead of 1/sqrt(D): scores spread over ~10-20 units,
+    so the running maximum rises by more than 2^8 across key tiles again and
+    again and the O correction runs (the lazy-rescale reading).  The forward
+    outputs O and L are held element by element to the tolerance plus their
+    own 16-bit rounding.  The gradients grow with the scores (|dQ| ~ 50 here)
+    and carry the rounding of the 16-bit MMA operands P and dS at that size,
+    so they are held to the scaled tolerance plus two roundings of the
+    largest value (bf16 meets ~1.7 u of it); tO gets a per-element bound from
+    the terms it is the difference of."""
+    from _parity import ROUND_U
+    ta = gpu_lib
+    names = ("q", "k", "v", "do", "tq", "tk", "tv")
+    cpu, g = inputs(1, 2, M, N, D, dtype, 91, names)
+    o, lse = ta.attn_fwd(g["q"], g["k"], g["v"], causal, scale)
+    dq, dk, dv = ta.attn_bwd(g["q"], g["k"], g["v"], o, lse, g["do"], causal, scale)
+    o2, lse2, to = ta.attn_fwd_jvp(g["q"], g["k"], g["v"], g["tq"], g["tk"], g["tv"], causal, scale)
+    assert ta.sync_status() == "TA_OK"
+    u = ROUND_U[dtype]
+    O, L = oracle.attention_fwd_bhsd(cpu["q"], cpu["k"], cpu["v"], causal, scale)
+    compare("O", o, O, o_tol(dtype), u)
+    compare("L", lse, L, TOL["L"] * scale * 4)  # L scales with the scores; fp32 at |L| ~ 100
+    for name, got, r in zip(("dQ", "dK", "dV"), (dq, dk, dv),
+                            oracle.attention_bwd_bhsd(cpu["q"], cpu["k"], cpu["v"], cpu["do"], causal, scale)):
+        compare(name, got, r, TOL["grad"] * scale + 2 * u * float(np.abs(r).max()))
+    _, _, tO = oracle.attention_jvp_bhsd(cpu["q"], cpu["k"], cpu["v"], cpu["tq"], cpu["tk"], cpu["tv"], causal,
+                                         scale)
+    compare("O(jvp)", o2, O, o_tol(dtype), u)
+    # tO = (P o T) V - mu O + P tV is a difference of two large terms; each
+    # carries ~u of its own size (P o T and P rounded before their products),
+    # so the bound is taken element by element from those terms
+    keep = oracle.allowed_mask(M, N, causal)
+    got = to.float().cpu().double().numpy()
+    for h in range(2):
+        q, k, v, tq, tk = (cpu[n][0, h].double().numpy() for n in ("q", "k", "v", "tq", "tk"))
+        S = np.where(keep, scale * q @ k.T, -np.inf)
+        P = np.exp(S - L[0, h][:, None])
+        T = np.where(keep, scale * (tq @ k.T + q @ tk.T), 0.0)
+        mu = (P * T).sum(axis=1)
+        tv = cpu["tv"][0, h].double().numpy()
+        bound = TOL["tO"] + 2 * u * ((P * np.abs(T)) @ np.abs(v) + np.abs(mu)[:, None] * np.abs(O[0, h])
+                                     + P @ np.abs(tv))
+        err = np.abs(got[0, h] - tO[0, h])
+        assert np.all(err <= bound), f"tO: head {h} exceeds its bound by {np.max(err - bound):.3e}"
