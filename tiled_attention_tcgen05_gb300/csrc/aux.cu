@@ -78,15 +78,18 @@ __global__ void __launch_bounds__(256) jvp_delta_kernel(const uint4* __restrict_
   }
 }
 
+// SM count of the current device (cached per device).
 static int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  int* n = (dev >= 0 && dev < kMaxDevices) ? &cache[dev] : nullptr;
+  int v = n ? *n : 0;
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    if (n) *n = v;
   }
-  return n;
+  return v;
 }
 
 cudaError_t launch_delta(bool bf16, int D, const void* o, const void* dO, float* delta, long long rows,

@@ -1503,12 +1503,9 @@ template <typename T, int MODE, int D, int PART = -1>
 static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DkdvCfg<MODE, D, PART>;
   auto kern = attn_bwd_dkdv_kernel<T, MODE, D, PART>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static bool attr[kMaxDevices] = {};
+  cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+  if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
@@ -1519,12 +1516,9 @@ template <typename T, int MODE, int D>
 static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DqCfg<MODE, D>;
   auto kern = attn_bwd_dq_kernel<T, MODE, D>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static bool attr[kMaxDevices] = {};
+  cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+  if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
@@ -1535,12 +1529,9 @@ template <typename T, int D>
 static cudaError_t launch_dkdv_std_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DkdvStdCfg<D>;
   auto kern = attn_bwd_dkdv_std_kernel<T, D>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static bool attr[kMaxDevices] = {};
+  cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+  if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, a);
@@ -1565,12 +1556,9 @@ template <typename T, int D>
 static cudaError_t launch_dq_std_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DqStdCfg<D>;
   auto kern = attn_bwd_dq_std_kernel<T, D>;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static bool attr[kMaxDevices] = {};
+  cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+  if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, a);

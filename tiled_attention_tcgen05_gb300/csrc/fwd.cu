@@ -892,12 +892,9 @@ template <typename T, int MODE, int D>
 static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<MODE, D>;
   auto kern = attn_fwd_kernel<T, MODE, D>;
-  static bool attr_set = false;  // per instantiation; the attribute is per device-function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool attr[kMaxDevices] = {};
+  cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+  if (e_attr != cudaSuccess) return e_attr;
   dim3 grid(a.BH, a.num_q_tiles);
   kern<<<grid, 192, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, maps.v2, a);
   return cudaGetLastError();
@@ -906,25 +903,19 @@ static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStrea
 template <typename T, int D, bool PW = false>
 static cudaError_t launch_fwd2_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
   using C = Fwd2Cfg<D, PW>;
-  static bool attr_set = false;
+  static bool attr[kMaxDevices] = {};
   const long long pairs = (a.M + 2 * kBM - 1) / (2 * kBM);
   const long long blocks = pairs * a.BH;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   if constexpr (PW) {
     auto kern = attn_fwd2_pw_kernel<T, D>;
-    if (!attr_set) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-      if (e != cudaSuccess) return e;
-      attr_set = true;
-    }
+    cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+    if (e_attr != cudaSuccess) return e_attr;
     kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, a);
   } else {
     auto kern = attn_fwd2_kernel<T, D>;
-    if (!attr_set) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-      if (e != cudaSuccess) return e;
-      attr_set = true;
-    }
+    cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+    if (e_attr != cudaSuccess) return e_attr;
     kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, a);
   }
   return cudaGetLastError();

@@ -345,12 +345,9 @@ template <int D>
 static cudaError_t launch_fwd_f8_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
   using C = F8Cfg<D>;
   auto kern = attn_fwd_f8_kernel<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static bool attr[kMaxDevices] = {};
+  cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+  if (e_attr != cudaSuccess) return e_attr;
   const long long pairs = (a.M + 2 * kBM - 1) / (2 * kBM);
   const long long blocks = static_cast<long long>(a.BH) * pairs;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;

@@ -77,6 +77,23 @@ struct MergePtrs {
 };
 cudaError_t launch_merge(bool bwd, int dtype, int D, const MergePtrs& p, long long rows, cudaStream_t s);
 
+// Opts kernel `kern` into `bytes` of dynamic shared memory on the current
+// device, once per device (the attribute is per device, so a process that
+// drives several GPUs sets it on each); `done` is the caller's per-kernel
+// table.
+constexpr int kMaxDevices = 64;
+template <typename K>
+inline cudaError_t smem_attr_once(K kern, int bytes, bool (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < kMaxDevices;
+  if (tracked && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && tracked) done[dev] = true;
+  return e;
+}
+
 // Profiling hooks (no-ops unless ta_profile_enable(1)).
 void prof_begin(const char* name, cudaStream_t s);
 void prof_end(cudaStream_t s);

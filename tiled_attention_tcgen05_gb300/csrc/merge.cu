@@ -140,15 +140,18 @@ __global__ void __launch_bounds__(256) merge_bwd_kernel(const T* __restrict__ o1
   }
 }
 
+// SM count of the current device (cached per device).
 static int merge_sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  int* n = (dev >= 0 && dev < kMaxDevices) ? &cache[dev] : nullptr;
+  int v = n ? *n : 0;
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+    if (n) *n = v;
   }
-  return n;
+  return v;
 }
 
 template <typename T, int D>
