@@ -17,17 +17,6 @@ def o_tol(dtype: str) -> float:
     return TOL["O_bf16"] if dtype == "bf16" else TOL["O_f16"]
 
 
-def jvp_grad_tol(dtype: str) -> float:
-    """Gradients of the backward of the JVP.  Its row constants
-    delta2 = <dO, O> + <dtO, tO> and eps = <dtO, O> are formed from the two
-    stored, rounded outputs O and tO (as the plain backward forms delta from
-    the stored O), so where the exact dS and dT cancel (one visible key: P = 1)
-    the rounding of both outputs remains: about u sqrt(D) s max|K| per term,
-    u the unit roundoff.  Twice the plain gradients' 5e-2 for bf16 (u = 2^-8);
-    fp16 (u = 2^-11) keeps 5e-2."""
-    return 1e-1 if dtype == "bf16" else TOL["grad"]
-
-
 def to_np(t) -> np.ndarray:
     return t.detach().float().cpu().double().numpy()
 
@@ -84,3 +73,71 @@ def sample_heads(B, H, n=2):
         return hs
     pick = [hs[0], hs[-1]] + [hs[len(hs) // 2]][: max(0, n - 2)]
     return pick[:n]
+
+
+def jvp_bwd_bounds(cpu, causal, u, sm_scale=None, heads=None):
+    """Element-wise error bounds for the backward of the JVP (beyond a flat
+    unit-scale tolerance), per head, from the quantities the kernels round:
+
+    * the row constants delta2 = <dO,O> + <dtO,tO> and eps = <dtO,O> are
+      formed from the stored 16-bit O and tO, and tO already carries the
+      rounding of P o T before its product with V: over the D terms of each
+      row, r_d2 = u rms-sum(dO O, dtO tO, dtO (P o |T|) |V|) and
+      r_e = u rms-sum(dtO O), so dS moves by P (r_d2 + |T - mu| r_e) and dT by
+      P r_e, and every gradient sums those moves over its keys or queries;
+    * P, tP, dS and dT are rounded to 16 bits before the gradient MMAs (u of
+      each term) and every result once more on output.
+    The roundings are independent, so sums combine as the root of the summed
+    squares; the bound is 4 times that (a 4-sigma allowance).  It matters
+    where the exact gradients cancel (one key: P = 1) and the key-side
+    gradients sum the rows' rounding over every query.
+    Returns {name: [B, H, ...] bound} for dq, dk, dv, dtq, dtk, dtv (heads not
+    listed stay 0)."""
+    import oracle
+    x = {n: cpu[n].double().numpy() for n in ("q", "k", "v", "tq", "tk", "tv", "do", "dto")}
+    B, H, M, D = x["q"].shape
+    N = x["k"].shape[2]
+    s = oracle.default_scale(D, sm_scale)
+    keep = oracle.allowed_mask(M, N, causal)
+    out = {n: np.zeros((B, H) + (M if n in ("dq", "dtq") else N, D)) for n in ("dq", "dk", "dv", "dtq", "dtk", "dtv")}
+    for b in range(B):
+        for h in range(H):
+            if heads is not None and (b, h) not in heads:
+                continue
+            q, k, v, tq, tk, tv, do, dto = (x[n][b, h] for n in ("q", "k", "v", "tq", "tk", "tv", "do", "dto"))
+            O, L, tO = oracle.attention_jvp(q, k, v, tq, tk, tv, causal, sm_scale)
+            fin = np.isfinite(L)
+            S = np.where(keep, s * q @ k.T, -np.inf)
+            P = np.zeros_like(S)
+            P[fin] = np.exp(S[fin] - L[fin, None])
+            T = np.where(keep, s * (tq @ k.T + q @ tk.T), 0.0)
+            mu = (P * T).sum(axis=1)
+            tP = P * (T - mu[:, None])
+            dT = P * (dto @ v.T - (dto * O).sum(axis=1)[:, None])
+            dS = P * (do @ v.T + dto @ tv.T - ((do * O).sum(axis=1) + (dto * tO).sum(axis=1))[:, None]) \
+                + (T - mu[:, None]) * dT
+            r_d2 = u * np.sqrt(((do * O) ** 2 + (dto * tO) ** 2 + (dto * ((P * np.abs(T)) @ np.abs(v))) ** 2)
+                               .sum(axis=1))
+            r_e = u * np.sqrt(((dto * O) ** 2).sum(axis=1))
+            mdS = P * (r_d2[:, None] + np.abs(T - mu[:, None]) * r_e[:, None]) + u * np.abs(dS)
+            mdT = P * r_e[:, None] + u * np.abs(dT)
+            g = oracle.attention_jvp_bwd(q, k, v, tq, tk, tv, do, dto, causal, sm_scale)
+            # independent roundings add in quadrature over the summed keys or
+            # queries: a 4-sigma allowance on the root of the summed squares
+            rs = lambda a, bb: 4.0 * np.sqrt(a ** 2 @ bb ** 2)
+            out["dq"][b, h] = s * (rs(mdS, k) + rs(mdT, tk)) + u * np.abs(g[0])
+            out["dk"][b, h] = s * (rs(mdS.T, q) + rs(mdT.T, tq)) + u * np.abs(g[1])
+            out["dv"][b, h] = u * (rs(P.T, do) + rs(np.abs(tP).T, dto)) + u * np.abs(g[2])
+            out["dtq"][b, h] = s * rs(mdT, k) + u * np.abs(g[3])
+            out["dtk"][b, h] = s * rs(mdT.T, q) + u * np.abs(g[4])
+            out["dtv"][b, h] = u * rs(P.T, dto) + u * np.abs(g[5])
+    return out
+
+
+def compare_bounded(name, got, ref, tol, bound):
+    """Asserts |got - ref| <= tol + bound element by element (same shapes)."""
+    g = to_np(got) if hasattr(got, "detach") else np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, f"{name}: shape {g.shape} vs {r.shape}"
+    excess = float((np.abs(g - r) - tol - bound).max())
+    assert excess <= 0, f"{name}: error exceeds {tol:.1e} + its bound by {excess:.3e}"

@@ -1,8 +1,10 @@
 """GPU parity of the backward of the JVP (attn_bwd_jvp) through the C ABI
 against the fp64 oracle: the gradients of <dO, O> + <dtO, tO> with respect to
-q, k, v and the tangents.  16-bit cases compare every element at the
-tolerance derived for it (max_abs 5e-2 fp16, 1e-1 bf16, unit-normal inputs;
-see jvp_grad_tol); the fp32 mode at 1e-4.
+q, k, v and the tangents.  16-bit cases compare every element against the
+gradients' 5e-2 (unit-normal inputs) plus a bound derived element by element
+from the roundings the kernels make (jvp_bwd_bounds: the row constants from
+the stored O and tO, the 16-bit MMA operands, the output); the fp32 mode at
+1e-4.
 The forward outputs (o, lse, to, tlse) are the GPU's own attn_fwd_jvp."""
 import numpy as np
 import pytest
@@ -10,7 +12,7 @@ import torch
 
 import oracle
 import synth_inputs as si
-from _parity import TOL, compare, inputs, jvp_grad_tol, sample_heads
+from _parity import ROUND_U, TOL, compare, compare_bounded, inputs, jvp_bwd_bounds, sample_heads
 
 pytestmark = pytest.mark.gpu
 
@@ -44,8 +46,9 @@ def test_jvp_backward_small(gpu_lib, B, H, M, N, D, dtype, causal):
     cpu, g = inputs(B, H, M, N, D, dtype, 61, NAMES)
     grads = _run(gpu_lib, g, causal)
     ref = oracle.attention_jvp_bwd_bhsd(*(cpu[n] for n in NAMES), causal)
+    bounds = jvp_bwd_bounds(cpu, causal, ROUND_U[dtype])
     for name, got, r in zip(GRADS, grads, ref):
-        compare(name, got, r, jvp_grad_tol(dtype))
+        compare_bounded(name, got, r, TOL["grad"], bounds[name])
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -56,9 +59,11 @@ def test_jvp_backward_fp16_b2_h8_s1024_d64(gpu_lib, causal):
     grads = _run(gpu_lib, g, causal)
     heads = sample_heads(B, H, 3)
     ref = oracle.attention_jvp_bwd_bhsd(*(cpu[n] for n in NAMES), causal, heads=heads)
+    bounds = jvp_bwd_bounds(cpu, causal, ROUND_U["f16"], heads=heads)
     for name, got, r in zip(GRADS, grads, ref):
-        compare(name, np.stack([got[b, h].float().cpu().numpy() for b, h in heads]),
-                np.stack([r[b, h] for b, h in heads]), jvp_grad_tol("f16"))
+        compare_bounded(name, np.stack([got[b, h].float().cpu().numpy() for b, h in heads]),
+                        np.stack([r[b, h] for b, h in heads]), TOL["grad"],
+                        np.stack([bounds[name][b, h] for b, h in heads]))
 
 
 @pytest.mark.parametrize("B,H,M,N,D,causal", [(1, 2, 128, 128, 64, False), (1, 1, 200, 333, 128, True),
