@@ -63,3 +63,84 @@ def test_uniform_attention_every_element_full_size(gpu_lib, causal, dtype, D):
         _, _, dQr = oracle.attention_rows(np.zeros((S, D)), cpu["k"][0, h], cpu["v"][0, h], cpu["do"][0, h], rows,
                                           causal)
         compare(f"dQ rows [head {h}]", dq[0, h, rows], dQr, TOL["grad"])
+
+
+def test_piecewise_uniform_every_element_full_size(gpu_lib):
+    """The piecewise workload's shape (B=2, H=16, M=N=4096, D=64, bf16,
+    causal, w=512) with q1 = q2 = 0: the near and the far scores are both 0,
+    so the closed forms above hold whatever the threshold, dk1 = dk2 = 0
+    exactly, and dq1 / dq2 split dQ by distance (rows of two heads against
+    the oracle)."""
+    ta = gpu_lib
+    Bp, Hp, Sp, Dp, w = 2, 16, 4096, 64, 512
+    cpu, g = inputs(Bp, Hp, Sp, Sp, Dp, "bf16", 88, ("k1", "k2", "v", "do"))
+    q = torch.zeros_like(g["k1"])
+    o, lse = ta.piecewise_fwd(q, g["k1"], q, g["k2"], g["v"], w, True)
+    dq1, dk1, dq2, dk2, dv = ta.piecewise_bwd(q, g["k1"], q, g["k2"], g["v"], o, lse, g["do"], w, True)
+    assert ta.sync_status() == "TA_OK"
+    u = ROUND_U["bf16"]
+    n = torch.arange(1, Sp + 1, dtype=torch.float64)[:, None]
+    compare("O", o, (cpu["v"].double().cumsum(2) / n).numpy(), 1e-5, u)
+    compare("L", lse, np.broadcast_to(np.log(n[:, 0].numpy()), (Bp, Hp, Sp)), 1e-5)
+    compare("dv", dv, (cpu["do"].double() / n).flip(2).cumsum(2).flip(2).numpy(), TOL["grad"], u)
+    assert torch.all(dk1 == 0) and torch.all(dk2 == 0), "dk1, dk2 must be exactly 0 when q1 = q2 = 0"
+    rows = [0, 511, 512, 513, 2047, 4095]
+    zero = np.zeros((Sp, Dp))
+    for b, h in ((0, 0), (Bp - 1, Hp - 1)):
+        x = [zero, cpu["k1"][b, h], zero, cpu["k2"][b, h], cpu["v"][b, h], cpu["do"][b, h]]
+        ref = oracle.piecewise_bwd(*x, True, None, w)
+        compare(f"dq1 rows [{b},{h}]", dq1[b, h, rows], ref[0][rows], TOL["grad"])
+        compare(f"dq2 rows [{b},{h}]", dq2[b, h, rows], ref[2][rows], TOL["grad"])
+
+
+def test_fp8_forward_uniform_every_element_full_size(gpu_lib):
+    """The e5m2 forward at the benchmark size (B=1, H=32, M=N=8192, D=128,
+    causal) with q = 0: P = 1 is exact in e5m2, so O is the running mean of v
+    up to the fp32 sums and the output's e5m2 rounding, and L = ln(i + 1)."""
+    import synth_inputs as si
+    ta = gpu_lib
+    v = si.randn((B, H, S, 128), "e5m2", si.seed_for(87, 0))
+    k = si.randn((B, H, S, 128), "e5m2", si.seed_for(87, 1))
+    q = torch.zeros(B, H, S, 128, dtype=torch.uint8).view(torch.float8_e5m2)
+    vt = v.view(torch.uint8).transpose(-1, -2).contiguous().view(torch.float8_e5m2)
+    o, lse = ta.attn_fwd_fp8(q.cuda(), k.cuda(), vt.cuda(), True)
+    assert ta.sync_status() == "TA_OK"
+    n = torch.arange(1, S + 1, dtype=torch.float64)[:, None]
+    O = (v.to(torch.float64).cumsum(2) / n).numpy()
+    got = o.cpu().to(torch.float64).numpy()
+    # one e5m2 rounding: 2^-3 relative, or half the subnormal spacing 2^-16
+    # below the smallest normal 2^-14
+    assert np.all(np.abs(got - O) <= 2.0 ** -3 * np.abs(O) + 2.0 ** -17), "O outside one e5m2 rounding of the mean"
+    compare("L", lse, np.broadcast_to(np.log(n[:, 0].numpy()), (B, H, S)), 1e-5)
+
+
+def test_merge_equal_lse_every_element_full_size(gpu_lib):
+    """The merge at the benchmark's state size (B=1, H=32, M=8192, D=128,
+    bf16): two states with equal L merge to O = (O1 + O2)/2 and L + ln 2,
+    and with dL = 0 the backward gives dO1 = dO2 = dO/2 and dL1 = -dL2 =
+    <dO, O1 - O2>/4; rows where both parts saw no key stay O = 0, L = -inf."""
+    import synth_inputs as si
+    ta = gpu_lib
+    o1, o2, do = (si.randn((B, H, S, 128), "bf16", si.seed_for(86, i)) for i in range(3))
+    lse = si.randn((B, H, S), "f32", si.seed_for(86, 3)) * 3
+    lse[..., 5] = -float("inf")
+    o1[..., 5, :] = 0
+    o2[..., 5, :] = 0
+    g = [t.cuda() for t in (o1, lse, o2, lse, do)]
+    mo, ml = ta.merge_fwd(*g[:4])
+    d1, l1, d2, l2 = ta.merge_bwd(*g, None)
+    assert ta.sync_status() == "TA_OK"
+    u = ROUND_U["bf16"]
+    a, b, dd = (t.double() for t in (o1, o2, do))
+    # the weights 1/2 come from exp(l - L) in fp32 (relative error ~2^-22),
+    # then one rounding of the stored result
+    compare("O", mo, ((a + b) / 2).numpy(), 1e-5, u)
+    compare("L", ml, (lse.double() + np.log(2.0)).numpy(), 1e-5)
+    half = (dd / 2).numpy()
+    half[..., 5, :] = 0
+    compare("dO1", d1, half, 1e-5, u)
+    compare("dO2", d2, half, 1e-5, u)
+    t = ((dd * (a - b)).sum(-1) / 4).numpy()
+    t[..., 5] = 0
+    compare("dL1", l1, t, 1e-4, 2.0 ** -20)
+    compare("dL2", l2, -t, 1e-4, 2.0 ** -20)
