@@ -172,6 +172,20 @@ static ta_status check_ptrs(std::initializer_list<const void*> ps) {
 
 static ta_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TA_OK : TA_ERR_CUDA; }
 
+// Heads per group of the two-tile forward's tile order (grouped_tile): as
+// many as keep the group's K and V within a quarter of the 129 MB L2, so the
+// CTAs resident at once re-read them from L2, but at least kGroupHeads.
+// Larger groups put more of the heaviest causal tiles first: with groups of
+// 8 heads at B4 H16 S2048 the last group's heaviest tiles start late and the
+// SMs sit idle a fifth of the time (groups of 32 there; 8 at B1 H32 S8192).
+static int fwd_group_heads(const Problem& p) {
+  const long long per_head = 2ll * p.N * p.D * p.esize;
+  long long g = per_head > 0 ? (32ll << 20) / per_head : p.BH;
+  if (g < kGroupHeads) g = kGroupHeads;
+  if (g > p.BH) g = p.BH;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
 static FwdArgs fwd_args(const Problem& p, int causal, int w, void* o, float* lse, void* to, float* tlse) {
   FwdArgs a;
   a.o = o;
@@ -185,6 +199,7 @@ static FwdArgs fwd_args(const Problem& p, int causal, int w, void* o, float* lse
   a.num_q_tiles = (p.M + kBM - 1) / kBM;
   a.causal = causal ? 1 : 0;
   a.w = w;
+  a.group_heads = fwd_group_heads(p);
   a.sm_scale = p.sm_scale;
   a.scale_log2 = p.sm_scale * kLog2e;
   a.dg = p.D;

@@ -31,6 +31,7 @@ struct FwdArgs {
   int num_q_tiles;
   int causal;
   int w;          // piecewise threshold
+  int group_heads;   // heads per group of the two-tile forward's tile order (grouped_tile)
   float scale_log2;  // sm_scale * log2(e)
   float sm_scale;
   int dg;            // head dimension of the tensors in memory (row stride, columns stored)

@@ -570,7 +570,7 @@ __device__ __forceinline__ void fwd2_body(const CUtensorMap& tm_q, const CUtenso
   const int lane = threadIdx.x & 31;
   const int pairs = (args.M + 2 * kBM - 1) / (2 * kBM);
   int bh, rank;
-  grouped_tile(blockIdx.x, args.BH, pairs, kGroupHeads, &bh, &rank);
+  grouped_tile(blockIdx.x, args.BH, pairs, args.group_heads, &bh, &rank);
   const int pair = pairs - 1 - rank;  // heaviest causal pairs first
   const int q0 = pair * 2 * kBM;
   int n_t[2];
