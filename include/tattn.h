@@ -40,6 +40,12 @@
  *    default stream).  Argument errors are reported synchronously before any
  *    launch; a bounded-wait timeout inside a kernel is recorded in a device
  *    error word that ta_sync_status() reads.
+ *  - Host threads may call the entry points concurrently (the library's
+ *    per-device set-up is idempotent and its caches are atomic).  A thread
+ *    needs no CUDA set-up of its own: with no current context, a call binds
+ *    the current device's primary context first.  The device error word is
+ *    shared by every call on a device, and ta_profile_* expect one host
+ *    thread issuing the calls they time.
  */
 #ifndef TATTN_H_
 #define TATTN_H_

@@ -1,6 +1,7 @@
 // C ABI of libtattn.so: argument validation, TMA tensor-map encoding, kernel
 // dispatch, the device error word behind the bounded waits, and per-kernel
 // CUDA-event timing.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -19,15 +20,17 @@ namespace ta {
 static __device__ uint32_t g_err_word;
 
 static uint32_t* error_word_ptr() {
-  static uint32_t* cache[64] = {};
+  static std::atomic<uint32_t*> cache[kMaxDevices];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  uint32_t* w = cache[dev].load(std::memory_order_acquire);
+  if (!w) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<uint32_t*>(p);
+    w = static_cast<uint32_t*>(p);
+    cache[dev].store(w, std::memory_order_release);
   }
-  return cache[dev];
+  return w;
 }
 
 static uint64_t g_timeout_ns = [] {
@@ -56,13 +59,37 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// The driver call that encodes tensor maps needs a current context.  A host
+// thread whose first CUDA work is a call into this library has none yet
+// (cudaGetDevice and the cached look-ups bind nothing), so when the thread
+// has no current context the current device's primary context is bound
+// first (cudaSetDevice does that).  A thread that has one, including one in
+// the middle of a stream capture, is left as it is.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+static bool ensure_context() {
+  static CtxGetCurrentFn get = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (get && get(&c) == CUDA_SUCCESS && c != nullptr) return true;
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess && cudaSetDevice(dev) == cudaSuccess;
+}
+
 // [BH, S, D] 16-bit tensor viewed as a 3-D map with 64 x box_rows x 1 boxes
 // and 128-byte swizzle; rows past S (and, for D < 64, columns past D) read as
 // zeros.
 static bool make_map(CUtensorMap* map, const void* ptr, long long BH, long long S, int D, bool bf16,
                      int box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || !ensure_context()) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(S) * D * 2};
   cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
@@ -80,7 +107,7 @@ static bool make_map(CUtensorMap* map, const void* ptr, long long BH, long long 
 static bool make_map_u8(CUtensorMap* map, const void* ptr, long long BH, long long rows, long long cols, int box_cols,
                         int box_rows) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || !ensure_context()) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows * cols)};
   cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
@@ -97,7 +124,7 @@ struct ProfRec {
   cudaEvent_t a, b;
 };
 static std::mutex g_prof_mu;
-static bool g_prof_on = false;
+static std::atomic<bool> g_prof_on{false};
 static std::vector<ProfRec> g_prof_recs;
 static std::vector<cudaEvent_t> g_prof_pool;
 static size_t g_prof_pool_next = 0;

@@ -80,14 +80,14 @@ __global__ void __launch_bounds__(256) jvp_delta_kernel(const uint4* __restrict_
 
 // SM count of the current device (cached per device).
 static int sm_count() {
-  static int cache[kMaxDevices] = {};
+  static std::atomic<int> cache[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-  int* n = (dev >= 0 && dev < kMaxDevices) ? &cache[dev] : nullptr;
-  int v = n ? *n : 0;
+  std::atomic<int>* n = (dev >= 0 && dev < kMaxDevices) ? &cache[dev] : nullptr;
+  int v = n ? n->load(std::memory_order_relaxed) : 0;
   if (v <= 0) {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
-    if (n) *n = v;
+    if (n) n->store(v, std::memory_order_relaxed);
   }
   return v;
 }

@@ -1503,7 +1503,7 @@ template <typename T, int MODE, int D, int PART = -1>
 static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DkdvCfg<MODE, D, PART>;
   auto kern = attn_bwd_dkdv_kernel<T, MODE, D, PART>;
-  static bool attr[kMaxDevices] = {};
+  static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
@@ -1516,7 +1516,7 @@ template <typename T, int MODE, int D>
 static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DqCfg<MODE, D>;
   auto kern = attn_bwd_dq_kernel<T, MODE, D>;
-  static bool attr[kMaxDevices] = {};
+  static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
@@ -1529,7 +1529,7 @@ template <typename T, int D>
 static cudaError_t launch_dkdv_std_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DkdvStdCfg<D>;
   auto kern = attn_bwd_dkdv_std_kernel<T, D>;
-  static bool attr[kMaxDevices] = {};
+  static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
@@ -1556,7 +1556,7 @@ template <typename T, int D>
 static cudaError_t launch_dq_std_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DqStdCfg<D>;
   auto kern = attn_bwd_dq_std_kernel<T, D>;
-  static bool attr[kMaxDevices] = {};
+  static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);

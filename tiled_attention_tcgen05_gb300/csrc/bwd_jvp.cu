@@ -493,7 +493,7 @@ template <typename T, bool KEYS, int D>
 static cudaError_t launch_jvp_bwd_t(const JvpBwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = JvpBwdCfg<D>;
   auto kern = attn_bwd_jvp_kernel<T, KEYS, D, jvp_tangents_fit<D, KEYS>()>;
-  static bool attr[kMaxDevices] = {};
+  static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   const int rows = KEYS ? a.N : a.M;

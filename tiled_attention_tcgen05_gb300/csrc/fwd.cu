@@ -892,7 +892,7 @@ template <typename T, int MODE, int D>
 static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<MODE, D>;
   auto kern = attn_fwd_kernel<T, MODE, D>;
-  static bool attr[kMaxDevices] = {};
+  static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   dim3 grid(a.BH, a.num_q_tiles);
@@ -903,7 +903,7 @@ static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStrea
 template <typename T, int D, bool PW = false>
 static cudaError_t launch_fwd2_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
   using C = Fwd2Cfg<D, PW>;
-  static bool attr[kMaxDevices] = {};
+  static std::atomic<bool> attr[kMaxDevices];
   const long long pairs = (a.M + 2 * kBM - 1) / (2 * kBM);
   const long long blocks = pairs * a.BH;
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;

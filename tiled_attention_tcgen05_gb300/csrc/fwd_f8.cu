@@ -345,7 +345,7 @@ template <int D>
 static cudaError_t launch_fwd_f8_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
   using C = F8Cfg<D>;
   auto kern = attn_fwd_f8_kernel<D>;
-  static bool attr[kMaxDevices] = {};
+  static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   const long long pairs = (a.M + 2 * kBM - 1) / (2 * kBM);

@@ -1,6 +1,7 @@
 // Host-side declarations shared by the kernel translation units and the
 // C-ABI layer.
 #pragma once
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -82,15 +83,18 @@ cudaError_t launch_merge(bool bwd, int dtype, int D, const MergePtrs& p, long lo
 // drives several GPUs sets it on each); `done` is the caller's per-kernel
 // table.
 constexpr int kMaxDevices = 64;
+// Per-device flags and caches are atomics: host threads may make their
+// first calls on a device at the same time (each then does the idempotent
+// set-up itself).
 template <typename K>
-inline cudaError_t smem_attr_once(K kern, int bytes, bool (&done)[kMaxDevices]) {
+inline cudaError_t smem_attr_once(K kern, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const bool tracked = dev >= 0 && dev < kMaxDevices;
-  if (tracked && done[dev]) return cudaSuccess;
+  if (tracked && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && tracked) done[dev] = true;
+  if (e == cudaSuccess && tracked) done[dev].store(true, std::memory_order_release);
   return e;
 }
 
