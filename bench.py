@@ -46,17 +46,23 @@ def step_flops(w=WORKLOAD):
 def kernel_algorithmic(name, w=WORKLOAD):
     """(bound, per-launch algorithmic FLOPs or bytes) of each library kernel.
 
-    attn_fwd: the forward's two matmuls.  attn_bwd_dkdv: four of the
-    backward's five algorithmic matmuls (S^T recompute, dP^T, dV, dK).
+    attn_fwd: the forward's two matmuls.  attn_bwd_fused: all five of the
+    backward's matmuls (S^T recompute, dP^T, dV, dK, dQ^T).  The two-pass
+    backward's attn_bwd_dkdv: four of them (S^T recompute, dP^T, dV, dK);
     attn_bwd_dq: the dQ matmul (its S and dP recomputes are extra work, not
-    counted).  bwd_delta: bytes of O and dO read plus delta written."""
+    counted).  bwd_delta: bytes of O and dO read plus delta written (the
+    step's two-pass backward; attn_bwd_fused's delta pass also zeroes its
+    fp32 dQ accumulator).  bwd_dq_convert: the accumulator read, dQ
+    written."""
     f = flops_fwd(w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"])
     rows = w["B"] * w["H"] * w["M"]
     table = {
         "attn_fwd": ("tensor", f),
+        "attn_bwd_fused": ("tensor", 2.5 * f),
         "attn_bwd_dkdv": ("tensor", 2.0 * f),
         "attn_bwd_dq": ("tensor", 0.5 * f),
         "bwd_delta": ("hbm", rows * w["D"] * 2 * 2 + rows * 4),
+        "bwd_dq_convert": ("hbm", rows * w["D"] * (4 + 2)),
     }
     return table.get(name)
 
@@ -306,6 +312,40 @@ def fp8_measure(ta, torch, si, dev, stream, w, bf16_peak, iters=10):
     return {"ms": ms, "flops": flops, "achieved": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peak,
             "peak_source": "measured bf16 burst x 2 (nominal fp8 / bf16)", "frac": tf / peak,
             "workload": "e5m2 forward, B1 H32 M=N=8192 D128 causal (L2 flushed before each timed launch)"}
+
+
+def bwd_fused_measure(ta, torch, dev, stream, g, o, lse, w, bf16_peak, iters=10):
+    """Times the two backward paths on the benchmark's shape and inputs,
+    outside the step's timed region, alternating calls (L2 flushed before
+    each): attn_bwd (delta, dK/dV pass, dQ pass) and attn_bwd_fused (delta,
+    one key-stationary pass with the fp32 dQ accumulator, dQ conversion).
+    Both against the backward's algorithmic FLOPs (2.5x the forward)."""
+    flops = 2.5 * flops_fwd(w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    bufs = {"two_pass": [torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])],
+            "fused": [torch.empty_like(g["q"]), torch.empty_like(g["k"]), torch.empty_like(g["v"])]}
+    calls = {"two_pass": ta.attn_bwd, "fused": ta.attn_bwd_fused}
+    for name, fn in calls.items():
+        for _ in range(2):
+            fn(g["q"], g["k"], g["v"], o, lse, g["do"], w["causal"], None, *bufs[name], stream=stream)
+    torch.cuda.synchronize(dev)
+    ms = {n: 0.0 for n in calls}
+    with torch.cuda.stream(stream):
+        for _ in range(iters):
+            for name, fn in calls.items():
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn(g["q"], g["k"], g["v"], o, lse, g["do"], w["causal"], None, *bufs[name], stream=stream)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ms[name] += e0.elapsed_time(e1) / iters
+    out = {"workload": "backward alone, B1 H32 M=N=8192 D128 bf16 causal (L2 flushed before each call)",
+           "flops": flops, "unit": "TFLOP/s", "peak": bf16_peak}
+    for name in calls:
+        tf = flops / (ms[name] * 1e-3) / 1e12
+        out[name] = {"ms": ms[name], "achieved": tf, "frac": tf / bf16_peak}
+    return out
 
 
 def jvp_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
@@ -583,6 +623,7 @@ def run_ours(args, rank, world, local_rank):
 
     merge = merge_measure(ta, torch, dev, stream, o, lse, dq, g["do"], hbm_peak)
     fp8 = fp8_measure(ta, torch, si, dev, stream, w, bf16_peak)
+    bwd_paths = bwd_fused_measure(ta, torch, dev, stream, g, o, lse, w, bf16_peak)
     jvp = jvp_measure(ta, torch, si, dev, stream, bf16_peak)
     other = configs_measure(ta, torch, si, dev, stream, bf16_peak)
     if ta.sync_status(stream) != "TA_OK":
@@ -623,6 +664,7 @@ def run_ours(args, rank, world, local_rank):
         "kernels": kernels,
         "merge": merge,
         "fp8_fwd": fp8,
+        "bwd_paths": bwd_paths,
         "jvp": jvp,
         "other_workloads": other,
         "cpu_baseline": {"value": cpu_f / cpu_secs / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),

@@ -89,6 +89,31 @@ ta_status attn_bwd(const void* q, const void* k, const void* v, const void* o, c
                    const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H,
                    int M, int N, int D, ta_dtype dt, int causal, float sm_scale, void* stream);
 
+/* Bytes of workspace attn_bwd_fused needs: delta [B,H,M] fp32 (padded to 256
+ * bytes) followed by the fp32 dQ accumulator [B,H,M,D] (D = 128 in 16-bit;
+ * delta alone otherwise, where attn_bwd_fused returns TA_ERR_UNSUPPORTED). */
+size_t attn_bwd_fused_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt);
+
+/* attn_bwd in one key-stationary pass: five matmuls per (key, query) block
+ * pair (S^T, dP^T, dV, dK and dQ^T = K^T dS^T) instead of the seven of the
+ * separate dK/dV and dQ passes.  [FA-JVP] _attn_bwd computes dK/dV of its key
+ * block and dQ of its query block in one program, each recomputing S and dP;
+ * here the key block's CTA adds its dQ contribution into an fp32 accumulator
+ * in `ws` with atomics, and a final pass writes dq = sm_scale * acc in dt.
+ * Same arguments and outputs as attn_bwd.
+ *  - dt TA_F16 / TA_BF16 and D = 128 only; anything else returns
+ *    TA_ERR_UNSUPPORTED before any launch.
+ *  - ws: >= attn_bwd_fused_workspace_bytes(...) bytes, 16-byte aligned,
+ *    contents need not be initialised (the delta pass zeroes the accumulator).
+ *  - dq's fp32 summation order depends on the order the atomics land in, so
+ *    dq may differ between calls in its last bit; dk, dv and lse-related
+ *    outputs are deterministic.
+ *  - attn_bwd (the two passes) is the faster path on GB300 at the benchmark
+ *    shapes; this entry point is the five-matmul alternative. */
+ta_status attn_bwd_fused(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H,
+                         int M, int N, int D, ta_dtype dt, int causal, float sm_scale, void* stream);
+
 /* attn_bwd for callers that cannot allocate device memory or pass a
  * workspace (for example a host framework that has reserved all device memory
  * for its own pool, or a step loop that must not call cudaMalloc because it

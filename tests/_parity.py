@@ -52,6 +52,19 @@ def compare(name, got, ref, tol, round_u=0.0):
     return max_abs, max_rel
 
 
+def assert_same_up_to_summation_order(name, got, ref):
+    """Two results of the same call that may differ only in the order of an
+    fp32 sum (the fused backward adds dQ's per-key-tile contributions with
+    atomics): equal up to one unit in the last place of their 16-bit type,
+    i.e. |got - ref| <= 2 u |ref| (u the unit roundoff) plus 2^-20 for
+    values near zero, where the fp32 sums' own difference shows."""
+    u = {torch.bfloat16: ROUND_U["bf16"], torch.float16: ROUND_U["f16"], torch.float32: 2.0 ** -24}[got.dtype]
+    a, b = got.detach().double(), ref.detach().double()
+    assert a.shape == b.shape, f"{name}: shape {tuple(a.shape)} vs {tuple(b.shape)}"
+    excess = float(((a - b).abs() - 2 * u * b.abs() - 2.0 ** -20).max()) if a.numel() else 0.0
+    assert excess <= 0, f"{name}: differs by more than the last place (excess {excess:.3e})"
+
+
 def heads_of(x, heads):
     """Stack the selected (b, h) slices of a [B, H, ...] array/tensor."""
     a = to_np(x) if hasattr(x, "detach") else np.asarray(x)

@@ -72,11 +72,26 @@ def test_backward_workspace_and_validation(lib):
     vp = ctypes.c_void_p
     assert lib.attn_bwd_workspace_bytes(1, 32, 8192, 8192, 128, BF16) == 32 * 8192 * 4
     assert lib.attn_bwd_workspace_bytes(1, 1, 3, 3, 64, F16) == 256
+    # the fused backward: delta, then the fp32 dQ accumulator (D = 128, 16-bit)
+    assert lib.attn_bwd_fused_workspace_bytes(1, 32, 8192, 8192, 128, BF16) == 32 * 8192 * 4 + 32 * 8192 * 128 * 4
+    assert lib.attn_bwd_fused_workspace_bytes(1, 1, 3, 3, 128, F16) == 256 + 3 * 128 * 4
+    assert lib.attn_bwd_fused_workspace_bytes(1, 1, 3, 3, 128, F32) == 256
+    assert lib.attn_bwd_fused_workspace_bytes(0, 1, 3, 3, 128, F16) == 0
     assert lib.attn_bwd_workspace_bytes(0, 1, 3, 3, 64, F16) == 0
     p = [vp(16 * (i + 1)) for i in range(10)]
     st = lib.attn_bwd(*p[:9], vp(0), 1024, 1, 1, 128, 128, 64, BF16, 1, -1.0, vp(0))
     assert st == INVALID  # null workspace
     st = lib.attn_bwd(*p[:9], vp(0x2008), 1024, 1, 1, 128, 128, 64, BF16, 1, -1.0, vp(0))
+    assert st == ALIGNMENT
+    # attn_bwd_fused: a workspace with room for delta alone is refused before any
+    # launch; head sizes other than 128 and the fp32 mode are not supported
+    st = lib.attn_bwd_fused(*p[:9], vp(0x4000), 512, 1, 1, 128, 128, 128, BF16, 1, -1.0, vp(0))
+    assert st == INVALID
+    st = lib.attn_bwd_fused(*p[:9], vp(0x4000), 1 << 20, 1, 1, 128, 128, 64, BF16, 1, -1.0, vp(0))
+    assert st == UNSUPPORTED
+    st = lib.attn_bwd_fused(*p[:9], vp(0x4000), 1 << 20, 1, 1, 128, 128, 128, F32, 1, -1.0, vp(0))
+    assert st == UNSUPPORTED
+    st = lib.attn_bwd_fused(*p[:9], vp(0x4008), 1 << 20, 1, 1, 128, 128, 128, BF16, 1, -1.0, vp(0))
     assert st == ALIGNMENT
     # a head size outside {16, 32, 64, 128} is refused before any launch
     q = [vp(16 * (i + 1)) for i in range(14)]

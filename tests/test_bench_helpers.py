@@ -12,15 +12,20 @@ def test_step_flops_is_the_causal_fwd_plus_bwd_count():
 
 
 def test_kernel_algorithmic_work_adds_up_to_the_step():
-    """The tensor kernels' algorithmic FLOPs (forward 2 matmuls, dK/dV 4,
-    dQ 1 of the backward's 5) sum to the step's 7 matmul-equivalents; the
-    delta kernel's bytes are O and dO read plus delta written."""
-    f = [bench.kernel_algorithmic(k) for k in ("attn_fwd", "attn_bwd_dkdv", "attn_bwd_dq")]
-    assert all(b == "tensor" for b, _ in f)
-    assert abs(sum(x for _, x in f) - bench.step_flops()) < 1.0
+    """The tensor kernels' algorithmic FLOPs sum to the step's 7
+    matmul-equivalents either way the backward runs: forward 2 + dK/dV 4 +
+    dQ 1 (the step's attn_bwd), or forward 2 + fused backward 5
+    (attn_bwd_fused).  The delta kernel's bytes are O and dO read plus delta
+    written; the fused path's convert pass reads the fp32 accumulator and
+    writes dQ."""
+    for names in (("attn_fwd", "attn_bwd_fused"), ("attn_fwd", "attn_bwd_dkdv", "attn_bwd_dq")):
+        f = [bench.kernel_algorithmic(k) for k in names]
+        assert all(b == "tensor" for b, _ in f)
+        assert abs(sum(x for _, x in f) - bench.step_flops()) < 1.0
     w = bench.WORKLOAD
     rows = w["B"] * w["H"] * w["M"]
     assert bench.kernel_algorithmic("bwd_delta") == ("hbm", rows * w["D"] * 2 * 2 + rows * 4)
+    assert bench.kernel_algorithmic("bwd_dq_convert") == ("hbm", rows * w["D"] * 6)
     assert bench.kernel_algorithmic("no_such_kernel") is None
 
 

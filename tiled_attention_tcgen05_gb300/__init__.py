@@ -8,6 +8,7 @@ library is missing or fails to load, every call raises.
 Entry points (same names as the C ABI):
   attn_fwd(q, k, v, causal, sm_scale)                -> (o, lse)
   attn_bwd(q, k, v, o, lse, do, causal, sm_scale)    -> (dq, dk, dv)
+  attn_bwd_fused(q, k, v, o, lse, do, causal, sm_scale) -> (dq, dk, dv)  [D = 128]
   attn_fwd_jvp(q, k, v, tq, tk, tv, causal, sm_scale, with_tlse) -> (o, lse, to[, tlse])
   attn_bwd_jvp(q, k, v, tq, tk, tv, o, lse, to, tlse, do, dto, causal, sm_scale)
                                                      -> (dq, dk, dv, dtq, dtk, dtv)
@@ -24,8 +25,8 @@ import os
 
 import torch
 
-__all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_fwd_jvp", "attn_bwd_jvp", "piecewise_fwd", "piecewise_bwd", "merge_fwd", "merge_bwd", "attn_fwd_fp8",
-           "attn_bwd_workspace_bytes", "sync_status", "selftest_wait_timeout", "profile_enable",
+__all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_bwd_fused", "attn_fwd_jvp", "attn_bwd_jvp", "piecewise_fwd", "piecewise_bwd", "merge_fwd", "merge_bwd", "attn_fwd_fp8",
+           "attn_bwd_workspace_bytes", "attn_bwd_fused_workspace_bytes", "sync_status", "selftest_wait_timeout", "profile_enable",
            "profile_read", "set_wait_timeout_ms", "TAError", "STATUS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -41,6 +42,8 @@ _SIGS = {
     "attn_fwd": ([_vp] * 5 + [_i] * 7 + [_f, _vp], _i),
     "attn_bwd_workspace_bytes": ([_i] * 6, _sz),
     "attn_bwd": ([_vp] * 10 + [_sz] + [_i] * 7 + [_f, _vp], _i),
+    "attn_bwd_fused_workspace_bytes": ([_i] * 6, _sz),
+    "attn_bwd_fused": ([_vp] * 10 + [_sz] + [_i] * 7 + [_f, _vp], _i),
     "attn_fwd_jvp": ([_vp] * 10 + [_i] * 7 + [_f, _vp], _i),
     "attn_bwd_jvp_workspace_bytes": ([_i] * 6, _sz),
     "attn_bwd_jvp": ([_vp] * 19 + [_sz] + [_i] * 7 + [_f, _vp], _i),
@@ -132,6 +135,10 @@ def attn_bwd_workspace_bytes(B, H, M, N, D, dtype=torch.bfloat16) -> int:
     return int(load().attn_bwd_workspace_bytes(B, H, M, N, D, _DT[dtype]))
 
 
+def attn_bwd_fused_workspace_bytes(B, H, M, N, D, dtype=torch.bfloat16) -> int:
+    return int(load().attn_bwd_fused_workspace_bytes(B, H, M, N, D, _DT[dtype]))
+
+
 def attn_fwd(q, k, v, causal=False, sm_scale=None, o=None, lse=None, stream=None):
     lib = load()
     B, H, M, N, D, dt = _prep({"q": q, "k": k, "v": v}, ("q",), ("k", "v"))
@@ -155,6 +162,25 @@ def attn_bwd(q, k, v, o, lse, do, causal=False, sm_scale=None, dq=None, dk=None,
     _check("attn_bwd", lib.attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
                                     _ptr(dk), _ptr(dv), _ptr(ws), ws.numel() * ws.element_size(), B, H, M, N,
                                     D, dt, int(bool(causal)), _scale(sm_scale), _stream(stream)))
+    return dq, dk, dv
+
+
+def attn_bwd_fused(q, k, v, o, lse, do, causal=False, sm_scale=None, dq=None, dk=None, dv=None, ws=None,
+                   stream=None):
+    """attn_bwd in one key-stationary pass (five matmuls per block pair; dq
+    summed in fp32 with atomics).  D = 128, float16/bfloat16."""
+    lib = load()
+    B, H, M, N, D, dt = _prep({"q": q, "k": k, "v": v, "o": o, "do": do}, ("q", "o", "do"), ("k", "v"))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    nws = int(lib.attn_bwd_fused_workspace_bytes(B, H, M, N, D, dt))
+    if ws is None:
+        ws = torch.empty(max(nws, 16), device=q.device, dtype=torch.uint8)
+    _check("attn_bwd_fused", lib.attn_bwd_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                                ws.numel() * ws.element_size(), B, H, M, N, D, dt,
+                                                int(bool(causal)), _scale(sm_scale), _stream(stream)))
     return dq, dk, dv
 
 

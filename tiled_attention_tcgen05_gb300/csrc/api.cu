@@ -262,6 +262,17 @@ static size_t delta_bytes(long long BH, int M) {
   return (static_cast<size_t>(BH) * static_cast<size_t>(M) * sizeof(float) + 255) & ~size_t(255);
 }
 
+// attn_bwd_fused (16-bit, D = 128) runs the fused key-stationary kernel,
+// which adds dQ into an fp32 accumulator [BH, M, D] kept in the workspace
+// after delta.
+static bool bwd_fused_applies(int D, ta_dtype dt) {
+  return (dt == TA_F16 || dt == TA_BF16) && bwd_fused_supported(kernel_d(D)) && kernel_d(D) == D;
+}
+
+static size_t dq_acc_bytes(long long BH, int M, int D) {
+  return static_cast<size_t>(BH) * static_cast<size_t>(M) * static_cast<size_t>(D) * sizeof(float);
+}
+
 static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* k, const void* v,
                          const void* q2, const void* k2, const void* v2, void* o, float* lse, void* to,
                          float* tlse, int causal, int w, cudaStream_t s) {
@@ -302,7 +313,7 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
 static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* k, const void* v,
                          const void* q2, const void* k2, const void* o, const float* lse, const void* dO,
                          void* dq, void* dk, void* dq2, void* dk2, void* dv, void* ws, size_t ws_bytes,
-                         int causal, int w, cudaStream_t s) {
+                         int causal, int w, cudaStream_t s, bool fused = false) {
   if (p.BH == 0) return TA_OK;
   const bool pw = (mode == kPiecewise);
   const size_t kv_bytes = static_cast<size_t>(p.BH) * p.N * p.D * p.esize;
@@ -312,12 +323,15 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
     if (e == cudaSuccess && pw) e = launch_zero(dk2, kv_bytes, s);
     return cuda_status(e);
   }
-  if (ws_bytes < delta_bytes(p.BH, p.M)) return TA_ERR_INVALID_ARG;
+  const bool use_acc = fused && !pw && !p.f32 && p.N > 0;
+  const size_t db = delta_bytes(p.BH, p.M);
+  if (ws_bytes < db || (use_acc && ws_bytes - db < dq_acc_bytes(p.BH, p.M, p.D))) return TA_ERR_INVALID_ARG;
   float* delta = static_cast<float*>(ws);
+  float* acc = use_acc ? reinterpret_cast<float*>(static_cast<char*>(ws) + db) : nullptr;
   prof_begin("bwd_delta", s);
   cudaError_t e = p.f32 ? launch_f32_delta(p.D, static_cast<const float*>(o), static_cast<const float*>(dO),
                                            delta, p.BH * p.M, s)
-                        : launch_delta(p.bf16, p.D, o, dO, delta, p.BH * p.M, s);
+                        : launch_delta(p.bf16, p.D, o, dO, delta, p.BH * p.M, s, acc);
   prof_end(s);
   if (e != cudaSuccess) return TA_ERR_CUDA;
   const size_t q_bytes = static_cast<size_t>(p.BH) * p.M * p.D * p.esize;
@@ -353,6 +367,21 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
   a.dv = dv;
   a.dq2 = dq2;
   a.dk2 = dk2;
+  if (use_acc) {  // dK, dV and the dQ accumulator in one pass, then dQ = sm_scale * acc
+    BwdMaps fm = maps;  // Q and dO stream in steps of bwd_fused_step_rows() rows
+    if (!make_map(&fm.q, q, p.BH, p.M, p.D, p.bf16, bwd_fused_step_rows()) ||
+        !make_map(&fm.dO, dO, p.BH, p.M, p.D, p.bf16, bwd_fused_step_rows()))
+      return TA_ERR_CUDA;
+    a.dq_acc = acc;
+    prof_begin("attn_bwd_fused", s);
+    e = launch_bwd_fused(p.bf16, p.D, fm, a, s);
+    prof_end(s);
+    if (e != cudaSuccess) return TA_ERR_CUDA;
+    prof_begin("bwd_dq_convert", s);
+    e = launch_dq_convert(p.bf16, p.D, acc, dq, p.BH * p.M, p.sm_scale, s);
+    prof_end(s);
+    return cuda_status(e);
+  }
   prof_begin(pw ? "piecewise_bwd_dkdv" : "attn_bwd_dkdv", s);
   e = launch_bwd_dkdv(mode, p.bf16, kernel_d(p.D), maps, a, s);
   prof_end(s);
@@ -469,6 +498,23 @@ static ta_status run_bwd_jvp(const Problem& p, const void* q, const void* k, con
   e = launch_bwd_jvp(false, p.bf16, kd, jm, ap, s);
   prof_end(s);
   return cuda_status(e);
+}
+
+// attn_bwd with the choice of path: allow_fused = false keeps the two-pass
+// backward (dK/dV pass, then dQ pass), whose only scratch is delta.
+ta_status bwd_entry(bool allow_fused, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H, int M,
+                    int N, int D, ta_dtype dt, int causal, float sm_scale, void* stream) {
+  Problem p;
+  ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
+  if (st != TA_OK) return st;
+  if (p.BH == 0 || (M == 0 && N == 0)) return TA_OK;
+  if (M == 0) st = check_ptrs({dk, dv});
+  else if (N == 0) st = check_ptrs({o, dO, dq, ws});
+  else st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, ws});
+  if (st != TA_OK) return st;
+  return run_bwd(kStd, p, q, k, v, nullptr, nullptr, o, lse, dO, dq, dk, nullptr, nullptr, dv, ws, ws_bytes,
+                 causal, 0, static_cast<cudaStream_t>(stream), allow_fused && bwd_fused_applies(D, dt));
 }
 
 }  // namespace ta
@@ -611,27 +657,39 @@ size_t attn_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt) 
   return delta_bytes(static_cast<long long>(B) * H, M);
 }
 
+size_t attn_bwd_fused_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt) {
+  (void)N;
+  if (B <= 0 || H <= 0 || M <= 0) return 0;
+  const long long BH = static_cast<long long>(B) * H;
+  return delta_bytes(BH, M) + (bwd_fused_applies(D, dt) ? dq_acc_bytes(BH, M, D) : 0);
+}
+
 size_t piecewise_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt) {
-  return attn_bwd_workspace_bytes(B, H, M, N, D, dt);
+  (void)N;
+  (void)D;
+  (void)dt;
+  if (B <= 0 || H <= 0 || M <= 0) return 0;
+  return delta_bytes(static_cast<long long>(B) * H, M);
 }
 
 ta_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dO,
                    void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H, int M, int N, int D,
                    ta_dtype dt, int causal, float sm_scale, void* stream) {
-  Problem p;
-  ta_status st = check_common(B, H, M, N, D, dt, sm_scale, &p);
-  if (st != TA_OK) return st;
-  if (p.BH == 0 || (M == 0 && N == 0)) return TA_OK;
-  if (M == 0) st = check_ptrs({dk, dv});
-  else if (N == 0) st = check_ptrs({o, dO, dq, ws});
-  else st = check_ptrs({q, k, v, o, lse, dO, dq, dk, dv, ws});
-  if (st != TA_OK) return st;
-  return run_bwd(kStd, p, q, k, v, nullptr, nullptr, o, lse, dO, dq, dk, nullptr, nullptr, dv, ws, ws_bytes,
-                 causal, 0, static_cast<cudaStream_t>(stream));
+  return ta::bwd_entry(false, q, k, v, o, lse, dO, dq, dk, dv, ws, ws_bytes, B, H, M, N, D, dt, causal, sm_scale,
+                       stream);
+}
+
+ta_status attn_bwd_fused(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H,
+                         int M, int N, int D, ta_dtype dt, int causal, float sm_scale, void* stream) {
+  if (dt != TA_F16 && dt != TA_BF16) return TA_ERR_UNSUPPORTED;
+  if (!bwd_fused_applies(D, dt)) return TA_ERR_UNSUPPORTED;
+  return ta::bwd_entry(true, q, k, v, o, lse, dO, dq, dk, dv, ws, ws_bytes, B, H, M, N, D, dt, causal, sm_scale,
+                       stream);
 }
 
 size_t attn_bwd_jvp_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt) {
-  return 2 * attn_bwd_workspace_bytes(B, H, M, N, D, dt);
+  return 2 * piecewise_bwd_workspace_bytes(B, H, M, N, D, dt);  // eps and delta2
 }
 
 ta_status attn_bwd_jvp(const void* q, const void* k, const void* v, const void* tq, const void* tk, const void* tv,

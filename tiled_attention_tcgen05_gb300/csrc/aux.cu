@@ -11,9 +11,12 @@ namespace ta {
 
 // One group of D/8 threads per row; each thread reads 16 bytes of O and of
 // dO (8 elements), so a warp reads whole 128-byte lines of both tensors.
+// When acc is not null each thread also zeroes its 8 floats of the row's
+// [D] fp32 accumulator.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) delta_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dO,
-                                                    float* __restrict__ delta, long long rows) {
+                                                    float* __restrict__ delta, long long rows,
+                                                    float4* __restrict__ zacc) {
   constexpr int G = D / 8;  // threads per row
   constexpr int RPB = 256 / G;
   const int g = threadIdx.x % G;
@@ -34,6 +37,10 @@ __global__ void __launch_bounds__(256) delta_kernel(const uint4* __restrict__ o,
 #pragma unroll
     for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (act && g == 0) delta[row] = acc;
+    if (act && zacc) {
+      zacc[row * (D / 4) + 2 * g] = make_float4(0.f, 0.f, 0.f, 0.f);
+      zacc[row * (D / 4) + 2 * g + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -93,7 +100,7 @@ static int sm_count() {
 }
 
 cudaError_t launch_delta(bool bf16, int D, const void* o, const void* dO, float* delta, long long rows,
-                         cudaStream_t s) {
+                         cudaStream_t s, float* acc) {
   if (rows <= 0) return cudaSuccess;
   const int rpb = 256 / (D / 8);
   long long blocks = (rows + rpb - 1) / rpb;
@@ -101,21 +108,51 @@ cudaError_t launch_delta(bool bf16, int D, const void* o, const void* dO, float*
   if (blocks > cap) blocks = cap;
   const uint4* a = static_cast<const uint4*>(o);
   const uint4* b = static_cast<const uint4*>(dO);
+  float4* z = reinterpret_cast<float4*>(acc);
   if (D == 16) {
-    if (bf16) delta_kernel<__nv_bfloat16, 16><<<blocks, 256, 0, s>>>(a, b, delta, rows);
-    else delta_kernel<__half, 16><<<blocks, 256, 0, s>>>(a, b, delta, rows);
+    if (bf16) delta_kernel<__nv_bfloat16, 16><<<blocks, 256, 0, s>>>(a, b, delta, rows, z);
+    else delta_kernel<__half, 16><<<blocks, 256, 0, s>>>(a, b, delta, rows, z);
   } else if (D == 32) {
-    if (bf16) delta_kernel<__nv_bfloat16, 32><<<blocks, 256, 0, s>>>(a, b, delta, rows);
-    else delta_kernel<__half, 32><<<blocks, 256, 0, s>>>(a, b, delta, rows);
+    if (bf16) delta_kernel<__nv_bfloat16, 32><<<blocks, 256, 0, s>>>(a, b, delta, rows, z);
+    else delta_kernel<__half, 32><<<blocks, 256, 0, s>>>(a, b, delta, rows, z);
   } else if (D == 64) {
-    if (bf16) delta_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, s>>>(a, b, delta, rows);
-    else delta_kernel<__half, 64><<<blocks, 256, 0, s>>>(a, b, delta, rows);
+    if (bf16) delta_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, s>>>(a, b, delta, rows, z);
+    else delta_kernel<__half, 64><<<blocks, 256, 0, s>>>(a, b, delta, rows, z);
   } else if (D == 128) {
-    if (bf16) delta_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, s>>>(a, b, delta, rows);
-    else delta_kernel<__half, 128><<<blocks, 256, 0, s>>>(a, b, delta, rows);
+    if (bf16) delta_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, s>>>(a, b, delta, rows, z);
+    else delta_kernel<__half, 128><<<blocks, 256, 0, s>>>(a, b, delta, rows, z);
   } else {
     return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+// dq = acc * scale in the element type: each thread converts 8 consecutive
+// floats (two 16-byte loads, one 16-byte store).
+template <typename T>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
+                                                         long long n8, float scale) {
+  constexpr bool BF = DT<T>::bf16;
+  for (long long i = blockIdx.x * 256ll + threadIdx.x; i < n8; i += 256ll * gridDim.x) {
+    const float4 a = acc[2 * i], b = acc[2 * i + 1];
+    uint4 r;
+    r.x = pack2<BF>(a.x * scale, a.y * scale);
+    r.y = pack2<BF>(a.z * scale, a.w * scale);
+    r.z = pack2<BF>(b.x * scale, b.y * scale);
+    r.w = pack2<BF>(b.z * scale, b.w * scale);
+    dq[i] = r;
+  }
+}
+
+cudaError_t launch_dq_convert(bool bf16, int D, const float* acc, void* dq, long long rows, float scale,
+                              cudaStream_t s) {
+  const long long n8 = rows * (D / 8);
+  if (n8 <= 0) return cudaSuccess;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > sm_count() * 8ll) blocks = sm_count() * 8ll;
+  const float4* a = reinterpret_cast<const float4*>(acc);
+  if (bf16) dq_convert_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(a, static_cast<uint4*>(dq), n8, scale);
+  else dq_convert_kernel<__half><<<blocks, 256, 0, s>>>(a, static_cast<uint4*>(dq), n8, scale);
   return cudaGetLastError();
 }
 

@@ -64,26 +64,7 @@ __device__ __forceinline__ int pw_class_b(int q0, int k0, int P_SEQ, int w) {
   return kNearB | kFarB;
 }
 
-template <int D>
-__device__ __forceinline__ void load_tile_b(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int row0, int bh) {
-#pragma unroll
-  for (int kb = 0; kb < D / 64; ++kb) tma_load_3d(dst + kb * (kBM * 128), map, bar, kb * 64, row0, bh);
-}
 
-// d = A B^T over D: A, B are 128-row x D K-major swizzled tiles in smem.
-template <int D>
-__device__ __forceinline__ void mma_abT(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem, uint32_t idesc) {
-  const uint64_t da0 = sdesc_sw128(a_smem, 16, 1024);
-  const uint64_t db0 = sdesc_sw128(b_smem, 16, 1024);
-  uint64_t da[D / 16], db[D / 16];
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint64_t off = static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
-    da[kk] = da0 + off;
-    db[kk] = db0 + off;
-  }
-  mma_ss_n<D / 16>(d_tmem, da, db, idesc, 0u);
-}
 
 // d (+)= X Y: X is 128 x 128 16-bit in TMEM whose K-steps 0-3 sit at columns
 // x + [0, 32) and K-steps 4-7 at x + [64, 96) (the two column halves); Y is a
@@ -841,9 +822,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpMma) tmem_dealloc(tmem, 512);
 }
 
-// K-steps of chunk group g (the 32-key / 32-query chunk g of both column
-// halves): {2g, 2g + 1, 2g + 4, 2g + 5}.
-__device__ __forceinline__ constexpr int chunk_kstep(int g, int i) { return 2 * g + (i & 1) + 4 * (i >> 1); }
 
 // d (+)= X Y over the K-steps of chunk group g only (X, Y as in mma_tY); the
 // first MMA accumulates iff `accumulate`.  Whole converged warp.
@@ -862,21 +840,6 @@ __device__ __forceinline__ void mma_tY_g(uint32_t d_tmem, uint32_t x_tmem, uint3
   mma_ts_n<4>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
-// The same for X with interleaved K-steps (as mma_tY_il).
-template <int G>
-__device__ __forceinline__ void mma_tY_il_g(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
-                                            bool accumulate) {
-  const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
-  uint32_t a[4];
-  uint64_t b[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int kk = chunk_kstep(G, i);
-    a[i] = x_tmem + (kk >> 1) * 32 + (kk & 1) * 8;
-    b[i] = dy + static_cast<uint64_t>((kk * 16 * 128) >> 4);
-  }
-  mma_ts_n<4>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
-}
 
 // ======================================================================
 //      dQ, standard mode: Q and dO in TMEM, three-or-more-deep K/V ring
@@ -917,26 +880,6 @@ __device__ __forceinline__ void mma_tB(uint32_t d_tmem, uint32_t a_tmem, uint32_
   mma_ts_n<D / 16>(d_tmem, a, b, idesc, 0u);
 }
 
-// Copies row r of a 128 x D 16-bit K-major 128-byte-swizzled tile from shared
-// memory into TMEM lane r, columns taddr .. taddr + D/2 (two elements per
-// column, lower index in the low half): the layout an A operand is read in.
-// Warp-collective.
-template <int D>
-__device__ __forceinline__ void tile_row_to_tmem(const uint8_t* tile, int r, uint32_t taddr) {
-#pragma unroll
-  for (int kb = 0; kb < D / 64; ++kb) {
-    uint32_t v[32];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint4 c = *reinterpret_cast<const uint4*>(tile + kb * (kBM * 128) + r * 128 + ((j ^ (r & 7)) * 16));
-      v[4 * j + 0] = c.x;
-      v[4 * j + 1] = c.y;
-      v[4 * j + 2] = c.z;
-      v[4 * j + 3] = c.w;
-    }
-    tmem_st_x32(taddr + 32 * kb, v);
-  }
-}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)

@@ -58,6 +58,7 @@ struct BwdArgs {
   float scale_log2;
   float sm_scale;
   int dg;  // head dimension of the tensors in memory (row stride, columns stored)
+  float* dq_acc;  // fused backward: fp32 dQ accumulator [BH, M, D] (zeroed by the delta pass)
   uint32_t* err;
   uint64_t timeout_ns;
 };

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "tattn.h"
 
 namespace ta {
 
@@ -24,9 +25,22 @@ cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const Fw
 // maps.v the transposed V [BH, D, N] with 128 x D boxes.
 cudaError_t launch_fwd_f8(int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s);
 
-// delta_i = sum_d O_id dO_id for BH*M rows.
+// delta_i = sum_d O_id dO_id for BH*M rows; when acc is not null the same
+// pass also zeroes acc, a [rows, D] fp32 array (the fused backward's dQ
+// accumulator).
 cudaError_t launch_delta(bool bf16, int D, const void* o, const void* dO, float* delta, long long rows,
-                         cudaStream_t s);
+                         cudaStream_t s, float* acc = nullptr);
+// dq = acc * scale rounded to the element type, for rows x D elements.
+cudaError_t launch_dq_convert(bool bf16, int D, const float* acc, void* dq, long long rows, float scale,
+                              cudaStream_t s);
+// Fused backward (dK, dV and the fp32 dQ accumulator a.dq_acc in one
+// key-stationary pass) for the standard mode at the kernel head dimensions
+// bwd_fused_supported() accepts.
+bool bwd_fused_supported(int D);
+// Query rows per streamed step of the fused backward: its Q and dO maps take
+// boxes of this many rows (K and V keep 128-row boxes).
+int bwd_fused_step_rows();
+cudaError_t launch_bwd_fused(bool bf16, int D, const BwdMaps& maps, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& maps, const BwdArgs& a,
                             cudaStream_t s);
 cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& maps, const BwdArgs& a, cudaStream_t s);
@@ -97,6 +111,14 @@ inline cudaError_t smem_attr_once(K kern, int bytes, std::atomic<bool> (&done)[k
   if (e == cudaSuccess && tracked) done[dev].store(true, std::memory_order_release);
   return e;
 }
+
+// attn_bwd with the choice of path: allow_fused = false keeps the two-pass
+// backward (key-stationary dK/dV, then query-stationary dQ), whose only
+// scratch is delta (ws >= delta's bytes); true takes the fused pass where it
+// applies (ws >= attn_bwd_workspace_bytes).
+ta_status bwd_entry(bool allow_fused, const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H, int M,
+                    int N, int D, ta_dtype dt, int causal, float sm_scale, void* stream);
 
 // Profiling hooks (no-ops unless ta_profile_enable(1)).
 void prof_begin(const char* name, cudaStream_t s);

@@ -8,11 +8,15 @@
 // loop that must not call cudaMalloc because the call synchronises the
 // device and its latency is unbounded.  This entry point keeps that scratch
 // in a fixed-size array that lives in this library's device image instead, so
-// the call itself allocates nothing.
+// the call itself allocates nothing.  It runs the two-pass backward (dK/dV
+// pass, then dQ pass), whose only scratch is delta; attn_bwd's fused pass
+// would also need an fp32 dQ accumulator of B*H*M*D floats.
+#include <climits>
 #include <mutex>
 
 #include "tattn.h"
 #include "common.cuh"
+#include "launch.h"
 
 namespace ta {
 
@@ -21,19 +25,43 @@ namespace ta {
 constexpr long long kNoAllocRows = 1ll << 21;
 static __device__ __align__(256) float g_noalloc_delta[kNoAllocRows];
 
+typedef CUresult (*NaCtxGetCurrentFn)(CUcontext*);
+
+// The calling thread's current context (null when it has none or the driver
+// entry point is unavailable).
+static CUcontext current_context() {
+  static NaCtxGetCurrentFn get = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get = reinterpret_cast<NaCtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (get && get(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
 // Device address of g_noalloc_delta for the current device.  In host code the
-// array's name only stands in for the symbol, so the address is looked up once
-// per device (with that device current) and cached.
+// array's name only stands in for the symbol, so the address is looked up
+// with the device current and cached per device, together with the context
+// it was looked up in: after cudaDeviceReset (or under another context) the
+// module is loaded afresh and the next call looks the address up again.
 static ta_status noalloc_scratch(void** out) {
   static std::mutex mu;
-  static void* cache[64] = {};
+  static void* cache[kMaxDevices] = {};
+  static CUcontext cache_ctx[kMaxDevices] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TA_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TA_ERR_CUDA;
   std::lock_guard<std::mutex> lk(mu);
-  if (!cache[dev]) {
+  const CUcontext ctx = current_context();
+  if (!cache[dev] || ctx == nullptr || ctx != cache_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_delta) != cudaSuccess || p == nullptr) return TA_ERR_CUDA;
     cache[dev] = p;
+    cache_ctx[dev] = current_context();  // the lookup binds a context if the thread had none
   }
   *out = cache[dev];
   return TA_OK;
@@ -46,10 +74,13 @@ extern "C" ta_status attn_bwd_noalloc(const void* q, const void* k, const void* 
                                       int H, int M, int N, int D, ta_dtype dt, int causal, float sm_scale,
                                       void* stream) {
   if (B < 0 || H < 0 || M < 0) return TA_ERR_INVALID_ARG;
-  if (static_cast<long long>(B) * H * M > ta::kNoAllocRows) return TA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;  // < 2^62: no overflow
+  if (BH > INT_MAX) return TA_ERR_INVALID_ARG;
+  if (BH * M > ta::kNoAllocRows) return TA_ERR_UNSUPPORTED;  // BH * M < 2^62
   void* scratch = nullptr;
   const ta_status st = ta::noalloc_scratch(&scratch);
   if (st != TA_OK) return st;
-  return attn_bwd(q, k, v, o, lse, dO, dq, dk, dv, scratch, static_cast<size_t>(ta::kNoAllocRows) * sizeof(float),
-                  B, H, M, N, D, dt, causal, sm_scale, stream);
+  return ta::bwd_entry(false, q, k, v, o, lse, dO, dq, dk, dv, scratch,
+                       static_cast<size_t>(ta::kNoAllocRows) * sizeof(float), B, H, M, N, D, dt, causal, sm_scale,
+                       stream);
 }
