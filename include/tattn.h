@@ -125,7 +125,12 @@ ta_status attn_bwd_fused(const void* q, const void* k, const void* v, const void
  *    exits).  Larger problems return TA_ERR_UNSUPPORTED without launching.
  *  - The call allocates nothing.  Its first call on a device looks up the
  *    array's device address (cudaGetSymbolAddress) with that device current;
- *    make that first call before any stream capture.
+ *    make that first call before any stream capture.  The address is cached
+ *    together with the context it was looked up in; after cudaDeviceReset
+ *    (or from another context) the next call looks it up again, so that call,
+ *    too, belongs before any capture.
+ *  - B*H > 2^31 - 1 returns TA_ERR_INVALID_ARG, as in attn_bwd.
+ *  - It runs the two-pass backward of attn_bwd (its only scratch is delta).
  *  - Every call shares the one array and fully rewrites the rows it uses, so
  *    nothing needs clearing between calls; calls that may run at the same
  *    time on the GPU (other streams, other host threads) race on it. */
