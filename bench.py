@@ -497,6 +497,41 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device error word: {status}")
     ms = ev0.elapsed_time(ev1) / args.steps
 
+    # ---- the host link's copy rates on this machine (outside every timed region):
+    # each direction alone and both at once, one copy of the step's size each
+    def link_rates(reps=5):
+        n = 268 << 20
+        hi = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        ho = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        di = torch.empty(n, dtype=torch.uint8, device=dev)
+        do_ = torch.empty(n, dtype=torch.uint8, device=dev)
+        s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        rates = {}
+        for name, ups, downs in (("h2d_gbs", 1, 0), ("d2h_gbs", 0, 1), ("both_gbs", 1, 1)):
+            best = 0.0
+            for _ in range(reps):
+                torch.cuda.synchronize(dev)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                s1.wait_stream(stream)
+                s2.wait_stream(stream)
+                if ups:
+                    with torch.cuda.stream(s1):
+                        di.copy_(hi, non_blocking=True)
+                if downs:
+                    with torch.cuda.stream(s2):
+                        ho.copy_(do_, non_blocking=True)
+                stream.wait_stream(s1)
+                stream.wait_stream(s2)
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                best = max(best, n * (ups + downs) / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+            rates[name] = best
+        del hi, ho, di, do_
+        return rates
+
+    link = link_rates()
+
     # ---- end-to-end: pinned host inputs -> device -> results back to host.
     # Every step copies its own inputs in and all its results out inside the
     # timed region.  The copies run on their own streams into double-buffered
@@ -652,6 +687,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms,
                 "host_enqueue_ms_per_step": e2e_host_ms,
+                "link": {**link, "copy_floor_ms": (h2d + d2h) / (link["both_gbs"] * 1e9) * 1e3,
+                         "how": "pinned copies of 268 MB, best of 5, each direction alone and both at once"},
                 "method": "pinned host inputs copied in and all results copied out every step (one contiguous "
                           "buffer each way), on copy streams overlapping the neighbouring steps' kernels "
                           "(double-buffered device memory); "
