@@ -85,10 +85,6 @@ struct FusedCfg {
   static_assert(COL_DK + D <= 512, "TMEM overflow");
 };
 
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
@@ -492,8 +488,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
         for (int jq = 0; jq < 4; ++jq) {
           const uint32_t a = dsb + g * (16 * 128) + (((4 * hc + jq) ^ swz) << 4);
-          sts32(a, pd[2 * jq]);
-          sts32(a + 8 * 128, pd[2 * jq + 1]);
+          sts_b32(a, pd[2 * jq]);
+          sts_b32(a + 8 * 128, pd[2 * jq + 1]);
         }
       }
       tmem_st_wait();
