@@ -99,12 +99,27 @@ def _code_only(text):
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
-def kernel_source_hash():
-    """Hash of the kernel sources' code (comments excluded), the key under
-    which profiles/traffic.json records the DRAM counters it was taken on."""
-    h = hashlib.sha256()
+# The device sources each measured kernel is compiled from: its own .cu file
+# and the device headers it includes (launch.h and tattn.h only declare host
+# functions; the tensor maps built in api.cu must match the boxes each kernel
+# expects, so a change there shows in the kernel's own source too).
+_DEVICE_HEADERS = ("common.cuh", "ptx.cuh", "tmem_ldst.cuh")
+KERNEL_SOURCES = {
+    "attn_fwd": ("fwd.cu",),
+    "attn_bwd_dkdv": ("bwd.cu", "bwd_common.cuh"),
+    "attn_bwd_dq": ("bwd.cu", "bwd_common.cuh"),
+}
+
+
+def kernel_source_hash(kernel=None):
+    """Hash of the code (comments excluded) of the sources `kernel` is compiled
+    from (KERNEL_SOURCES), or of every kernel source when `kernel` is None: the
+    key under which profiles/traffic.json records the DRAM counters it was
+    taken on."""
     csrc = os.path.join(ROOT, "tiled_attention_tcgen05_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = sorted(os.listdir(csrc)) if kernel is None else sorted(KERNEL_SOURCES[kernel] + _DEVICE_HEADERS)
+    h = hashlib.sha256()
+    for f in files:
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
@@ -112,19 +127,19 @@ def kernel_source_hash():
 
 def ncu_traffic(kernel):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None
-    when the summary was taken on different kernel sources."""
+    when the summary was taken on different sources of that kernel."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or kernel not in KERNEL_SOURCES:
         return None
     try:
         with open(p) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_hash") != kernel_source_hash():
-        return None
     ent = d.get("kernels", {}).get(kernel)
-    return ent.get("dram_bytes_per_launch") if ent else None
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    return ent.get("dram_bytes_per_launch")
 
 
 class ClockSampler:

@@ -42,6 +42,11 @@ def test_source_hash_ignores_comments_only():
     assert bench._code_only("int x = 1;") != bench._code_only("int x = 2;")
     h = bench.kernel_source_hash()
     assert len(h) == 16 and h == bench.kernel_source_hash()
+    # each measured kernel is keyed by its own sources: the forward's key does
+    # not move with the backward's file, and both kernels of bwd.cu share one
+    assert bench.kernel_source_hash("attn_fwd") != bench.kernel_source_hash("attn_bwd_dkdv")
+    assert bench.kernel_source_hash("attn_bwd_dq") == bench.kernel_source_hash("attn_bwd_dkdv")
+    assert bench.ncu_traffic("no_such_kernel") is None
 
 
 def test_peak_lookup_accepts_plain_and_nested_values():
