@@ -105,7 +105,7 @@ def _code_only(text):
 # expects, so a change there shows in the kernel's own source too).
 _DEVICE_HEADERS = ("common.cuh", "ptx.cuh", "tmem_ldst.cuh")
 KERNEL_SOURCES = {
-    "attn_fwd": ("fwd.cu",),
+    "attn_fwd": ("fwd.cu", "cluster.cuh"),
     "attn_bwd_dkdv": ("bwd.cu", "bwd_common.cuh"),
     "attn_bwd_dq": ("bwd.cu", "bwd_common.cuh"),
 }
@@ -363,11 +363,36 @@ def bwd_fused_measure(ta, torch, dev, stream, g, o, lse, w, bf16_peak, iters=10)
     return out
 
 
+def timed_calls(ta, torch, dev, stream, flush, fn, iters):
+    """(device ms, call ms) per call of `fn`, L2 flushed before each call.  The
+    device time is the sum of the call's kernels, each bracketed by the
+    library's own events on the launch stream (ta_profile_*); the call time is
+    taken between events recorded before and after the Python call, so it
+    also holds any wait of the GPU for the host (marshalling the arguments,
+    encoding the tensor maps), which shows when the kernels take only tens of
+    microseconds."""
+    call = 0.0
+    ta.profile_enable(True)
+    with torch.cuda.stream(stream):
+        for _ in range(iters):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            call += e0.elapsed_time(e1) / iters
+    prof = ta.profile_read()
+    ta.profile_enable(False)
+    return sum(v[1] for v in prof.values()) / iters, call
+
+
 def jvp_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
     """Times the JVP forward (attn_fwd_jvp with tL) and its backward
     (attn_bwd_jvp) on the JVP workload's shape, [2, 8, 1024, 64] fp16, causal
-    and not, outside the step's timed region; L2 is flushed before each timed
-    call (the inputs, 2 MB a tensor, fit in it).  Algorithmic FLOPs: the JVP
+    and not, outside the step's timed region, by the library's per-launch
+    events; L2 is flushed before each timed call (the inputs, 2 MB a tensor,
+    fit in it).  Algorithmic FLOPs: the JVP
     forward is 3x the primal forward (6 matmul-equivalents of 2 M N D), the
     backward of the JVP 15 matmul-equivalents (S, T, dtO V^T, dO V^T + dtO tV^T
     and the nine gradient products), i.e. 7.5x the primal forward."""
@@ -387,33 +412,46 @@ def jvp_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
             fwd()
             bwd()
         torch.cuda.synchronize(dev)
-        res = {}
-        for label, fn in (("fwd", fwd), ("bwd", bwd)):
-            ms = 0.0
-            with torch.cuda.stream(stream):
-                for _ in range(iters):
-                    flush.zero_()
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    fn()
-                    e1.record(stream)
-                    torch.cuda.synchronize(dev)
-                    ms += e0.elapsed_time(e1) / iters
-            res[label] = ms
+        timed = lambda fn: timed_calls(ta, torch, dev, stream, flush, fn, iters)
+        res = {"fwd": timed(fwd), "bwd": timed(bwd)}
+        # the forward with the key split forced each way (the library's own
+        # choice is what "fwd_ms" measured)
+        for mode in ("never", "always"):
+            ta.set_fwd_kv_split(mode)
+            fwd()
+            res[mode] = timed(fwd)
+        ta.set_fwd_kv_split("auto")
         f = flops_fwd(B, H, M, M, D, causal)
-        tf_f = 3 * f / (res["fwd"] * 1e-3) / 1e12
-        tf_b = 7.5 * f / (res["bwd"] * 1e-3) / 1e12
+        tf_f = 3 * f / (res["fwd"][0] * 1e-3) / 1e12
+        tf_b = 7.5 * f / (res["bwd"][0] * 1e-3) / 1e12
         out["causal" if causal else "noncausal"] = {
-            "fwd_ms": res["fwd"], "bwd_ms": res["bwd"], "fwd_tflops": tf_f, "bwd_tflops": tf_b,
-            "fwd_frac": tf_f / bf16_peak, "bwd_frac": tf_b / bf16_peak}
+            "fwd_ms": res["fwd"][0], "bwd_ms": res["bwd"][0], "fwd_tflops": tf_f, "bwd_tflops": tf_b,
+            "fwd_frac": tf_f / bf16_peak, "bwd_frac": tf_b / bf16_peak,
+            "fwd_call_ms": res["fwd"][1], "bwd_call_ms": res["bwd"][1],
+            "fwd_kv_split": ta.fwd_kv_split("attn_fwd_jvp", B, H, M, M, D, torch.float16, causal),
+            "fwd_ms_unsplit": res["never"][0], "fwd_ms_split": res["always"][0]}
+    # where the key split pays: few query tiles over a long key range
+    Bl, Hl, Ml, Nl = 1, 4, 1024, 8192
+    gl = {n: t.to(dev) for n, t in si.attention_inputs(Bl, Hl, Ml, Nl, D, "f16", 4, names=names[:6]).items()}
+    fwd = lambda: ta.attn_fwd_jvp(*(gl[n] for n in names[:6]), causal=False, with_tlse=True, stream=stream)
+    res = {}
+    for mode in ("never", "always", "auto"):
+        ta.set_fwd_kv_split(mode)
+        fwd()
+        res[mode] = timed_calls(ta, torch, dev, stream, flush, fwd, iters)[0]
+    ta.set_fwd_kv_split("auto")
+    out["long_keys"] = {"shape": "B1 H4 M=1024 N=8192 D64 fp16, non-causal (32 query tiles of 64 key tiles)",
+                        "fwd_kv_split": ta.fwd_kv_split("attn_fwd_jvp", Bl, Hl, Ml, Nl, D, torch.float16, False),
+                        "fwd_ms": res["auto"], "fwd_ms_unsplit": res["never"], "fwd_ms_split": res["always"]}
     return out
 
 
 def configs_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
     """Times one fwd+bwd step (forward then backward, inputs resident) on the
     other workloads: 1 (B1 H2 S128 D64 fp16, non-causal), 2 (B4 H16 S2048 D128
-    bf16 causal) and 5 (piecewise, B2 H16 S4096 D64 bf16 causal, w = 512).
-    L2 is flushed before each timed step.  FLOPs are the standard count
+    bf16 causal) and 5 (piecewise, B2 H16 S4096 D64 bf16 causal, w = 512),
+    as the device time of the step's kernels (timed_calls).  L2 is flushed
+    before each timed step.  FLOPs are the standard count
     (4 M N D per head forward, x 3.5 for forward + backward, x 0.5 causal); the
     piecewise path's second score products on straddling tiles are overhead."""
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -436,19 +474,11 @@ def configs_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
         for _ in range(3):
             fn()
         torch.cuda.synchronize(dev)
-        ms = 0.0
-        with torch.cuda.stream(stream):
-            for _ in range(iters):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-                torch.cuda.synchronize(dev)
-                ms += e0.elapsed_time(e1) / iters
+        ms, call_ms = timed_calls(ta, torch, dev, stream, flush, fn, iters)
         f = flops_fwd(B, H, M, N, D, causal) * 3.5
         tf = f / (ms * 1e-3) / 1e12
-        out[str(wid)] = {"workload": w["name"], "ms_per_step": ms, "tflops": tf, "frac": tf / bf16_peak}
+        out[str(wid)] = {"workload": w["name"], "ms_per_step": ms, "tflops": tf, "frac": tf / bf16_peak,
+                         "call_ms_per_step": call_ms}
     return out
 
 

@@ -255,6 +255,25 @@ ta_status ta_selftest_wait_timeout(int timeout_ms, void* stream);
 ta_status ta_profile_enable(int on);
 int ta_profile_read(const char** names, int* launches, double* total_ms, int cap);
 
+/* Key split of the one-query-tile forward (no counterpart on the pages; the
+ * merge is [MERGE] reference_forward's combine, done on the raw online-softmax
+ * state).  attn_fwd_jvp (all D) and piecewise_fwd at D = 128 (16-bit) run one
+ * 128-row query tile per CTA.  When that grid is under one wave of the GPU's
+ * SMs and a two-CTA split of every query tile's key tiles shortens the
+ * estimated schedule (list scheduling in launch order, costs in key tiles),
+ * each query tile gets a cluster of two CTAs: the second hands its running
+ * max, sum and unnormalised accumulators to the first over distributed shared
+ * memory, and the first combines them with the same rescale the online
+ * softmax applies between key tiles.  Results equal the unsplit kernel's up
+ * to fp32 rounding; nothing is allocated.
+ * ta_fwd_kv_split returns 2 when `entry` (0 attn_fwd, 1 piecewise_fwd,
+ * 2 attn_fwd_jvp) splits this problem on a GPU of `num_sms` SMs (<= 0: the
+ * current device's count), 1 when it does not, 0 for invalid arguments.
+ * ta_set_fwd_kv_split(mode) sets the choice for the process: 0 (default) by
+ * the estimate, 1 never, 2 wherever the kernel supports it. */
+int ta_fwd_kv_split(int entry, int B, int H, int M, int N, int D, ta_dtype dt, int causal, int num_sms);
+void ta_set_fwd_kv_split(int mode);
+
 /* Per-launch wait limit in milliseconds used by every kernel (default 2000,
  * or the TA_WAIT_TIMEOUT_MS environment variable at load time). */
 void ta_set_wait_timeout_ms(int ms);

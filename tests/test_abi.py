@@ -134,3 +134,46 @@ def test_jvp_backward_workspace_and_validation(lib):
     misaligned[11] = vp(0x2008)                             # dtO
     assert call(misaligned, vp(0x4000), nws) == ALIGNMENT
     assert lib.attn_bwd_jvp(*p, vp(0x4000), nws, 0, 1, 128, 128, 64, F16, 1, -1.0, vp(0)) == OK  # B = 0
+
+
+def test_forward_key_split_choice(lib):
+    """Which problems the one-query-tile forward splits (host logic only: the
+    SM count is passed in, so no CUDA call is made)."""
+    f = lib.ta_fwd_kv_split
+    STD, PW, JVP = 0, 1, 2
+    # the JVP workload [2, 8, 1024, 64] fp16 on 152 SMs: 128 CTAs, under one
+    # wave.  Split, they would be 256 CTAs in two waves: the second wave's
+    # set-up and epilogue cost what the shorter key ranges save -> no split,
+    # causal or not.
+    assert f(JVP, 2, 8, 1024, 1024, 64, F16, 1, 152) == 1
+    assert f(JVP, 2, 8, 1024, 1024, 64, F16, 0, 152) == 1
+    # one head: 8 CTAs; split, 16 CTAs in one wave with half the key tiles each
+    assert f(JVP, 1, 1, 1024, 1024, 64, F16, 1, 152) == 2
+    # more query tiles than SMs: the grid already balances itself
+    assert f(JVP, 1, 32, 8192, 8192, 128, BF16, 1, 152) == 1
+    # one key tile per query tile: nothing to share
+    assert f(JVP, 1, 4, 128, 128, 64, F16, 0, 152) == 1
+    # a few long rows: split
+    assert f(JVP, 1, 1, 1024, 4096, 128, BF16, 0, 152) == 2
+    # piecewise: the D = 128 forward (one query tile per CTA) splits, the D = 64
+    # two-tile forward and the standard forward never do
+    assert f(PW, 1, 1, 4096, 4096, 128, BF16, 1, 152) == 2
+    assert f(PW, 1, 1, 4096, 4096, 64, BF16, 1, 152) == 1
+    assert f(STD, 1, 1, 4096, 4096, 128, BF16, 1, 152) == 1
+    # the fp32 mode runs SIMT kernels
+    assert f(JVP, 1, 1, 1024, 4096, 64, F32, 0, 152) == 1
+    # invalid arguments
+    assert f(JVP, 1, 1, 1024, 1024, 96, F16, 0, 152) == 0
+    assert f(3, 1, 1, 1024, 1024, 64, F16, 0, 152) == 0
+    assert f(JVP, 0, 1, 1024, 1024, 64, F16, 0, 152) == 0
+    # the process-wide setting overrides the estimate
+    try:
+        lib.ta_set_fwd_kv_split(1)
+        assert f(JVP, 1, 1, 1024, 1024, 64, F16, 1, 152) == 1
+        lib.ta_set_fwd_kv_split(2)
+        assert f(JVP, 2, 8, 1024, 1024, 64, F16, 0, 152) == 2
+        assert f(JVP, 1, 32, 8192, 8192, 128, BF16, 1, 152) == 2
+        assert f(STD, 1, 1, 4096, 4096, 128, BF16, 1, 152) == 1  # no split kernel there
+    finally:
+        lib.ta_set_fwd_kv_split(0)
+    assert f(JVP, 2, 8, 1024, 1024, 64, F16, 0, 152) == 1

@@ -27,7 +27,7 @@ import torch
 
 __all__ = ["load", "lib_path", "attn_fwd", "attn_bwd", "attn_bwd_fused", "attn_fwd_jvp", "attn_bwd_jvp", "piecewise_fwd", "piecewise_bwd", "merge_fwd", "merge_bwd", "attn_fwd_fp8",
            "attn_bwd_workspace_bytes", "attn_bwd_fused_workspace_bytes", "sync_status", "selftest_wait_timeout", "profile_enable",
-           "profile_read", "set_wait_timeout_ms", "TAError", "STATUS"]
+           "profile_read", "set_wait_timeout_ms", "fwd_kv_split", "set_fwd_kv_split", "TAError", "STATUS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "libtattn.so")
@@ -60,6 +60,8 @@ _SIGS = {
     "ta_profile_read": ([ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_i), ctypes.POINTER(ctypes.c_double),
                          _i], _i),
     "ta_set_wait_timeout_ms": ([_i], None),
+    "ta_fwd_kv_split": ([_i] * 9, _i),
+    "ta_set_fwd_kv_split": ([_i], None),
 }
 
 
@@ -315,6 +317,26 @@ def selftest_wait_timeout(timeout_ms: int = 20, stream=None) -> str:
 
 def set_wait_timeout_ms(ms: int):
     load().ta_set_wait_timeout_ms(int(ms))
+
+
+_ENTRY = {"attn_fwd": 0, "piecewise_fwd": 1, "attn_fwd_jvp": 2}
+_SPLIT_MODE = {"auto": 0, "never": 1, "always": 2}
+
+
+def fwd_kv_split(entry: str, B: int, H: int, M: int, N: int, D: int, dtype, causal: bool, num_sms: int = 0) -> int:
+    """CTAs per 128-row query tile that forward entry point `entry` launches
+    for this problem (2: key split into a two-CTA cluster, 1: not split) on a
+    GPU with `num_sms` SMs (0: the current device's)."""
+    r = load().ta_fwd_kv_split(_ENTRY[entry], B, H, M, N, D, _DT[dtype], int(bool(causal)), int(num_sms))
+    if r == 0:
+        raise ValueError("invalid problem for ta_fwd_kv_split")
+    return r
+
+
+def set_fwd_kv_split(mode: str):
+    """Process-wide key-split choice of the one-query-tile forward: "auto"
+    (the library's estimate, the default), "never" or "always"."""
+    load().ta_set_fwd_kv_split(_SPLIT_MODE[mode])
 
 
 def profile_enable(on: bool = True):

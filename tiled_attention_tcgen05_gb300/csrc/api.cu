@@ -1,6 +1,7 @@
 // C ABI of libtattn.so: argument validation, TMA tensor-map encoding, kernel
 // dispatch, the device error word behind the bounded waits, and per-kernel
 // CUDA-event timing.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -273,6 +274,70 @@ static size_t dq_acc_bytes(long long BH, int M, int D) {
   return static_cast<size_t>(BH) * static_cast<size_t>(M) * static_cast<size_t>(D) * sizeof(float);
 }
 
+// ---------------------------------------- key split of the one-tile forward
+// The JVP forward and the D = 128 piecewise forward run one 128-row query
+// tile per CTA (one CTA per SM: each takes all 512 TMEM columns).  When the
+// grid is less than one wave, the slowest CTA (the query tile with the most
+// key tiles) sets the kernel's time; the key split gives each query tile a
+// cluster of two CTAs that take half of its key tiles each.  The choice
+// compares the two grids' makespans under list scheduling: CTAs start in
+// launch order on the first free SM, a CTA costs its key tiles plus
+// kSplitFixed tiles of set-up and epilogue, and the first CTA of a pair
+// kSplitMerge more for reading its partner's state; the split must save 15 %.
+// The fixed cost is measured: the JVP forward on [2, 8, 1024, 64] takes
+// ~27 us whether its CTAs walk 8 key tiles (one wave) or at most 4 (the
+// split: 256 CTAs, two waves), i.e. a CTA's set-up and epilogue cost about
+// as much as two to three key tiles.  Long key ranges with few query tiles
+// (decoding-like shapes) are where the split pays.
+static std::atomic<int> g_fwd_split_mode{0};  // 0 by the cost model, 1 never, 2 wherever a kernel can
+constexpr double kSplitFixed = 2.5, kSplitMerge = 0.5, kSplitGain = 0.85;
+
+static double list_makespan(const std::vector<double>& costs, int sms) {
+  std::vector<double> free_at(static_cast<size_t>(sms), 0.0);  // min-heap of SM free times
+  auto cmp = [](double a, double b) { return a > b; };
+  double span = 0.0;
+  for (double c : costs) {
+    std::pop_heap(free_at.begin(), free_at.end(), cmp);
+    free_at.back() += c;
+    span = std::max(span, free_at.back());
+    std::push_heap(free_at.begin(), free_at.end(), cmp);
+  }
+  return span;
+}
+
+static int device_sms() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+static bool fwd_split_plan(int mode, const Problem& p, int causal, int sms) {
+  if (p.f32 || p.BH == 0 || p.M == 0 || p.N == 0 || !fwd_split_capable(mode, kernel_d(p.D))) return false;
+  const int nq = (p.M + kBM - 1) / kBM;
+  if (2ll * nq > 65535) return false;
+  const int setting = g_fwd_split_mode.load(std::memory_order_relaxed);
+  if (setting == 1) return false;
+  if (setting == 2) return true;
+  if (sms <= 0 || p.BH * nq > sms) return false;  // a wave or more: the grid balances itself
+  std::vector<double> one, two;
+  for (int y = 0; y < nq; ++y) {  // launch order: heaviest query tile first, heads fastest
+    const int n = kv_tiles_for((nq - 1 - y) * kBM, p.M, p.N, p.N - p.M, causal);
+    const int h = (n + 1) / 2;
+    for (long long x = 0; x < p.BH; ++x) {
+      one.push_back(n + kSplitFixed);
+      two.push_back(h + kSplitFixed + (n - h > 0 ? kSplitMerge : 0.0));
+      two.push_back(n - h + kSplitFixed);
+    }
+  }
+  return list_makespan(two, sms) < kSplitGain * list_makespan(one, sms);
+}
+
 static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* k, const void* v,
                          const void* q2, const void* k2, const void* v2, void* o, float* lse, void* to,
                          float* tlse, int causal, int w, cudaStream_t s) {
@@ -305,7 +370,7 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
   FwdArgs a = fwd_args(p, causal, w, o, lse, to, tlse);
   static const char* names[3] = {"attn_fwd", "piecewise_fwd", "attn_fwd_jvp"};
   prof_begin(names[mode], s);
-  cudaError_t e = launch_fwd(mode, p.bf16, kernel_d(p.D), maps, a, s);
+  cudaError_t e = launch_fwd(mode, p.bf16, kernel_d(p.D), maps, a, fwd_split_plan(mode, p, causal, device_sms()), s);
   prof_end(s);
   return cuda_status(e);
 }
@@ -533,6 +598,16 @@ const char* ta_status_str(ta_status s) {
     case TA_ERR_TIMEOUT: return "TA_ERR_TIMEOUT";
   }
   return "TA_ERR_UNKNOWN";
+}
+
+void ta_set_fwd_kv_split(int mode) { g_fwd_split_mode.store(mode == 1 || mode == 2 ? mode : 0); }
+
+int ta_fwd_kv_split(int entry, int B, int H, int M, int N, int D, ta_dtype dt, int causal, int num_sms) {
+  Problem p;
+  if (entry < 0 || entry > 2 || B < 1 || H < 1) return 0;
+  if (check_common(B, H, M, N, D, dt, -1.f, &p) != TA_OK) return 0;
+  const int mode = entry == 0 ? kStd : entry == 1 ? kPiecewise : kJvp;
+  return fwd_split_plan(mode, p, causal, num_sms > 0 ? num_sms : device_sms()) ? 2 : 1;
 }
 
 void ta_set_wait_timeout_ms(int ms) { g_timeout_ns = static_cast<uint64_t>(ms > 0 ? ms : 2000) * 1000000ull; }

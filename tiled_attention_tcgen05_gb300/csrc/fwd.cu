@@ -31,6 +31,7 @@
 // instead of two.
 #include <cstdio>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -132,31 +133,54 @@ __device__ __forceinline__ void store_row_chunk(T* dst, const float* v32, float 
 
 #define TA_CHUNK(arr, c) (*reinterpret_cast<uint32_t(*)[32]>(&(arr)[32 * (c)]))
 
-template <typename T, int MODE, int D>
-__global__ void __launch_bounds__(192, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q2,
-                    const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2,
-                    const FwdArgs args) {
+// Key split (SPLIT): the kernel runs as clusters of two CTAs per query tile.
+// The first CTA of a pair takes the tile's first ceil(n/2) key tiles, the
+// second the rest; at the end the second CTA leaves its raw state (running
+// maximum m, sum l, JVP mu, and the unnormalised O and U rows) in its own
+// shared memory and the first CTA reads it over distributed shared memory and
+// combines the two online-softmax states before its epilogue:
+//   m = max(m0, m1), a_i = 2^(m_i - m), l = a0 l0 + a1 l1, O = a0 O0 + a1 O1
+// (mu and U like l and O), which is the rescale the softmax applies between
+// key tiles, applied once between the two halves.  Layout of the hand-over
+// area (the second CTA's dynamic shared memory, free once its last MMA is
+// done): m, l, mu as float[128] each, then O and U as float4 [D/32 chunks]
+// [8 quads][128 rows], so a warp's stores and loads are contiguous.
+constexpr int kSplitHdr = 2048;
+
+template <typename T, int MODE, int D, bool SPLIT>
+__device__ __forceinline__ void fwd1_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                          const CUtensorMap& tm_q2, const CUtensorMap& tm_k2,
+                                          const CUtensorMap& tm_v2, const FwdArgs& args) {
   using C = FwdCfg<MODE, D>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
   constexpr int NBUF = C::NBUF;
+  constexpr int NACC = (MODE == kJvp) ? 2 : 1;  // accumulators handed over: O (and U)
+  static_assert(!SPLIT || kSplitHdr + NACC * D * 512 <= C::SMEM - 1024, "hand-over area does not fit");
+  // each CTA takes all 512 TMEM columns: the two CTAs of a pair must sit on
+  // different SMs, which more than half an SM's shared memory guarantees
+  static_assert(!SPLIT || C::SMEM > kSmemMax / 2, "the CTAs of a pair could share an SM");
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q;
   __shared__ __align__(8) uint64_t bar_k[STAGES], bar_v[STAGES], bar_empty[STAGES];
   __shared__ __align__(8) uint64_t bar_s[NBUF], bar_p[NBUF];
   __shared__ __align__(8) uint64_t bar_o, bar_ofinal;
+  __shared__ __align__(8) uint64_t bar_peer;  // SPLIT: the second CTA's state is ready (first CTA's copy)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
-  const int qt = args.num_q_tiles - 1 - blockIdx.y;  // heaviest causal tiles first
+  const int part = SPLIT ? static_cast<int>(blockIdx.y & 1) : 0;  // = rank in the (1, 2, 1) cluster
+  const int qt = args.num_q_tiles - 1 - static_cast<int>(SPLIT ? blockIdx.y >> 1 : blockIdx.y);  // heaviest first
   const int q0 = qt * kBM;
-  const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
+  const int nkv_all = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
+  const int h_split = (nkv_all + 1) >> 1;
+  const int t0 = (SPLIT && part) ? h_split : 0;  // first key tile of this CTA
+  const int nkv = SPLIT ? (part ? nkv_all - h_split : h_split) : nkv_all;
+  const int n_peer = (SPLIT && !part) ? nkv_all - h_split : 0;  // key tiles the partner CTA took
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;                                  // Q | Q1 | Q  (+ Q2 | TQ)
@@ -180,6 +204,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     mbar_init(&bar_o, 1);
     mbar_init(&bar_ofinal, 1);
+    mbar_init(&bar_peer, kBM);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -188,6 +213,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (SPLIT) cluster_sync_all();  // the partner's barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
@@ -208,7 +234,7 @@ __global__ void __launch_bounds__(192, 1)
         if (t >= STAGES) {
           if (!mbar_wait(&bar_empty[st], ((t / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
         }
-        const int k0 = t * kBN;
+        const int k0 = (t0 + t) * kBN;
         if constexpr (MODE == kStd) {
           mbar_expect_tx(&bar_k[st], C::TILE);
           load_tile<D>(sKt(st, 0), &tm_k, &bar_k[st], k0, bh);
@@ -283,7 +309,7 @@ __global__ void __launch_bounds__(192, 1)
         if constexpr (MODE == kStd) {
           mma_qk<D>(tmem + (b ? C::COL_S1 : C::COL_S0), aQ, aK, idesc_qk, false);
         } else if constexpr (MODE == kPiecewise) {
-          const int cls = pw_class(q0, t * kBN, args.P_SEQ, args.w);
+          const int cls = pw_class(q0, (t0 + t) * kBN, args.P_SEQ, args.w);
           const uint32_t sb = tmem + (b ? C::COL_S1 : C::COL_S0);
           if (cls == kNear) {
             mma_qk<D>(sb, aQ, aK, idesc_qk, false);
@@ -291,7 +317,7 @@ __global__ void __launch_bounds__(192, 1)
             mma_qk<D>(sb, aQ2, smem_u32(sKt(st, 1)), idesc_qk, false);
           } else {
             // the previous tile's softmax must be done with the third buffer
-            if (t > 0 && pw_class(q0, (t - 1) * kBN, args.P_SEQ, args.w) == (kNear | kFar)) {
+            if (t > 0 && pw_class(q0, (t0 + t - 1) * kBN, args.P_SEQ, args.w) == (kNear | kFar)) {
               if (!warp_wait(&bar_p[(t - 1) % NBUF], ((t - 1) / NBUF) & 1, ctl, kErrTimeoutSoftmax)) {
                 ok = false;
                 break;
@@ -330,7 +356,7 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      const int k0 = t * kBN;
+      const int k0 = (t0 + t) * kBN;
       uint32_t s[128];
       const uint32_t s_col = (NBUF == 2 && b) ? C::COL_S1 : C::COL_S0;
       int cls = kNear;
@@ -456,53 +482,128 @@ __global__ void __launch_bounds__(192, 1)
     if (nkv > 0) ok = warp_wait(&bar_ofinal, 0, ctl, kErrTimeoutMma) && __all_sync(0xffffffffu, ok);
     tc_fence_after();
     const bool live = ok && nkv > 0;
-    const float inv_l = (live && l > 0.f) ? 1.f / l : 0.f;
-    if (row < args.M) {
-      T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
-      T* trow = nullptr;
-      if constexpr (MODE == kJvp) trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
-      args.lse[static_cast<size_t>(bh) * args.M + row] =
-          (live && l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
-      if constexpr (MODE == kJvp) {  // tL = sum_j P_ij T_ij = mu / l
-        if (args.tlse) args.tlse[static_cast<size_t>(bh) * args.M + row] = (live && l > 0.f) ? mu * inv_l : 0.f;
-      }
-      (void)trow;
-      if (!live) {
-        float z[32];
+    if (SPLIT && part == 1) {
+      // Hand the raw state over to the first CTA of the pair (which writes
+      // every output row); a CTA without key tiles has nothing to hand over.
+      if (nkv > 0) {
+        float* hs = reinterpret_cast<float*>(base);
+        hs[r] = live ? m_ref : -INFINITY;
+        hs[kBM + r] = live ? l : 0.f;
+        hs[2 * kBM + r] = live ? mu : 0.f;
+        float4* ho = reinterpret_cast<float4*>(base + kSplitHdr);
+        if (live) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = 0.f;
+          for (int a = 0; a < NACC; ++a) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld_x32(lane_addr + (a ? C::COL_U : C::COL_O) + 32 * c, ov);
+              tmem_ld_wait(ov);
+#pragma unroll
+              for (int g = 0; g < 8; ++g)
+                ho[((a * (D / 32) + c) * 8 + g) * kBM + r] =
+                    make_float4(__uint_as_float(ov[4 * g]), __uint_as_float(ov[4 * g + 1]),
+                                __uint_as_float(ov[4 * g + 2]), __uint_as_float(ov[4 * g + 3]));
+            }
+          }
+        }
+        mbar_arrive_cluster(mapa_shared(smem_u32(&bar_peer), 0));
+      }
+    } else {
+      // SPLIT: fold the partner's state in (a0, a1 scale this CTA's and the
+      // partner's accumulators; a1 = 0 leaves this CTA's own state).
+      float a0 = 1.f, a1 = 0.f;
+      uint32_t peer = 0;
+      if constexpr (SPLIT) {
+        if (n_peer > 0) {
+          const bool got = __all_sync(0xffffffffu, mbar_wait_cluster(&bar_peer, 0, ctl, kErrTimeoutOther));
+          peer = mapa_shared(smem_u32(base), 1);
+          if (got && live) {
+            const float m1 = ld_cluster_f32(peer + 4 * r);
+            const float l1 = ld_cluster_f32(peer + 4 * (kBM + r));
+            const float mu1 = ld_cluster_f32(peer + 4 * (2 * kBM + r));
+            if (l1 > 0.f) {
+              if (l > 0.f) {
+                const float m = fmaxf(m_ref, m1);
+                a0 = ex2(m_ref - m);
+                a1 = ex2(m1 - m);
+                m_ref = m;
+              } else {
+                a0 = 0.f;
+                a1 = 1.f;
+                m_ref = m1;
+              }
+              l = a0 * l + a1 * l1;
+              mu = a0 * mu + a1 * mu1;
+            }
+          }
+        }
+      }
+      // acc chunk c of accumulator a (0: O, 1: U), this CTA's TMEM rows merged with the partner's
+      auto acc_chunk = [&](int a, int c, const uint32_t (&ov)[32], float (&out)[32], float scale) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) out[j] = __uint_as_float(ov[j]) * a0;
+        if (SPLIT && a1 != 0.f) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const float4 pv = ld_cluster_v4(peer + kSplitHdr + (((a * (D / 32) + c) * 8 + g) * kBM + r) * 16);
+            out[4 * g] = fmaf(a1, pv.x, out[4 * g]);
+            out[4 * g + 1] = fmaf(a1, pv.y, out[4 * g + 1]);
+            out[4 * g + 2] = fmaf(a1, pv.z, out[4 * g + 2]);
+            out[4 * g + 3] = fmaf(a1, pv.w, out[4 * g + 3]);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) out[j] *= scale;
+      };
+      const float inv_l = (live && l > 0.f) ? 1.f / l : 0.f;
+      if (row < args.M) {
+        T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
+        T* trow = nullptr;
+        if constexpr (MODE == kJvp) trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
+        args.lse[static_cast<size_t>(bh) * args.M + row] =
+            (live && l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+        if constexpr (MODE == kJvp) {  // tL = sum_j P_ij T_ij = mu / l
+          if (args.tlse) args.tlse[static_cast<size_t>(bh) * args.M + row] = (live && l > 0.f) ? mu * inv_l : 0.f;
+        }
+        (void)trow;
+        if (!live) {
+          float z[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) z[j] = 0.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            store_row_chunk<T>(orow + 32 * c, z, 0.f, chunk_groups(args.dg, 32 * c));
+            if constexpr (MODE == kJvp) store_row_chunk<T>(trow + 32 * c, z, 0.f, chunk_groups(args.dg, 32 * c));
+          }
+        }
+      }
+      if (live) {
+        // tcgen05.ld is warp-collective: every lane loads, rows >= M skip the store.
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          store_row_chunk<T>(orow + 32 * c, z, 0.f, chunk_groups(args.dg, 32 * c));
-          if constexpr (MODE == kJvp) store_row_chunk<T>(trow + 32 * c, z, 0.f, chunk_groups(args.dg, 32 * c));
-        }
-      }
-    }
-    if (live) {
-      // tcgen05.ld is warp-collective: every lane loads, rows >= M skip the store.
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tmem_ld_x32(lane_addr + C::COL_O + 32 * c, ov);
-        tmem_ld_wait(ov);
-        float of[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) of[j] = __uint_as_float(ov[j]) * inv_l;
-        if (row < args.M) {
-          T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
-          store_row_chunk<T>(orow + 32 * c, of, 1.f, chunk_groups(args.dg, 32 * c));
-        }
-        if constexpr (MODE == kJvp) {
-          uint32_t uv[32];
-          tmem_ld_x32(lane_addr + C::COL_U + 32 * c, uv);
-          tmem_ld_wait(uv);
-          const float mu_l = mu * inv_l;
-          float tv[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) tv[j] = __uint_as_float(uv[j]) * inv_l - mu_l * of[j];
+          uint32_t ov[32];
+          tmem_ld_x32(lane_addr + C::COL_O + 32 * c, ov);
+          tmem_ld_wait(ov);
+          float of[32];
+          acc_chunk(0, c, ov, of, inv_l);
           if (row < args.M) {
-            T* trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
-            store_row_chunk<T>(trow + 32 * c, tv, 1.f, chunk_groups(args.dg, 32 * c));
+            T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
+            store_row_chunk<T>(orow + 32 * c, of, 1.f, chunk_groups(args.dg, 32 * c));
+          }
+          if constexpr (MODE == kJvp) {
+            uint32_t uv[32];
+            tmem_ld_x32(lane_addr + C::COL_U + 32 * c, uv);
+            tmem_ld_wait(uv);
+            const float mu_l = mu * inv_l;
+            float tv[32];
+            acc_chunk(1, c, uv, tv, inv_l);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) tv[j] -= mu_l * of[j];
+            if (row < args.M) {
+              T* trow = reinterpret_cast<T*>(args.to) + (static_cast<size_t>(bh) * args.M + row) * args.dg;
+              store_row_chunk<T>(trow + 32 * c, tv, 1.f, chunk_groups(args.dg, 32 * c));
+            }
           }
         }
       }
@@ -511,8 +612,29 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
+  // SPLIT: the second CTA's shared memory stays alive until the first has read it
+  if constexpr (SPLIT) cluster_sync_all();
   tc_fence_after();
   if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+template <typename T, int MODE, int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q2,
+                    const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2,
+                    const FwdArgs args) {
+  fwd1_body<T, MODE, D, false>(tm_q, tm_k, tm_v, tm_q2, tm_k2, tm_v2, args);
+}
+
+// Grid (BH, 2 x query tiles): blocks (x, 2i) and (x, 2i + 1) form a cluster.
+template <typename T, int MODE, int D>
+__global__ void __cluster_dims__(1, 2, 1) __launch_bounds__(192, 1)
+    attn_fwd_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q2,
+                          const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2,
+                          const FwdArgs args) {
+  fwd1_body<T, MODE, D, true>(tm_q, tm_k, tm_v, tm_q2, tm_k2, tm_v2, args);
 }
 
 // ======================================================================
@@ -889,8 +1011,18 @@ __global__ void __launch_bounds__(320, 1)
 
 // ---------------------------------------------------------------- host side
 template <typename T, int MODE, int D>
-static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, cudaStream_t stream) {
+static cudaError_t launch_fwd_t(const FwdMaps& maps, const FwdArgs& a, bool split, cudaStream_t stream) {
   using C = FwdCfg<MODE, D>;
+  if (split) {
+    if (2ll * a.num_q_tiles > 65535) return cudaErrorInvalidValue;
+    auto kern = attn_fwd_split_kernel<T, MODE, D>;
+    static std::atomic<bool> attr[kMaxDevices];
+    cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
+    if (e_attr != cudaSuccess) return e_attr;
+    dim3 grid(a.BH, 2 * a.num_q_tiles);
+    kern<<<grid, 192, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, maps.v2, a);
+    return cudaGetLastError();
+  }
   auto kern = attn_fwd_kernel<T, MODE, D>;
   static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
@@ -921,7 +1053,11 @@ static cudaError_t launch_fwd2_t(const FwdMaps& maps, const FwdArgs& a, cudaStre
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s) {
+bool fwd_split_capable(int mode, int D) { return mode == kJvp || (mode == kPiecewise && D == 128); }
+
+cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, bool split,
+                       cudaStream_t s) {
+  if (split && !fwd_split_capable(mode, D)) return cudaErrorInvalidValue;
   if (mode == kStd) {
     if (D == 64) return bf16 ? launch_fwd2_t<__nv_bfloat16, 64>(maps, a, s) : launch_fwd2_t<__half, 64>(maps, a, s);
     if (D == 128) return bf16 ? launch_fwd2_t<__nv_bfloat16, 128>(maps, a, s) : launch_fwd2_t<__half, 128>(maps, a, s);
@@ -930,8 +1066,8 @@ cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const Fw
     return bf16 ? launch_fwd2_t<__nv_bfloat16, 64, true>(maps, a, s) : launch_fwd2_t<__half, 64, true>(maps, a, s);
 #define TA_FWD_CASE(MODE_, D_)                                                          \
   if (mode == MODE_ && D == D_)                                                         \
-    return bf16 ? launch_fwd_t<__nv_bfloat16, MODE_, D_>(maps, a, s)                    \
-                : launch_fwd_t<__half, MODE_, D_>(maps, a, s);
+    return bf16 ? launch_fwd_t<__nv_bfloat16, MODE_, D_>(maps, a, split, s)             \
+                : launch_fwd_t<__half, MODE_, D_>(maps, a, split, s);
   TA_FWD_CASE(kPiecewise, 128)
   TA_FWD_CASE(kJvp, 64)
   TA_FWD_CASE(kJvp, 128)

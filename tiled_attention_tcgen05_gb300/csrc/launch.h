@@ -20,7 +20,11 @@ struct BwdMaps {
   CUtensorMap q2, k2;       // piecewise only
 };
 
-cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s);
+// split: run the one-query-tile forward as two-CTA clusters that share each
+// query tile's key tiles (fwd_split_capable(mode, D) kernels only).
+bool fwd_split_capable(int mode, int D);
+cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, bool split,
+                       cudaStream_t s);
 // e5m2 forward: maps.q, maps.k are [BH, S, D] 8-bit maps with 128 x 128 boxes,
 // maps.v the transposed V [BH, D, N] with 128 x D boxes.
 cudaError_t launch_fwd_f8(int D, const FwdMaps& maps, const FwdArgs& a, cudaStream_t s);

@@ -8,8 +8,9 @@ Workloads (synth_inputs.WORKLOADS): 1 fwd+bwd fp16 B1 H2 S128 D64 non-causal;
 D128; 4 JVP forward (with tL) and the backward of the JVP, fp16 B2 H8 S1024
 D64 (--causal 0/1); 5 piecewise fwd+bwd bf16 causal B2 H16 S4096 D64 w=512.
 --shape B,H,S,D replaces the workload's sizes; --op merge / --op fp8 runs the
-merge (forward and backward) or the e5m2 forward instead.  Prints the mean
-milliseconds per step.
+merge (forward and backward) or the e5m2 forward instead; --kv-split sets
+the key split of the one-query-tile forward.  Prints the mean milliseconds per
+step.
 """
 from __future__ import annotations
 
@@ -87,8 +88,11 @@ def main():
     ap.add_argument("--shape", type=str, default=None, help="B,H,S,D instead of the workload's own (M = N = S)")
     ap.add_argument("--op", type=str, default=None, choices=["merge", "fp8"],
                     help="time attn_merge_fwd/bwd or attn_fwd_fp8 instead of a workload")
+    ap.add_argument("--kv-split", type=str, default="auto", choices=["auto", "never", "always"],
+                    help="key split of the one-query-tile forward (JVP, D = 128 piecewise)")
     a = ap.parse_args()
     ta.load()
+    ta.set_fwd_kv_split(a.kv_split)
     shape = tuple(int(x) for x in a.shape.split(",")) if a.shape else None
     step = make_op_step(a.op, shape) if a.op else make_step(a.workload, a.causal, shape)
     for _ in range(a.warmup):
