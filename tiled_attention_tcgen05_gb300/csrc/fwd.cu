@@ -51,14 +51,23 @@ struct FwdCfg {
   static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
   // Two S buffers let QK^T(t + 1) run before P V(t); that needs a second
   // K/V stage (tile t + 1's keys arrive while tile t's values are in use).
-  static constexpr int NBUF = (MODE == kJvp || STAGES < 2) ? 1 : 2;
+  // The JVP at D = 64 (JVP2) double-buffers S and keeps T in a buffer of its
+  // own: S0 | S1 | T | O | U fill the 512 columns.  P goes over the first 64
+  // columns of its S buffer and P o T over the other 64, so T's columns are
+  // free once the softmax has read T, and T(t + 1) is computed while the
+  // softmax still works on tile t.  At D = 128 the JVP keeps one S buffer
+  // (S | T | O | U) and writes P o T over T.
+  static constexpr bool JVP2 = (MODE == kJvp && D == 64);
+  static constexpr int NBUF = ((MODE == kJvp && !JVP2) || STAGES < 2) ? 1 : 2;
   static constexpr int SMEM = NQ * TILE + STAGES * STAGE + 1024;
   static constexpr uint32_t COL_S0 = 0;    // S (buffer 0) | jvp S
-  static constexpr uint32_t COL_S1 = 128;  // S (buffer 1) | jvp T
-  static constexpr uint32_t COL_O = 256;
-  static constexpr uint32_t COL_U = 256 + D;  // jvp tangent accumulator
+  static constexpr uint32_t COL_S1 = 128;  // S (buffer 1) | jvp (D = 128) T
+  static constexpr uint32_t COL_T = JVP2 ? 256 : 128;  // jvp T
+  static constexpr uint32_t COL_O = JVP2 ? 384 : 256;
+  static constexpr uint32_t COL_U = COL_O + D;  // jvp tangent accumulator
   static constexpr uint32_t COL_X = 256 + D;  // piecewise: S(q2, k2) of a tile that needs both products
   static_assert(STAGES >= 1, "tile does not fit in shared memory");
+  static_assert(!JVP2 || STAGES >= 2, "the JVP's second S buffer needs a second K/V stage");
   static_assert(COL_U + (MODE == kJvp ? D : 0) <= 512, "TMEM overflow");
   static_assert(MODE != kPiecewise || COL_X + 128 <= 512, "TMEM overflow");
 };
@@ -167,6 +176,7 @@ __device__ __forceinline__ void fwd1_body(const CUtensorMap& tm_q, const CUtenso
   __shared__ __align__(8) uint64_t bar_s[NBUF], bar_p[NBUF];
   __shared__ __align__(8) uint64_t bar_o, bar_ofinal;
   __shared__ __align__(8) uint64_t bar_peer;  // SPLIT: the second CTA's state is ready (first CTA's copy)
+  __shared__ __align__(8) uint64_t bar_t, bar_tfree;  // JVP2: T(t) computed / T(t) read by the softmax
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -205,6 +215,8 @@ __device__ __forceinline__ void fwd1_body(const CUtensorMap& tm_q, const CUtenso
     mbar_init(&bar_o, 1);
     mbar_init(&bar_ofinal, 1);
     mbar_init(&bar_peer, kBM);
+    mbar_init(&bar_t, 1);
+    mbar_init(&bar_tfree, 4);
     fence_mbar_init();
   }
   if (warp == 5) {
@@ -284,9 +296,10 @@ __device__ __forceinline__ void fwd1_body(const CUtensorMap& tm_q, const CUtenso
         tc_fence_after();
         const uint32_t p_col = (NBUF == 2) ? (b ? C::COL_S1 : C::COL_S0) : C::COL_S0;
         mma_pv<D>(tmem + C::COL_O, tmem + p_col, smem_u32(sVt(st, 0)), idesc_pv, u > 0);
-        if constexpr (MODE == kJvp) {
-          mma_pv<D>(tmem + C::COL_U, tmem + C::COL_S1, smem_u32(sVt(st, 0)), idesc_pv, u > 0);
-          mma_pv<D>(tmem + C::COL_U, tmem + C::COL_S0, smem_u32(sVt(st, 1)), idesc_pv, true);
+        if constexpr (MODE == kJvp) {  // U += (P o T) V + P tV
+          const uint32_t pt_col = C::JVP2 ? p_col + 64 : C::COL_T;
+          mma_pv<D>(tmem + C::COL_U, tmem + pt_col, smem_u32(sVt(st, 0)), idesc_pv, u > 0);
+          mma_pv<D>(tmem + C::COL_U, tmem + p_col, smem_u32(sVt(st, 1)), idesc_pv, true);
         }
         commit_el(&bar_empty[st]);
         commit_el(done_bar);
@@ -328,12 +341,21 @@ __device__ __forceinline__ void fwd1_body(const CUtensorMap& tm_q, const CUtenso
             mma_qk<D>(tmem + C::COL_X, aQ2, smem_u32(sKt(st, 1)), idesc_qk, false);
           }
         } else {
-          mma_qk<D>(tmem + C::COL_S0, aQ, aK, idesc_qk, false);
+          mma_qk<D>(tmem + (b ? C::COL_S1 : C::COL_S0), aQ, aK, idesc_qk, false);
+          if constexpr (C::JVP2) {
+            commit_el(&bar_s[b]);
+            // T's columns are free once the softmax has read T(t - 1)
+            if (t > 0 && !warp_wait(&bar_tfree, (t - 1) & 1, ctl, kErrTimeoutSoftmax)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           // T = tq K^T + q tk^T (the sm_scale factor is applied by the softmax)
-          mma_qk<D>(tmem + C::COL_S1, aQ2, aK, idesc_qk, false);
-          mma_qk<D>(tmem + C::COL_S1, aQ, smem_u32(sKt(st, 1)), idesc_qk, true);
+          mma_qk<D>(tmem + C::COL_T, aQ2, aK, idesc_qk, false);
+          mma_qk<D>(tmem + C::COL_T, aQ, smem_u32(sKt(st, 1)), idesc_qk, true);
         }
-        commit_el(&bar_s[b]);
+        commit_el(C::JVP2 ? &bar_t : &bar_s[b]);
         if (NBUF == 2 && t > 0) {
           ok = issue_pv(t - 1, &bar_o);
         }
@@ -432,13 +454,27 @@ __device__ __forceinline__ void fwd1_body(const CUtensorMap& tm_q, const CUtenso
         tmem_st_x16(lane_addr + p_col + 16 * c, pk);
       }
       if constexpr (MODE == kJvp) {
-        // P o T (T = sm_scale * (tq k^T + q tk^T)) over the first 64 columns of T
+        // P o T (T = sm_scale * (tq k^T + q tk^T)), 16-bit, over the second
+        // half of the S buffer (JVP2) or the first 64 columns of T
+        if constexpr (C::JVP2) {
+          if (!warp_wait(&bar_t, t & 1, ctl, kErrTimeoutMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        const uint32_t pt_col = C::JVP2 ? s_col + 64 : C::COL_T;
         float mp4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t tr[32];
-          tmem_ld_x32(lane_addr + C::COL_S1 + 32 * c, tr);
+          tmem_ld_x32(lane_addr + C::COL_T + 32 * c, tr);
           tmem_ld_wait(tr);
+          if (C::JVP2 && c == 3) {  // every T column read: T(t + 1) may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar_tfree);
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -447,7 +483,7 @@ __device__ __forceinline__ void fwd1_body(const CUtensorMap& tm_q, const CUtenso
             mp4[j & 3] += a0 + a1;
             pk[j] = pack2<BF>(a0, a1);
           }
-          tmem_st_x16(lane_addr + C::COL_S1 + 16 * c, pk);
+          tmem_st_x16(lane_addr + pt_col + 16 * c, pk);
         }
         mu = mu * alpha + ((mp4[0] + mp4[1]) + (mp4[2] + mp4[3]));
       }
