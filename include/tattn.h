@@ -63,7 +63,8 @@ typedef enum {
   TA_ERR_UNSUPPORTED = 2, /* D or dtype outside the supported set */
   TA_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned */
   TA_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
-  TA_ERR_TIMEOUT = 5      /* a kernel's bounded wait ran out (ta_sync_status) */
+  TA_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (ta_sync_status) */
+  TA_ERR_GUARD = 6        /* guard build only: a device-side check failed (ta_sync_status) */
 } ta_status;
 
 typedef enum { TA_F16 = 0, TA_BF16 = 1, TA_F32 = 2 } ta_dtype;
@@ -234,7 +235,8 @@ ta_status attn_merge_bwd(const void* o1, const float* lse1, const void* o2, cons
                          int M, int D, ta_dtype dt, void* stream);
 /* Synchronises `stream`, then reads and clears the device error word that
  * the kernels set when a bounded wait runs out.  TA_OK, TA_ERR_TIMEOUT or
- * TA_ERR_CUDA (an asynchronous CUDA error). */
+ * TA_ERR_CUDA (an asynchronous CUDA error); in the guard build also
+ * TA_ERR_GUARD when a device-side check failed since the last call. */
 ta_status ta_sync_status(void* stream);
 
 /* Human-readable name of a status code (static string). */
@@ -273,6 +275,26 @@ int ta_profile_read(const char** names, int* launches, double* total_ms, int cap
  * the estimate, 1 never, 2 wherever the kernel supports it. */
 int ta_fwd_kv_split(int entry, int B, int H, int M, int N, int D, ta_dtype dt, int causal, int num_sms);
 void ta_set_fwd_kv_split(int mode);
+
+/* Guard build (no counterpart on the pages; it stands in for a memory-error
+ * checker).  The same sources compiled with TA_GUARD into libtattn_guard.so
+ * check, on the device, the operands of every TMA load (destination inside
+ * the block's dynamic shared memory on a 1024-byte boundary, innermost
+ * coordinate a multiple of 16 elements, no negative coordinate), every TMEM
+ * load and store (lane field = the calling warp's quadrant, columns inside
+ * the 512 allocated), every MMA batch (accumulator and TMEM operand inside
+ * the allocation, shared-memory descriptors inside the dynamic shared
+ * memory), the 16-byte alignment of the row stores and every CTA's work
+ * decode.  A failed check skips its access and makes ta_sync_status return
+ * TA_ERR_GUARD.  ta_guard_build() is 1 in that library and 0 in libtattn.so;
+ * ta_guard_last() describes the first failing check ("unit.cu:line", the
+ * value it rejected and the block's dynamic shared memory base and size) that the
+ * last TA_ERR_GUARD reported; ta_selftest_guard() launches one thread that
+ * fails a check on purpose without touching memory (TA_ERR_GUARD at the next
+ * ta_sync_status in the guard build, TA_OK in the product build). */
+int ta_guard_build(void);
+const char* ta_guard_last(void);
+ta_status ta_selftest_guard(void* stream);
 
 /* Per-launch wait limit in milliseconds used by every kernel (default 2000,
  * or the TA_WAIT_TIMEOUT_MS environment variable at load time). */

@@ -177,3 +177,16 @@ def test_forward_key_split_choice(lib):
     finally:
         lib.ta_set_fwd_kv_split(0)
     assert f(JVP, 2, 8, 1024, 1024, 64, F16, 0, 152) == 1
+
+
+def test_guard_build_flag(lib):
+    """libtattn.so compiles the device-side checks out; libtattn_guard.so (the
+    test build, csrc/guard.cuh) has them and exports the same functions."""
+    assert lib.ta_guard_build() == 0
+    assert lib.ta_guard_last() == b""
+    from tiled_attention_tcgen05_gb300 import build
+    g = ctypes.CDLL(build.build(guard=True))
+    g.ta_guard_build.restype = ctypes.c_int
+    assert g.ta_guard_build() == 1
+    for n in declared_functions():
+        assert hasattr(g, n), f"{n} declared in tattn.h but not exported by the guard build"

@@ -34,7 +34,7 @@ _LIB_PATH = os.path.join(_PKG, "libtattn.so")
 _lib = None
 
 STATUS = {0: "TA_OK", 1: "TA_ERR_INVALID_ARG", 2: "TA_ERR_UNSUPPORTED", 3: "TA_ERR_ALIGNMENT",
-          4: "TA_ERR_CUDA", 5: "TA_ERR_TIMEOUT"}
+          4: "TA_ERR_CUDA", 5: "TA_ERR_TIMEOUT", 6: "TA_ERR_GUARD"}
 _DT = {torch.float16: 0, torch.bfloat16: 1, torch.float32: 2}
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -62,6 +62,9 @@ _SIGS = {
     "ta_set_wait_timeout_ms": ([_i], None),
     "ta_fwd_kv_split": ([_i] * 9, _i),
     "ta_set_fwd_kv_split": ([_i], None),
+    "ta_guard_build": ([], _i),
+    "ta_guard_last": ([], ctypes.c_char_p),
+    "ta_selftest_guard": ([_vp], _i),
 }
 
 

@@ -18,6 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtattn.so")
+# The guard build (device-side checks compiled in with TA_GUARD, see
+# csrc/guard.cuh): a test library, built beside the product one.
+BUILD_GUARD = os.path.join(PKG, "_build_guard")
+LIB_GUARD = os.path.join(PKG, "libtattn_guard.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + os.path.join(ROOT, "include")]
@@ -41,14 +45,16 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(p) for p in paths if os.path.exists(p))
 
 
-def build(verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile and link; returns the path of libtattn.so."""
+def build(verbose: bool = False, ptxas_info: bool = False, guard: bool = False) -> str:
+    """Compile and link; returns the path of libtattn.so (guard=True:
+    libtattn_guard.so, the same sources with the device-side checks)."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    bdir, lib = (BUILD_GUARD, LIB_GUARD) if guard else (BUILD, LIB)
+    os.makedirs(bdir, exist_ok=True)
     newest = _deps_mtime()
     srcs = _sources()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    objs = [os.path.join(bdir, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DTA_GUARD"] if guard else [])
 
     def compile_one(pair):
         src, obj = pair
@@ -65,14 +71,14 @@ def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     for log in logs:
         if log:
             sys.stderr.write(log)
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + ".tmp"
+    if not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + ".tmp"
         cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

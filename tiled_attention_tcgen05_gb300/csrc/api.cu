@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -32,6 +33,37 @@ static uint32_t* error_word_ptr() {
     cache[dev].store(w, std::memory_order_release);
   }
   return w;
+}
+
+// ------------------------------------------------------------ guard build
+// "unit:line value .. smem base+size" of the first guard failure seen by the
+// last ta_sync_status that found one (guard build), "" otherwise.
+static char g_guard_last[128] = "";
+
+static ta_status guard_status() {
+#ifdef TA_GUARD
+  struct Unit {
+    const char* name;
+    uint32_t (*take)(uint32_t*);
+  };
+  static const Unit units[] = {{"aux.cu", guard_take_aux},       {"fwd.cu", guard_take_fwd},
+                               {"fwd_f8.cu", guard_take_fwd_f8}, {"bwd.cu", guard_take_bwd},
+                               {"bwd_fused.cu", guard_take_bwd_fused}, {"bwd_jvp.cu", guard_take_bwd_jvp},
+                               {"merge.cu", guard_take_merge},   {"fp32.cu", guard_take_fp32}};
+  bool failed = false;
+  for (const Unit& u : units) {
+    uint32_t info[4] = {0u, 0u, 0u, 0u};  // line, rejected value, shared memory base, size
+    if (u.take(info) != 0u) {
+      if (!failed)
+        std::snprintf(g_guard_last, sizeof(g_guard_last), "%s:%u value 0x%x smem 0x%x+0x%x", u.name, info[0],
+                      info[1], info[2], info[3]);
+      failed = true;
+    }
+  }
+  return failed ? TA_ERR_GUARD : TA_OK;
+#else
+  return TA_OK;
+#endif
 }
 
 static uint64_t g_timeout_ns = [] {
@@ -588,6 +620,14 @@ using namespace ta;
 
 extern "C" {
 
+int ta_guard_build(void) { return ta::kGuardBuild ? 1 : 0; }
+
+const char* ta_guard_last(void) { return ta::g_guard_last; }
+
+ta_status ta_selftest_guard(void* stream) {
+  return ta::launch_guard_selftest(static_cast<cudaStream_t>(stream)) == cudaSuccess ? TA_OK : TA_ERR_CUDA;
+}
+
 const char* ta_status_str(ta_status s) {
   switch (s) {
     case TA_OK: return "TA_OK";
@@ -596,6 +636,7 @@ const char* ta_status_str(ta_status s) {
     case TA_ERR_ALIGNMENT: return "TA_ERR_ALIGNMENT";
     case TA_ERR_CUDA: return "TA_ERR_CUDA";
     case TA_ERR_TIMEOUT: return "TA_ERR_TIMEOUT";
+    case TA_ERR_GUARD: return "TA_ERR_GUARD";
   }
   return "TA_ERR_UNKNOWN";
 }
@@ -812,7 +853,7 @@ ta_status ta_sync_status(void* stream) {
     if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return TA_ERR_CUDA;
     return TA_ERR_TIMEOUT;
   }
-  return TA_OK;
+  return ta::guard_status();
 }
 
 ta_status ta_profile_enable(int on) {

@@ -216,4 +216,18 @@ cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Guard self-test: one thread evaluates a check that fails by construction
+// (no memory is touched); in the guard build it records kErrGuard and this
+// line, in the product build the check is compiled out.
+__global__ void guard_selftest_kernel(int zero) {
+  if (!TA_CHECK(zero != 0)) return;
+}
+
+cudaError_t launch_guard_selftest(cudaStream_t s) {
+  guard_selftest_kernel<<<1, 1, 0, s>>>(0);
+  return cudaGetLastError();
+}
+
 }  // namespace ta
+
+TA_GUARD_ACCESSOR(aux)

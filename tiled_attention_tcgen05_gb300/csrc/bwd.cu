@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int bh, kt;  // key tiles with the most query tiles (the first ones, causal) first
-  grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt);
+  if (!grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt)) return;
   const int k0 = kt * kBN;
   const int num_q_tiles = (args.M + kBM - 1) / kBM;
   const int i0 = first_q_tile_for(k0, args.P_SEQ, args.causal);
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int lane = threadIdx.x & 31;
   const int num_q_tiles = (args.M + kBM - 1) / kBM;
   int bh, rank;
-  grouped_tile(blockIdx.x, args.BH, num_q_tiles, kGroupHeads, &bh, &rank);
+  if (!grouped_tile(blockIdx.x, args.BH, num_q_tiles, kGroupHeads, &bh, &rank)) return;
   const int qt = num_q_tiles - 1 - rank;  // heaviest causal tiles first
   const int q0 = qt * kBM;
   const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
@@ -900,7 +900,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int lane = threadIdx.x & 31;
   const int num_q_tiles = (args.M + kBM - 1) / kBM;
   int bh, rank;
-  grouped_tile(blockIdx.x, args.BH, num_q_tiles, kGroupHeads, &bh, &rank);
+  if (!grouped_tile(blockIdx.x, args.BH, num_q_tiles, kGroupHeads, &bh, &rank)) return;
   const int qt = num_q_tiles - 1 - rank;  // heaviest causal tiles first
   const int q0 = qt * kBM;
   const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
@@ -1180,7 +1180,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int bh, kt;  // key tiles with the most query tiles (the first ones, causal) first
-  grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt);
+  if (!grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt)) return;
   const int k0 = kt * kBN;
   const int num_q_tiles = (args.M + kBM - 1) / kBM;
   const int i0 = first_q_tile_for(k0, args.P_SEQ, args.causal);
@@ -1517,3 +1517,5 @@ cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& m, const Bw
 }
 
 }  // namespace ta
+
+TA_GUARD_ACCESSOR(bwd)

@@ -10,6 +10,7 @@ namespace ta {
 template <typename T>
 __device__ __forceinline__ void store_chunk32(T* dst, const uint32_t* v, float scale, int ng) {
   constexpr bool BF = DT<T>::bf16;
+  if (!TA_CHECK((reinterpret_cast<uintptr_t>(dst) & 15u) == 0u && ng >= 0 && ng <= 4)) return;
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {

@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int bh, kt;  // key tiles with the most queries (the first ones, causal) first
-  grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt);
+  if (!grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt)) return;
   const int k0 = kt * kBN;
   const int num_steps = (args.M + kQS - 1) / kQS;
   int s0 = 0;  // first step that sees one of the tile's keys
@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const int q0 = (s0 + s) * kQS;
       float* row = acc + static_cast<size_t>(q0) * D;
       const int nrow = args.M - q0;  // rows of the step that exist
+      if (!TA_CHECK(q0 >= 0 && q0 < args.M && bh < args.BH)) continue;
 #pragma unroll
       for (int jr = 0; jr < kQS; ++jr)
         if (jr < nrow) red_add_f32(row + static_cast<size_t>(jr) * D, __uint_as_float(v[jr]));
@@ -552,3 +553,5 @@ cudaError_t launch_bwd_fused(bool bf16, int D, const BwdMaps& m, const BwdArgs& 
 }
 
 }  // namespace ta
+
+TA_GUARD_ACCESSOR(bwd_fused)

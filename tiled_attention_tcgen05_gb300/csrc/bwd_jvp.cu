@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
   const int x_len = KEYS ? args.N : args.M;  // rows of the stationary tensors
   const int ntiles = (x_len + kBM - 1) / kBM;
   int bh, rank;
-  grouped_tile(blockIdx.x, args.BH, ntiles, kGroupHeads, &bh, &rank);
+  if (!grouped_tile(blockIdx.x, args.BH, ntiles, kGroupHeads, &bh, &rank)) return;
   const int xt = KEYS ? rank : ntiles - 1 - rank;  // heaviest causal tiles first
   const int x0 = xt * kBM;
   // streamed steps u0 .. u0 + nu - 1 (64 rows each)
@@ -528,3 +528,5 @@ cudaError_t launch_bwd_jvp(bool keys, bool bf16, int D, const JvpBwdMaps& m, con
 }
 
 }  // namespace ta
+
+TA_GUARD_ACCESSOR(bwd_jvp)

@@ -92,7 +92,9 @@ __host__ __device__ inline int first_q_tile_for(int k0, int P_SEQ, int causal) {
 // taken in groups of G (so the resident CTAs of one wave share the K/V or
 // Q/dO of only G heads and reuse them through L2), and within a group rank 0
 // (the caller's heaviest tile) comes first for every head.
-__device__ __forceinline__ void grouped_tile(int id, int BH, int ntiles, int G, int* bh, int* rank) {
+// Returns false (a guard-build check) when the block index decodes outside
+// the problem; the caller's CTA then does nothing.
+__device__ __forceinline__ bool grouped_tile(int id, int BH, int ntiles, int G, int* bh, int* rank) {
   const int per_group = G * ntiles;
   const int grp = id / per_group;
   const int h0 = grp * G;
@@ -100,6 +102,7 @@ __device__ __forceinline__ void grouped_tile(int id, int BH, int ntiles, int G, 
   const int within = id - grp * per_group;
   *rank = within / gh;
   *bh = h0 + within % gh;
+  return TA_CHECK(gh > 0 && *bh >= 0 && *bh < BH && *rank >= 0 && *rank < ntiles);
 }
 constexpr int kGroupHeads = 8;
 

@@ -529,3 +529,5 @@ cudaError_t launch_f32_jvp_bwd(int D, const F32JvpPtrs& p, const BwdArgs& a, cud
 }
 
 }  // namespace ta
+
+TA_GUARD_ACCESSOR(fp32)

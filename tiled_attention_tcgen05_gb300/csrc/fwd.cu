@@ -128,6 +128,7 @@ __device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_
 template <typename T>
 __device__ __forceinline__ void store_row_chunk(T* dst, const float* v32, float scale, int ng = 4) {
   constexpr bool BF = DT<T>::bf16;
+  if (!TA_CHECK((reinterpret_cast<uintptr_t>(dst) & 15u) == 0u && ng >= 0 && ng <= 4)) return;
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -185,6 +186,7 @@ __device__ __forceinline__ void fwd1_body(const CUtensorMap& tm_q, const CUtenso
   const int bh = blockIdx.x;
   const int part = SPLIT ? static_cast<int>(blockIdx.y & 1) : 0;  // = rank in the (1, 2, 1) cluster
   const int qt = args.num_q_tiles - 1 - static_cast<int>(SPLIT ? blockIdx.y >> 1 : blockIdx.y);  // heaviest first
+  if (!TA_CHECK(bh < args.BH && qt >= 0 && qt < args.num_q_tiles)) return;  // both CTAs of a pair alike
   const int q0 = qt * kBM;
   const int nkv_all = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
   const int h_split = (nkv_all + 1) >> 1;
@@ -728,7 +730,7 @@ __device__ __forceinline__ void fwd2_body(const CUtensorMap& tm_q, const CUtenso
   const int lane = threadIdx.x & 31;
   const int pairs = (args.M + 2 * kBM - 1) / (2 * kBM);
   int bh, rank;
-  grouped_tile(blockIdx.x, args.BH, pairs, args.group_heads, &bh, &rank);
+  if (!grouped_tile(blockIdx.x, args.BH, pairs, args.group_heads, &bh, &rank)) return;
   const int pair = pairs - 1 - rank;  // heaviest causal pairs first
   const int q0 = pair * 2 * kBM;
   int n_t[2];
@@ -1112,3 +1114,5 @@ cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const Fw
 }
 
 }  // namespace ta
+
+TA_GUARD_ACCESSOR(fwd)

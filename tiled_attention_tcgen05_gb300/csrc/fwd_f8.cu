@@ -70,6 +70,7 @@ __device__ __forceinline__ uint32_t pack4_e5m2(float a, float b, float c, float 
 
 // 32 fp32 values (x scale) -> 32 e5m2 bytes at dst (16-byte aligned).
 __device__ __forceinline__ void store_chunk32_e5m2(uint8_t* dst, const float* v, float scale) {
+  if (!TA_CHECK((reinterpret_cast<uintptr_t>(dst) & 15u) == 0u)) return;
   uint4 u[2];
   uint32_t* w = reinterpret_cast<uint32_t*>(u);
 #pragma unroll
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(320, 1)
   const int lane = threadIdx.x & 31;
   const int pairs = (args.M + 2 * kBM - 1) / (2 * kBM);
   int bh, rank;
-  grouped_tile(blockIdx.x, args.BH, pairs, kGroupHeads, &bh, &rank);
+  if (!grouped_tile(blockIdx.x, args.BH, pairs, kGroupHeads, &bh, &rank)) return;
   const int pair = pairs - 1 - rank;  // heaviest causal pairs first
   const int q0 = pair * 2 * kBM;
   int n_t[2];
@@ -362,3 +363,5 @@ cudaError_t launch_fwd_f8(int D, const FwdMaps& maps, const FwdArgs& a, cudaStre
 }
 
 }  // namespace ta
+
+TA_GUARD_ACCESSOR(fwd_f8)

@@ -23,6 +23,22 @@ struct BwdMaps {
 // split: run the one-query-tile forward as two-CTA clusters that share each
 // query tile's key tiles (fwd_split_capable(mode, D) kernels only).
 bool fwd_split_capable(int mode, int D);
+// One thread fails a guard check on purpose (guard build; nothing in the
+// product build).
+cudaError_t launch_guard_selftest(cudaStream_t s);
+#ifdef TA_GUARD
+// Each translation unit's guard word: returns the failure bits and copies the
+// first failure's line, rejected value, shared memory base and size to
+// info[0..3] (all cleared).
+uint32_t guard_take_aux(uint32_t* info);
+uint32_t guard_take_fwd(uint32_t* info);
+uint32_t guard_take_fwd_f8(uint32_t* info);
+uint32_t guard_take_bwd(uint32_t* info);
+uint32_t guard_take_bwd_fused(uint32_t* info);
+uint32_t guard_take_bwd_jvp(uint32_t* info);
+uint32_t guard_take_merge(uint32_t* info);
+uint32_t guard_take_fp32(uint32_t* info);
+#endif
 cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, bool split,
                        cudaStream_t s);
 // e5m2 forward: maps.q, maps.k are [BH, S, D] 8-bit maps with 128 x 128 boxes,

@@ -196,3 +196,5 @@ cudaError_t launch_merge(bool bwd, int dtype, int D, const MergePtrs& p, long lo
 }
 
 }  // namespace ta
+
+TA_GUARD_ACCESSOR(merge)

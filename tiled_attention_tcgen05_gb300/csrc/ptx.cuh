@@ -115,6 +115,10 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 // bytes on `bar`.  Coordinates are element indices (innermost first).
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1,
                                             int c2) {
+  if (!TA_CHECK_V((smem_u32(dst) & 1023u) == 0u && guard_in_dyn_smem(smem_u32(dst)) && (c0 & 15) == 0 && c1 >= 0 &&
+                      c2 >= 0,
+                  smem_u32(dst)))
+    return;
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
@@ -375,6 +379,16 @@ template <int N>
 __device__ __forceinline__ void mma_ss_n(uint32_t d, const uint64_t (&a)[N], const uint64_t (&b)[N], uint32_t idesc,
                                          uint32_t acc) {
   static_assert(N == 2 || N == 4 || N == 8, "batch of 2, 4 or 8");
+#ifdef TA_GUARD
+  // value: the accumulator address, or 0x80000000 | the first rejected descriptor's address field
+  uint32_t bad = (guard_tmem_cols(d, 1) && (d >> 16) == 0u) ? 0u : (d | 1u);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if (!bad && !guard_sdesc(a[i])) bad = 0x80000000u | static_cast<uint32_t>(a[i] & 0x3FFFu);
+    if (!bad && !guard_sdesc(b[i])) bad = 0xC0000000u | static_cast<uint32_t>(b[i] & 0x3FFFu);
+  }
+  if (!TA_CHECK_V(bad == 0u, bad)) return;
+#endif
   if constexpr (N == 8) mma_ss_x8(d, a, b, idesc, acc);
   else if constexpr (N == 4) mma_ss_x4(d, a, b, idesc, acc);
   else mma_ss_x2(d, a, b, idesc, acc);
@@ -383,6 +397,15 @@ template <int N>
 __device__ __forceinline__ void mma_ts_n(uint32_t d, const uint32_t (&a)[N], const uint64_t (&b)[N], uint32_t idesc,
                                          uint32_t acc) {
   static_assert(N == 2 || N == 4 || N == 8, "batch of 2, 4 or 8");
+#ifdef TA_GUARD
+  uint32_t bad = (guard_tmem_cols(d, 1) && (d >> 16) == 0u) ? 0u : (d | 1u);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if (!bad && !(guard_tmem_cols(a[i], 1) && (a[i] >> 16) == 0u)) bad = a[i] | 1u;
+    if (!bad && !guard_sdesc(b[i])) bad = 0xC0000000u | static_cast<uint32_t>(b[i] & 0x3FFFu);
+  }
+  if (!TA_CHECK_V(bad == 0u, bad)) return;
+#endif
   if constexpr (N == 8) mma_ts_x8(d, a, b, idesc, acc);
   else if constexpr (N == 4) mma_ts_x4(d, a, b, idesc, acc);
   else mma_ts_x2(d, a, b, idesc, acc);
@@ -391,6 +414,16 @@ template <int N>
 __device__ __forceinline__ void mma_ss_f8_n(uint32_t d, const uint64_t (&a)[N], const uint64_t (&b)[N], uint32_t idesc,
                                             uint32_t acc) {
   static_assert(N == 2 || N == 4 || N == 8, "batch of 2, 4 or 8");
+#ifdef TA_GUARD
+  // value: the accumulator address, or 0x80000000 | the first rejected descriptor's address field
+  uint32_t bad = (guard_tmem_cols(d, 1) && (d >> 16) == 0u) ? 0u : (d | 1u);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if (!bad && !guard_sdesc(a[i])) bad = 0x80000000u | static_cast<uint32_t>(a[i] & 0x3FFFu);
+    if (!bad && !guard_sdesc(b[i])) bad = 0xC0000000u | static_cast<uint32_t>(b[i] & 0x3FFFu);
+  }
+  if (!TA_CHECK_V(bad == 0u, bad)) return;
+#endif
   if constexpr (N == 8) mma_ss_f8_x8(d, a, b, idesc, acc);
   else if constexpr (N == 4) mma_ss_f8_x4(d, a, b, idesc, acc);
   else mma_ss_f8_x2(d, a, b, idesc, acc);
@@ -399,6 +432,15 @@ template <int N>
 __device__ __forceinline__ void mma_ts_f8_n(uint32_t d, const uint32_t (&a)[N], const uint64_t (&b)[N],
                                             uint32_t idesc, uint32_t acc) {
   static_assert(N == 2 || N == 4 || N == 8, "batch of 2, 4 or 8");
+#ifdef TA_GUARD
+  uint32_t bad = (guard_tmem_cols(d, 1) && (d >> 16) == 0u) ? 0u : (d | 1u);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if (!bad && !(guard_tmem_cols(a[i], 1) && (a[i] >> 16) == 0u)) bad = a[i] | 1u;
+    if (!bad && !guard_sdesc(b[i])) bad = 0xC0000000u | static_cast<uint32_t>(b[i] & 0x3FFFu);
+  }
+  if (!TA_CHECK_V(bad == 0u, bad)) return;
+#endif
   if constexpr (N == 8) mma_ts_f8_x8(d, a, b, idesc, acc);
   else if constexpr (N == 4) mma_ts_f8_x4(d, a, b, idesc, acc);
   else mma_ts_f8_x2(d, a, b, idesc, acc);
