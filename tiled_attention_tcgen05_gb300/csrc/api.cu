@@ -397,7 +397,7 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
             make_map(&maps.v, v, p.BH, p.N, p.D, p.bf16) &&
             make_map(&maps.q2, q2 ? q2 : q, p.BH, p.M, p.D, p.bf16) &&
             make_map(&maps.k2, k2 ? k2 : k, p.BH, p.N, p.D, p.bf16) &&
-            make_map(&maps.v2, v2 ? v2 : v, p.BH, p.N, p.D, p.bf16);
+            make_map(&maps.v2, v2 ? v2 : v, p.BH, p.N, p.D, p.bf16) && make_map(&maps.o, o, p.BH, p.M, p.D, p.bf16);
   if (!ok) return TA_ERR_CUDA;
   FwdArgs a = fwd_args(p, causal, w, o, lse, to, tlse);
   static const char* names[3] = {"attn_fwd", "piecewise_fwd", "attn_fwd_jvp"};
@@ -405,6 +405,14 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
   cudaError_t e = launch_fwd(mode, p.bf16, kernel_d(p.D), maps, a, fwd_split_plan(mode, p, causal, device_sms()), s);
   prof_end(s);
   return cuda_status(e);
+}
+
+// Maps of the gradients the standard backward kernels store by TMA (those
+// that are not null).
+static bool make_grad_maps(BwdMaps* m, const Problem& p, void* dq, void* dk, void* dv) {
+  return (!dq || make_map(&m->dq, dq, p.BH, p.M, p.D, p.bf16)) &&
+         (!dk || make_map(&m->dk, dk, p.BH, p.N, p.D, p.bf16)) &&
+         (!dv || make_map(&m->dv, dv, p.BH, p.N, p.D, p.bf16));
 }
 
 static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* k, const void* v,
@@ -456,7 +464,7 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
   bool ok = make_map(&maps.q, q, p.BH, p.M, p.D, p.bf16) && make_map(&maps.k, k, p.BH, p.N, p.D, p.bf16) &&
             make_map(&maps.v, v, p.BH, p.N, p.D, p.bf16) && make_map(&maps.dO, dO, p.BH, p.M, p.D, p.bf16) &&
             make_map(&maps.q2, q2 ? q2 : q, p.BH, p.M, p.D, p.bf16) &&
-            make_map(&maps.k2, k2 ? k2 : k, p.BH, p.N, p.D, p.bf16);
+            make_map(&maps.k2, k2 ? k2 : k, p.BH, p.N, p.D, p.bf16) && make_grad_maps(&maps, p, dq, dk, dv);
   if (!ok) return TA_ERR_CUDA;
   BwdArgs a = bwd_args(p, causal, w, lse, delta);
   a.dq = dq;
@@ -566,7 +574,7 @@ static ta_status run_bwd_jvp(const Problem& p, const void* q, const void* k, con
          make_map(m64[i], mrows[i], p.BH, p.M, p.D, p.bf16, 64) &&
          make_map(n128[i], nrows[i], p.BH, p.N, p.D, p.bf16, 128) &&
          make_map(n64[i], nrows[i], p.BH, p.N, p.D, p.bf16, 64);
-  if (!ok) return TA_ERR_CUDA;
+  if (!ok || !make_grad_maps(&maps, p, dtq, dtk, dtv)) return TA_ERR_CUDA;
   const int kd = kernel_d(p.D);
   // the JVP kernels write the tangents' gradients too where TMEM has room;
   // otherwise the plain backward of dtO computes them

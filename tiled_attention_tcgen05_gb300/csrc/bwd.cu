@@ -885,7 +885,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_std_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                           const BwdArgs args) {
+                           const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args) {
   using C = DqStdCfg<D>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
@@ -1076,12 +1076,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (nkv > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
-    T* dq = reinterpret_cast<T*>(args.dq) + g * args.dg;
-    const int dc = hc * (D / 2);
-    if (ok && nkv > 0) {
-      epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, true, args.sm_scale, args.dg);
-    } else if (in_m) {
-      zero_half<T, D>(dq, dc, args.dg);
+    // dQ (x sm_scale), rounded, is staged over the ring's first K slot (free:
+    // every MMA has finished) in the output map's swizzled box layout and
+    // written by TMA stores, which clip rows past M and columns past D.
+    (void)g;
+    const bool live = ok && nkv > 0;
+#pragma unroll
+    for (int cc = 0; cc < D / 64; ++cc) {
+      const int c = hc * (D / 64) + cc;  // this thread's 32-column chunks of the row
+      uint32_t v[32];
+      if (live) {
+        tmem_ld_x32(lane_addr + C::COL_DQ + 32 * c, v);
+        tmem_ld_wait(v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+      stage_row_chunk_sw128<BF>(smem_u32(sK(0)), r, c, v, args.sm_scale);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, kRowWarps * 32);
+    if (warp == 0 && lane == 0 && q0 < args.M) {
+#pragma unroll
+      for (int kb = 0; kb < D / 64; ++kb) tma_store_3d(&tm_dq, sK(0) + kb * (kBM * 128), kb * 64, q0, bh);
+      tma_store_commit_and_wait_read();
     }
   }
 
@@ -1150,6 +1168,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_std_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                             const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                              const BwdArgs args) {
   using C = DkdvStdCfg<D>;
   constexpr bool BF = DT<T>::bf16;
@@ -1421,17 +1440,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ epilogue
     if (nq > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
-    const bool st_row = j < args.N;
-    const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * args.dg;
-    T* dvp = reinterpret_cast<T*>(args.dv) + off;
-    T* dkp = reinterpret_cast<T*>(args.dk) + off;
-    const int dc = hc * (D / 2);
-    if (ok && nq > 0) {
-      epilogue_half<T, D>(lane_addr + C::COL_DV, dvp, dc, st_row, true, 1.f, args.dg);
-      epilogue_half<T, D>(lane_addr + C::COL_DK, dkp, dc, st_row, true, args.sm_scale, args.dg);
-    } else if (st_row) {
-      zero_half<T, D>(dvp, dc, args.dg);
-      zero_half<T, D>(dkp, dc, args.dg);
+    // dV and dK (x sm_scale), rounded, are staged over the K and V tiles
+    // (free: every MMA has finished) in the output maps' swizzled box layout
+    // and written by TMA stores, which clip rows past N and columns past D.
+    (void)j;
+    const int r = threadIdx.x & 127;  // this thread's key within the tile
+    const bool live = ok && nq > 0;
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {  // 0: dV over K, 1: dK over V
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = hc * (D / 64) + cc;  // this thread's 32-column chunks of the row
+        uint32_t v[32];
+        if (live) {
+          tmem_ld_x32(lane_addr + (a ? C::COL_DK : C::COL_DV) + 32 * c, v);
+          tmem_ld_wait(v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        stage_row_chunk_sw128<BF>(smem_u32(a ? sV : sK), r, c, v, a ? args.sm_scale : 1.f);
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, kRowWarps * 32);
+    if (warp == 0 && lane == 0 && k0 < args.N) {
+#pragma unroll
+      for (int kb = 0; kb < D / 64; ++kb) {
+        tma_store_3d(&tm_dv, sK + kb * (kBM * 128), kb * 64, k0, bh);
+        tma_store_3d(&tm_dk, sV + kb * (kBM * 128), kb * 64, k0, bh);
+      }
+      tma_store_commit_and_wait_read();
     }
   }
 
@@ -1477,7 +1516,7 @@ static cudaError_t launch_dkdv_std_t(const BwdMaps& m, const BwdArgs& a, cudaStr
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, a);
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv, a);
   return cudaGetLastError();
 }
 
@@ -1504,7 +1543,7 @@ static cudaError_t launch_dq_std_t(const BwdMaps& m, const BwdArgs& a, cudaStrea
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, a);
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.dq, a);
   return cudaGetLastError();
 }
 

@@ -106,6 +106,27 @@ __device__ __forceinline__ bool grouped_tile(int id, int BH, int ntiles, int G, 
 }
 constexpr int kGroupHeads = 8;
 
+// Stages 32 fp32 values (x scale, rounded to 16 bits) of row r, columns
+// [32 c, 32 c + 32), into a tile laid out as a 128-byte-swizzled TMA box
+// sequence: 64-column boxes of 128 rows x 128 bytes, box kb at
+// tile + kb * 16 KB, and in row r the 16-byte chunk j at position j ^ (r % 8)
+// (the layout CU_TENSOR_MAP_SWIZZLE_128B reads; a warp's 32 rows then spread
+// over the eight 16-byte bank groups).  `v` are fp32 bit patterns.
+template <bool BF>
+__device__ __forceinline__ void stage_row_chunk_sw128(uint32_t tile, int r, int c, const uint32_t* v, float scale) {
+  const uint32_t rowp = tile + static_cast<uint32_t>((c >> 1) * (kBM * 128) + r * 128);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = 4 * (c & 1) + q;
+    const uint32_t* u = v + 8 * q;
+    sts_v4(rowp + static_cast<uint32_t>((j ^ (r & 7)) << 4),
+           pack2<BF>(__uint_as_float(u[0]) * scale, __uint_as_float(u[1]) * scale),
+           pack2<BF>(__uint_as_float(u[2]) * scale, __uint_as_float(u[3]) * scale),
+           pack2<BF>(__uint_as_float(u[4]) * scale, __uint_as_float(u[5]) * scale),
+           pack2<BF>(__uint_as_float(u[6]) * scale, __uint_as_float(u[7]) * scale));
+  }
+}
+
 template <typename T>
 struct DT;
 template <>

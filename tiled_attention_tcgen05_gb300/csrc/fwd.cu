@@ -713,7 +713,8 @@ struct Fwd2Cfg {
 // kernel parameters, whose addresses the TMA instructions take.
 template <typename T, int D, bool PW>
 __device__ __forceinline__ void fwd2_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                          const CUtensorMap& tm_q2, const CUtensorMap& tm_k2, const FwdArgs args) {
+                                          const CUtensorMap& tm_q2, const CUtensorMap& tm_k2, const CUtensorMap& tm_o,
+                                          const FwdArgs args) {
   using C = Fwd2Cfg<D, PW>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int KST = C::KST, VST = C::VST;
@@ -1006,23 +1007,30 @@ __device__ __forceinline__ void fwd2_body(const CUtensorMap& tm_q, const CUtenso
     tc_fence_after();
     const bool live = ok && n > 0;
     const float inv_l = (live && l > 0.f) ? 1.f / l : 0.f;
-    T* orow = reinterpret_cast<T*>(args.o) + (static_cast<size_t>(bh) * args.M + (row < args.M ? row : 0)) * args.dg;
     if (row < args.M)
       args.lse[static_cast<size_t>(bh) * args.M + row] = (live && l > 0.f) ? (m_ref + lg2(l)) * kLn2 : -INFINITY;
+    // O of the tile, scaled and rounded, is staged over the tile's Q buffer
+    // (free: every MMA has finished) in the output map's swizzled box layout
+    // and written by TMA stores, which clip rows past M and columns past D.
+    const uint32_t stage = smem_u32(sQ) + static_cast<uint32_t>(w * C::TILE);
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
-      float of[32];
+      uint32_t ov[32];
       if (live) {
-        uint32_t ov[32];
         tmem_ld_x32(lane_addr + col_o[w] + 32 * c, ov);
         tmem_ld_wait(ov);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) of[j] = __uint_as_float(ov[j]);
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) of[j] = 0.f;
+        for (int j = 0; j < 32; ++j) ov[j] = 0u;
       }
-      if (row < args.M) store_row_chunk<T>(orow + 32 * c, of, inv_l, chunk_groups(args.dg, 32 * c));
+      stage_row_chunk_sw128<BF>(stage, r, c, ov, inv_l);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + w, 4 * 32);  // the tile's four warps have staged their rows
+    if ((warp & 3) == 0 && lane == 0 && tq0 < args.M) {
+#pragma unroll
+      for (int kb = 0; kb < D / 64; ++kb) tma_store_3d(&tm_o, sQ + w * C::TILE + kb * (kBM * 128), kb * 64, tq0, bh);
+      tma_store_commit_and_wait_read();
     }
   }
 
@@ -1035,16 +1043,18 @@ __device__ __forceinline__ void fwd2_body(const CUtensorMap& tm_q, const CUtenso
 template <typename T, int D>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
-  fwd2_body<T, D, false>(tm_q, tm_k, tm_v, tm_q, tm_k, args);
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                     const FwdArgs args) {
+  fwd2_body<T, D, false>(tm_q, tm_k, tm_v, tm_q, tm_k, tm_o, args);
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(320, 1)
     attn_fwd2_pw_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_k1,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q2,
-                        const __grid_constant__ CUtensorMap tm_k2, const FwdArgs args) {
-  fwd2_body<T, D, true>(tm_q1, tm_k1, tm_v, tm_q2, tm_k2, args);
+                        const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_o,
+                        const FwdArgs args) {
+  fwd2_body<T, D, true>(tm_q1, tm_k1, tm_v, tm_q2, tm_k2, tm_o, args);
 }
 
 // ---------------------------------------------------------------- host side
@@ -1081,12 +1091,13 @@ static cudaError_t launch_fwd2_t(const FwdMaps& maps, const FwdArgs& a, cudaStre
     auto kern = attn_fwd2_pw_kernel<T, D>;
     cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
     if (e_attr != cudaSuccess) return e_attr;
-    kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, a);
+    kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.q2, maps.k2, maps.o,
+                                                                   a);
   } else {
     auto kern = attn_fwd2_kernel<T, D>;
     cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
     if (e_attr != cudaSuccess) return e_attr;
-    kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, a);
+    kern<<<static_cast<unsigned>(blocks), 320, C::SMEM, stream>>>(maps.q, maps.k, maps.v, maps.o, a);
   }
   return cudaGetLastError();
 }

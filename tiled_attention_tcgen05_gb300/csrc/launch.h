@@ -13,11 +13,13 @@ namespace ta {
 struct FwdMaps {
   CUtensorMap q, k, v;     // standard: q, k, v
   CUtensorMap q2, k2, v2;  // piecewise: q2, k2 (v2 unused); jvp: tq, tk, tv
+  CUtensorMap o;           // the output O (the two-tile forward stores it by TMA)
 };
 
 struct BwdMaps {
   CUtensorMap q, k, v, dO;  // piecewise: q1, k1, v, dO
   CUtensorMap q2, k2;       // piecewise only
+  CUtensorMap dq, dk, dv;   // outputs of the standard kernels, stored by TMA (built where not null)
 };
 
 // split: run the one-query-tile forward as two-CTA clusters that share each

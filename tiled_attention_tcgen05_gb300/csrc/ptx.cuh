@@ -126,6 +126,38 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// 3-D tiled store of one box from shared memory (in the map's swizzled
+// layout) to global memory, tracked as a bulk async-group of this thread.
+// Parts of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  if (!TA_CHECK_V((smem_u32(src) & 1023u) == 0u && guard_in_dyn_smem(smem_u32(src)) && (c0 & 15) == 0 && c1 >= 0 &&
+                      c2 >= 0,
+                  smem_u32(src)))
+    return;
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// Closes this thread's pending bulk stores into one group, then waits until
+// every group has finished reading its shared-memory source (the source may
+// then be reused or freed; the global writes complete asynchronously).
+__device__ __forceinline__ void tma_store_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// 16-byte store to a shared-memory address.
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Barrier over `count` threads (a multiple of 32) on hardware barrier `id`
+// (1..15; 0 is __syncthreads').
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // 32-bit store to a shared-memory address.
 __device__ __forceinline__ void sts_b32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
