@@ -407,12 +407,15 @@ static ta_status run_fwd(int mode, const Problem& p, const void* q, const void* 
   return cuda_status(e);
 }
 
-// Maps of the gradients the standard backward kernels store by TMA (those
-// that are not null).
-static bool make_grad_maps(BwdMaps* m, const Problem& p, void* dq, void* dk, void* dv) {
+// Maps of the gradients the backward kernels store by TMA (those that are
+// not null).
+static bool make_grad_maps(BwdMaps* m, const Problem& p, void* dq, void* dk, void* dv, void* dq2 = nullptr,
+                           void* dk2 = nullptr) {
   return (!dq || make_map(&m->dq, dq, p.BH, p.M, p.D, p.bf16)) &&
          (!dk || make_map(&m->dk, dk, p.BH, p.N, p.D, p.bf16)) &&
-         (!dv || make_map(&m->dv, dv, p.BH, p.N, p.D, p.bf16));
+         (!dv || make_map(&m->dv, dv, p.BH, p.N, p.D, p.bf16)) &&
+         (!dq2 || make_map(&m->dq2, dq2, p.BH, p.M, p.D, p.bf16)) &&
+         (!dk2 || make_map(&m->dk2, dk2, p.BH, p.N, p.D, p.bf16));
 }
 
 static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* k, const void* v,
@@ -464,7 +467,7 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
   bool ok = make_map(&maps.q, q, p.BH, p.M, p.D, p.bf16) && make_map(&maps.k, k, p.BH, p.N, p.D, p.bf16) &&
             make_map(&maps.v, v, p.BH, p.N, p.D, p.bf16) && make_map(&maps.dO, dO, p.BH, p.M, p.D, p.bf16) &&
             make_map(&maps.q2, q2 ? q2 : q, p.BH, p.M, p.D, p.bf16) &&
-            make_map(&maps.k2, k2 ? k2 : k, p.BH, p.N, p.D, p.bf16) && make_grad_maps(&maps, p, dq, dk, dv);
+            make_map(&maps.k2, k2 ? k2 : k, p.BH, p.N, p.D, p.bf16) && make_grad_maps(&maps, p, dq, dk, dv, dq2, dk2);
   if (!ok) return TA_ERR_CUDA;
   BwdArgs a = bwd_args(p, causal, w, lse, delta);
   a.dq = dq;
@@ -595,6 +598,12 @@ static ta_status run_bwd_jvp(const Problem& p, const void* q, const void* k, con
     prof_end(s);
     if (e != cudaSuccess) return TA_ERR_CUDA;
   }
+  ok = make_map(&jm.dq, dq, p.BH, p.M, p.D, p.bf16) && make_map(&jm.dk, dk, p.BH, p.N, p.D, p.bf16) &&
+       make_map(&jm.dv, dv, p.BH, p.N, p.D, p.bf16) &&
+       (!ap.dtq || make_map(&jm.dtq, dtq, p.BH, p.M, p.D, p.bf16)) &&
+       (!ap.dtk || make_map(&jm.dtk, dtk, p.BH, p.N, p.D, p.bf16)) &&
+       (!ap.dtv || make_map(&jm.dtv, dtv, p.BH, p.N, p.D, p.bf16));
+  if (!ok) return TA_ERR_CUDA;
   prof_begin("attn_bwd_jvp_dkdv", s);
   e = launch_bwd_jvp(true, p.bf16, kd, jm, ap, s);
   prof_end(s);

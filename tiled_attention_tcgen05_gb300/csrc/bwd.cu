@@ -118,7 +118,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
-                         const BwdArgs args) {
+                         const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dk,
+                         const __grid_constant__ CUtensorMap tm_dk2, const BwdArgs args) {
   using C = DkdvCfg<MODE, D, PART>;
   constexpr bool kDV = PART != 1, kDK1 = PART != 1, kDK2 = PART != 0;  // outputs of this launch
   constexpr bool BF = DT<T>::bf16;
@@ -458,26 +459,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (nq > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
     const bool live = ok && nq > 0;
-    const bool st_row = j < args.N;
-    const size_t off = (static_cast<size_t>(bh) * args.N + (st_row ? j : 0)) * args.dg;
-    T* dv = reinterpret_cast<T*>(args.dv) + off;
-    T* dk = reinterpret_cast<T*>(args.dk) + off;
-    const int dc = hc * (D / 2);  // this thread's half of the D columns
-    if (live) {
-      if constexpr (kDV) epilogue_half<T, D>(lane_addr + C::COL_DV, dv, dc, st_row, true, 1.f, args.dg);
-      if constexpr (!PW) {
-        epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, true, args.sm_scale, args.dg);
-      } else {
-        T* dk2 = reinterpret_cast<T*>(args.dk2) + off;
-        if constexpr (kDK1)
-          epilogue_half<T, D>(lane_addr + C::COL_DK, dk, dc, st_row, touched1, args.sm_scale, args.dg);
-        if constexpr (kDK2)
-          epilogue_half<T, D>(lane_addr + C::COL_DK2, dk2, dc, st_row, touched2, args.sm_scale, args.dg);
+    (void)j;
+    // The launch's outputs (dV, dK or dK1, dK2), rounded, are staged over the
+    // resident K / K2 / V tiles (free: every MMA has finished) in the output
+    // maps' swizzled box layout and written by TMA stores, which clip rows
+    // past N and columns past D.  An output no query tile touched is zero.
+    const int r = threadIdx.x & 127;  // this thread's key within the tile
+    auto stage_out = [&](int slot, uint32_t col, bool touched, float scale) {
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = hc * (D / 64) + cc;  // this thread's 32-column chunks of the row
+        uint32_t v[32];
+        if (live && touched) {
+          tmem_ld_x32(lane_addr + col + 32 * c, v);
+          tmem_ld_wait(v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        stage_row_chunk_sw128<BF>(smem_u32(base + slot * C::TILE), r, c, v, scale);
       }
-    } else if (st_row) {
-      if constexpr (kDV) zero_half<T, D>(dv, dc, args.dg);
-      if constexpr (kDK1) zero_half<T, D>(dk, dc, args.dg);
-      if constexpr (PW && kDK2) zero_half<T, D>(reinterpret_cast<T*>(args.dk2) + off, dc, args.dg);
+    };
+    if constexpr (kDV) stage_out(0, C::COL_DV, true, 1.f);
+    if constexpr (kDK1) stage_out(1, C::COL_DK, !PW || touched1, args.sm_scale);
+    if constexpr (PW && kDK2) stage_out(2, C::COL_DK2, touched2, args.sm_scale);
+    fence_proxy_async_smem();
+    named_bar_sync(1, kRowWarps * 32);
+    if (warp == 0 && lane == 0 && k0 < args.N) {
+#pragma unroll
+      for (int kb = 0; kb < D / 64; ++kb) {
+        const int off = kb * (kBM * 128);
+        if constexpr (kDV) tma_store_3d(&tm_dv, base + off, kb * 64, k0, bh);
+        if constexpr (kDK1) tma_store_3d(&tm_dk, base + C::TILE + off, kb * 64, k0, bh);
+        if constexpr (PW && kDK2) tma_store_3d(&tm_dk2, base + 2 * C::TILE + off, kb * 64, k0, bh);
+      }
+      tma_store_commit_and_wait_read();
     }
   }
 
@@ -515,6 +531,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
+                       const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dq2,
                        const BwdArgs args) {
   using C = DqCfg<MODE, D>;
   constexpr bool BF = DT<T>::bf16;
@@ -800,19 +817,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (nkv > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
     const bool live = ok && nkv > 0;
-    T* dq = reinterpret_cast<T*>(args.dq) + g * args.dg;
-    const int dc = hc * (D / 2);
-    if (live) {
-      if constexpr (!PW) {
-        epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, true, args.sm_scale, args.dg);
-      } else {
-        T* dq2 = reinterpret_cast<T*>(args.dq2) + g * args.dg;
-        epilogue_half<T, D>(lane_addr + C::COL_DQ, dq, dc, in_m, touched1, args.sm_scale, args.dg);
-        epilogue_half<T, D>(lane_addr + C::COL_DQ2, dq2, dc, in_m, touched2, args.sm_scale, args.dg);
+    (void)g;
+    (void)in_m;
+    // dQ (dQ1, dQ2), rounded, is staged over the resident Q / Q2 tiles (free:
+    // every MMA has finished) in the output maps' swizzled box layout and
+    // written by TMA stores, which clip rows past M and columns past D.  An
+    // output no key tile touched is zero.
+    auto stage_out = [&](int slot, uint32_t col, bool touched) {
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = hc * (D / 64) + cc;  // this thread's 32-column chunks of the row
+        uint32_t v[32];
+        if (live && touched) {
+          tmem_ld_x32(lane_addr + col + 32 * c, v);
+          tmem_ld_wait(v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        stage_row_chunk_sw128<BF>(smem_u32(base + slot * C::TILE), threadIdx.x & 127, c, v, args.sm_scale);
       }
-    } else if (in_m) {
-      zero_half<T, D>(dq, dc, args.dg);
-      if constexpr (PW) zero_half<T, D>(reinterpret_cast<T*>(args.dq2) + g * args.dg, dc, args.dg);
+    };
+    stage_out(0, C::COL_DQ, !PW || touched1);
+    if constexpr (PW) stage_out(1, C::COL_DQ2, touched2);
+    fence_proxy_async_smem();
+    named_bar_sync(1, kRowWarps * 32);
+    if (warp == 0 && lane == 0 && q0 < args.M) {
+#pragma unroll
+      for (int kb = 0; kb < D / 64; ++kb) {
+        tma_store_3d(&tm_dq, base + kb * (kBM * 128), kb * 64, q0, bh);
+        if constexpr (PW) tma_store_3d(&tm_dq2, base + C::TILE + kb * (kBM * 128), kb * 64, q0, bh);
+      }
+      tma_store_commit_and_wait_read();
     }
   }
 
@@ -1490,7 +1526,8 @@ static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, m.dv, m.dk,
+                                                                    m.dk2, a);
   return cudaGetLastError();
 }
 
@@ -1503,7 +1540,8 @@ static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t 
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, a);
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, m.dq, m.dq2,
+                                                                    a);
   return cudaGetLastError();
 }
 

@@ -124,6 +124,8 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
                         const __grid_constant__ CUtensorMap tx2, const __grid_constant__ CUtensorMap tx3,
                         const __grid_constant__ CUtensorMap ty0, const __grid_constant__ CUtensorMap ty1,
                         const __grid_constant__ CUtensorMap ty2, const __grid_constant__ CUtensorMap ty3,
+                        const __grid_constant__ CUtensorMap tz0, const __grid_constant__ CUtensorMap tz1,
+                        const __grid_constant__ CUtensorMap tz2, const __grid_constant__ CUtensorMap tz3,
                         const BwdArgs args) {
   using C = JvpBwdCfg<D>;
   constexpr bool BF = DT<T>::bf16;
@@ -447,39 +449,46 @@ __global__ void __launch_bounds__(kJvpThreads, 1)
     if (nu > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
     tc_fence_after();
     const bool live = ok && nu > 0;
-    const bool st_row = xr < x_len;
-    const size_t off = (static_cast<size_t>(bh) * x_len + (st_row ? xr : 0)) * args.dg;
-    const int dc = h * (D / 2);  // this thread's half of the D columns
-    if constexpr (KEYS) {
-      T* dv = reinterpret_cast<T*>(args.dv) + off;
-      T* dk = reinterpret_cast<T*>(args.dk) + off;
-      if (live) {
-        epilogue_half<T, D>(lane_addr + C::COL_ACC, dv, dc, st_row, true, 1.f, args.dg);
-        epilogue_half<T, D>(lane_addr + C::COL_ACC + D, dk, dc, st_row, true, args.sm_scale, args.dg);
-      } else if (st_row) {
-        zero_half<T, D>(dv, dc, args.dg);
-        zero_half<T, D>(dk, dc, args.dg);
-      }
-      if constexpr (TANG) {
-        T* dtv = reinterpret_cast<T*>(args.dtv) + off;
-        T* dtk = reinterpret_cast<T*>(args.dtk) + off;
+    // The outputs (KEYS: dV, dK, then dtV, dtK; else dQ, then dtQ), rounded,
+    // are staged over the stationary tiles (free: every MMA has finished) in
+    // the output maps' swizzled box layout and written by TMA stores, which
+    // clip rows past the tensor and columns past D.
+    auto stage_out = [&](int slot, uint32_t col, float scale) {
+#pragma unroll
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = h * (D / 64) + cc;  // this thread's 32-column chunks of the row
+        uint32_t v[32];
         if (live) {
-          epilogue_half<T, D>(lane_addr + C::COL_ACC + 2 * D, dtv, dc, st_row, true, 1.f, args.dg);
-          epilogue_half<T, D>(lane_addr + C::COL_ACC + 3 * D, dtk, dc, st_row, true, args.sm_scale, args.dg);
-        } else if (st_row) {
-          zero_half<T, D>(dtv, dc, args.dg);
-          zero_half<T, D>(dtk, dc, args.dg);
+          tmem_ld_x32(lane_addr + col + 32 * c, v);
+          tmem_ld_wait(v);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
+        stage_row_chunk_sw128<BF>(smem_u32(sX(slot)), row, c, v, scale);
+      }
+    };
+    constexpr int NOUT = KEYS ? (TANG ? 4 : 2) : (TANG ? 2 : 1);
+    if constexpr (KEYS) {
+      stage_out(0, C::COL_ACC, 1.f);
+      stage_out(1, C::COL_ACC + D, args.sm_scale);
+      if constexpr (TANG) {
+        stage_out(2, C::COL_ACC + 2 * D, 1.f);
+        stage_out(3, C::COL_ACC + 3 * D, args.sm_scale);
       }
     } else {
-      T* dq = reinterpret_cast<T*>(args.dq) + off;
-      if (live) epilogue_half<T, D>(lane_addr + C::COL_ACC, dq, dc, st_row, true, args.sm_scale, args.dg);
-      else if (st_row) zero_half<T, D>(dq, dc, args.dg);
-      if constexpr (TANG) {
-        T* dtq = reinterpret_cast<T*>(args.dtq) + off;
-        if (live) epilogue_half<T, D>(lane_addr + C::COL_ACC + D, dtq, dc, st_row, true, args.sm_scale, args.dg);
-        else if (st_row) zero_half<T, D>(dtq, dc, args.dg);
-      }
+      stage_out(0, C::COL_ACC, args.sm_scale);
+      if constexpr (TANG) stage_out(1, C::COL_ACC + D, args.sm_scale);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, kJvpRowWarps * 32);
+    if (warp == 0 && lane == 0 && x0 < x_len) {
+      const CUtensorMap* outs[4] = {&tz0, &tz1, &tz2, &tz3};
+#pragma unroll
+      for (int o = 0; o < NOUT; ++o)
+#pragma unroll
+        for (int kb = 0; kb < D / 64; ++kb) tma_store_3d(outs[o], sX(o) + kb * C::XBLK, kb * 64, x0, bh);
+      tma_store_commit_and_wait_read();
     }
   }
 
@@ -502,10 +511,12 @@ static cudaError_t launch_jvp_bwd_t(const JvpBwdMaps& m, const BwdArgs& a, cudaS
   if (blocks == 0) return cudaSuccess;
   if constexpr (KEYS) {
     kern<<<static_cast<unsigned>(blocks), kJvpThreads, C::SMEM, s>>>(m.k128, m.tk128, m.v128, m.tv128, m.q64,
-                                                                      m.tq64, m.do64, m.dto64, a);
+                                                                      m.tq64, m.do64, m.dto64, m.dv, m.dk, m.dtv,
+                                                                      m.dtk, a);
   } else {
     kern<<<static_cast<unsigned>(blocks), kJvpThreads, C::SMEM, s>>>(m.q128, m.tq128, m.do128, m.dto128, m.k64,
-                                                                      m.tk64, m.v64, m.tv64, a);
+                                                                      m.tk64, m.v64, m.tv64, m.dq, m.dtq, m.dq,
+                                                                      m.dq, a);
   }
   return cudaGetLastError();
 }

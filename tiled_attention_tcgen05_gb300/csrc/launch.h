@@ -19,7 +19,8 @@ struct FwdMaps {
 struct BwdMaps {
   CUtensorMap q, k, v, dO;  // piecewise: q1, k1, v, dO
   CUtensorMap q2, k2;       // piecewise only
-  CUtensorMap dq, dk, dv;   // outputs of the standard kernels, stored by TMA (built where not null)
+  CUtensorMap dq, dk, dv;   // outputs, stored by TMA (built where not null)
+  CUtensorMap dq2, dk2;     // piecewise outputs
 };
 
 // split: run the one-query-tile forward as two-CTA clusters that share each
@@ -72,6 +73,9 @@ cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& maps, const
 struct JvpBwdMaps {
   CUtensorMap q128, tq128, do128, dto128, k128, tk128, v128, tv128;
   CUtensorMap q64, tq64, do64, dto64, k64, tk64, v64, tv64;
+  // outputs, stored by TMA with 128-row boxes (the tangents' only where the
+  // JVP kernels form them)
+  CUtensorMap dq, dk, dv, dtq, dtk, dtv;
 };
 // eps_i = <dtO_i, O_i>, delta2_i = <dO_i, O_i> + <dtO_i, tO_i> for BH*M rows.
 cudaError_t launch_jvp_delta(bool bf16, int D, const void* o, const void* dO, const void* to, const void* dto,
