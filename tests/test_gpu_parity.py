@@ -92,7 +92,7 @@ PW_CASES = [
     (1, 1, 256, 256, 64, "f16", True, -10000),
     (1, 2, 200, 333, 64, "bf16", True, 77),
     (1, 2, 333, 200, 64, "f16", True, 64),
-    (1, 1, 512, 512, 128, "bf16", True, 256),  # D = 128: dK/dV in two launches (dV, dK1; then dK2)
+    (1, 1, 512, 512, 128, "bf16", True, 256),  # D = 128: the one-pass key side with 64-query steps
     (1, 2, 300, 333, 128, "f16", False, 40),
     (1, 1, 384, 256, 128, "bf16", True, 0),
     (1, 2, 256, 256, 32, "bf16", True, 60),

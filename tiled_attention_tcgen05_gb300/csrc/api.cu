@@ -49,7 +49,8 @@ static ta_status guard_status() {
   static const Unit units[] = {{"aux.cu", guard_take_aux},       {"fwd.cu", guard_take_fwd},
                                {"fwd_f8.cu", guard_take_fwd_f8}, {"bwd.cu", guard_take_bwd},
                                {"bwd_fused.cu", guard_take_bwd_fused}, {"bwd_jvp.cu", guard_take_bwd_jvp},
-                               {"merge.cu", guard_take_merge},   {"fp32.cu", guard_take_fp32}};
+                               {"merge.cu", guard_take_merge},   {"fp32.cu", guard_take_fp32},
+                               {"bwd_pw_steps.cu", guard_take_bwd_pw_steps}};
   bool failed = false;
   for (const Unit& u : units) {
     uint32_t info[4] = {0u, 0u, 0u, 0u};  // line, rejected value, shared memory base, size
@@ -491,7 +492,16 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
     return cuda_status(e);
   }
   prof_begin(pw ? "piecewise_bwd_dkdv" : "attn_bwd_dkdv", s);
-  e = launch_bwd_dkdv(mode, p.bf16, kernel_d(p.D), maps, a, s);
+  if (pw && bwd_pw_steps_supported(kernel_d(p.D))) {  // the key side in one pass, 64-query steps
+    if (!make_map(&maps.q64, q, p.BH, p.M, p.D, p.bf16, 64) || !make_map(&maps.q264, q2, p.BH, p.M, p.D, p.bf16, 64) ||
+        !make_map(&maps.dO64, dO, p.BH, p.M, p.D, p.bf16, 64)) {
+      prof_end(s);
+      return TA_ERR_CUDA;
+    }
+    e = launch_bwd_pw_steps(p.bf16, maps, a, s);
+  } else {
+    e = launch_bwd_dkdv(mode, p.bf16, kernel_d(p.D), maps, a, s);
+  }
   prof_end(s);
   if (e != cudaSuccess) return TA_ERR_CUDA;
   prof_begin(pw ? "piecewise_bwd_dq" : "attn_bwd_dq", s);

@@ -42,8 +42,9 @@
 // piecewise mode overlaps more at D = 64, where TMEM has room: dK/dV keeps
 // P^T in its last 64 columns so the next query tile's S^T starts as soon as
 // the softmax holds S^T in registers, and dQ alternates two S buffers.  At
-// D = 128 the piecewise dK/dV pass runs as two launches (dV and dK1, then
-// dK2) because TMEM cannot hold all three accumulators beside S^T and dP^T.
+// D = 128, where TMEM cannot hold all three accumulators beside a 128-query
+// tile's S^T and dP^T, the piecewise key side runs in bwd_pw_steps.cu with
+// 64-query steps instead.
 #include "bwd_common.cuh"
 #include "common.cuh"
 #include "launch.h"
@@ -87,10 +88,8 @@ __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_
 // ======================================================================
 //                        dK, dV (key-stationary)
 // ======================================================================
-// PART selects the outputs of the key-stationary kernel: -1 all of them; for
-// piecewise D = 128, where TMEM cannot hold dV, dK1 and dK2 beside the score
-// buffers, two launches: 0 = dV and dK1, 1 = dK2 alone.
-template <int MODE, int D, int PART = -1>
+// The generic key-stationary kernel (piecewise D = 64: dV, dK1 and dK2).
+template <int MODE, int D>
 struct DkdvCfg {
   static constexpr int BLK = kBM * 128;
   static constexpr int TILE = (D / 64) * BLK;
@@ -102,26 +101,24 @@ struct DkdvCfg {
   static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
   static constexpr int SMEM = NRES * TILE + STAGES * STAGE + 1024;
   static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D;
-  static constexpr uint32_t COL_DK2 = (PART == 1) ? 256 : 256 + 2 * D;
+  static constexpr uint32_t COL_DK2 = 256 + 2 * D;
   // Piecewise, all outputs, with 64 spare columns for P^T (D = 64) and two
   // query stages: P^T lives there, so S^T's buffer frees as soon as the
   // softmax holds S^T in registers and the next tile's score MMA can start.
-  static constexpr bool EARLY = (MODE == kPiecewise) && (PART == -1) && (256 + 3 * D + 64 <= 512) && STAGES >= 2;
+  static constexpr bool EARLY = (MODE == kPiecewise) && (256 + 3 * D + 64 <= 512) && STAGES >= 2;
   static constexpr uint32_t COL_P = 256 + 3 * D;
   static_assert(STAGES >= 1, "tile does not fit in shared memory");
-  static_assert((PART == 1 ? 256 + D : PART == 0 ? 256 + 2 * D : COL_DK2 + (MODE == kPiecewise ? D : 0)) <= 512,
-                "TMEM overflow");
+  static_assert(COL_DK2 + (MODE == kPiecewise ? D : 0) <= 512, "TMEM overflow");
 };
 
-template <typename T, int MODE, int D, int PART>
+template <typename T, int MODE, int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                          const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
                          const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dk,
                          const __grid_constant__ CUtensorMap tm_dk2, const BwdArgs args) {
-  using C = DkdvCfg<MODE, D, PART>;
-  constexpr bool kDV = PART != 1, kDK1 = PART != 1, kDK2 = PART != 0;  // outputs of this launch
+  using C = DkdvCfg<MODE, D>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
   constexpr bool PW = (MODE == kPiecewise);
@@ -322,15 +319,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         commit_el(&bar_dp);
         if (!(ok = warp_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        if constexpr (kDV) mma_tY<D>(tmem + C::COL_DV, tmem + C::COL_A, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
+        mma_tY<D>(tmem + C::COL_DV, tmem + C::COL_A, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
         if constexpr (!PW) {
           mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, u > 0);  // dK += dS^T Q
         } else {
-          if ((cls & kNearB) && kDK1) {
+          if (cls & kNearB) {
             mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
             acc1 = true;
           }
-          if ((cls & kFarB) && kDK2) {  // the far part of dS: COL_B when the whole tile is far
+          if (cls & kFarB) {  // the far part of dS: COL_B when the whole tile is far
             const uint32_t src = (cls == kFarB) ? C::COL_B : C::COL_A + 32;
             mma_tY<D>(tmem + C::COL_DK2, tmem + src, smem_u32(sQ2(st)), idesc_g, acc2);
             acc2 = true;
@@ -480,18 +477,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         stage_row_chunk_sw128<BF>(smem_u32(base + slot * C::TILE), r, c, v, scale);
       }
     };
-    if constexpr (kDV) stage_out(0, C::COL_DV, true, 1.f);
-    if constexpr (kDK1) stage_out(1, C::COL_DK, !PW || touched1, args.sm_scale);
-    if constexpr (PW && kDK2) stage_out(2, C::COL_DK2, touched2, args.sm_scale);
+    stage_out(0, C::COL_DV, true, 1.f);
+    stage_out(1, C::COL_DK, !PW || touched1, args.sm_scale);
+    if constexpr (PW) stage_out(2, C::COL_DK2, touched2, args.sm_scale);
     fence_proxy_async_smem();
     named_bar_sync(1, kRowWarps * 32);
     if (warp == 0 && lane == 0 && k0 < args.N) {
 #pragma unroll
       for (int kb = 0; kb < D / 64; ++kb) {
         const int off = kb * (kBM * 128);
-        if constexpr (kDV) tma_store_3d(&tm_dv, base + off, kb * 64, k0, bh);
-        if constexpr (kDK1) tma_store_3d(&tm_dk, base + C::TILE + off, kb * 64, k0, bh);
-        if constexpr (PW && kDK2) tma_store_3d(&tm_dk2, base + 2 * C::TILE + off, kb * 64, k0, bh);
+        tma_store_3d(&tm_dv, base + off, kb * 64, k0, bh);
+        tma_store_3d(&tm_dk, base + C::TILE + off, kb * 64, k0, bh);
+        if constexpr (PW) tma_store_3d(&tm_dk2, base + 2 * C::TILE + off, kb * 64, k0, bh);
       }
       tma_store_commit_and_wait_read();
     }
@@ -1517,10 +1514,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-template <typename T, int MODE, int D, int PART = -1>
+template <typename T, int MODE, int D>
 static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
-  using C = DkdvCfg<MODE, D, PART>;
-  auto kern = attn_bwd_dkdv_kernel<T, MODE, D, PART>;
+  using C = DkdvCfg<MODE, D>;
+  auto kern = attn_bwd_dkdv_kernel<T, MODE, D>;
   static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
@@ -1562,13 +1559,7 @@ cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& m, const 
   if (mode == kStd && D == 64) return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 64>(m, a, s) : launch_dkdv_std_t<__half, 64>(m, a, s);
   if (mode == kStd && D == 128) return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 128>(m, a, s) : launch_dkdv_std_t<__half, 128>(m, a, s);
   if (mode == kPiecewise && D == 64) return bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dkdv_t<__half, kPiecewise, 64>(m, a, s);
-  if (mode == kPiecewise && D == 128) {  // dV and dK1, then dK2
-    cudaError_t e = bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 128, 0>(m, a, s)
-                         : launch_dkdv_t<__half, kPiecewise, 128, 0>(m, a, s);
-    if (e != cudaSuccess) return e;
-    return bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 128, 1>(m, a, s)
-                : launch_dkdv_t<__half, kPiecewise, 128, 1>(m, a, s);
-  }
+  // piecewise D = 128: the one-pass kernel of bwd_pw_steps.cu (launch_bwd_pw_steps)
   return cudaErrorNotSupported;
 }
 

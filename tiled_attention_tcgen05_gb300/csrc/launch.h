@@ -21,6 +21,7 @@ struct BwdMaps {
   CUtensorMap q2, k2;       // piecewise only
   CUtensorMap dq, dk, dv;   // outputs, stored by TMA (built where not null)
   CUtensorMap dq2, dk2;     // piecewise outputs
+  CUtensorMap q64, q264, dO64;  // piecewise D = 128: Q1, Q2, dO in 64-row boxes (the one-pass key side)
 };
 
 // split: run the one-query-tile forward as two-CTA clusters that share each
@@ -41,6 +42,7 @@ uint32_t guard_take_bwd_fused(uint32_t* info);
 uint32_t guard_take_bwd_jvp(uint32_t* info);
 uint32_t guard_take_merge(uint32_t* info);
 uint32_t guard_take_fp32(uint32_t* info);
+uint32_t guard_take_bwd_pw_steps(uint32_t* info);
 #endif
 cudaError_t launch_fwd(int mode, bool bf16, int D, const FwdMaps& maps, const FwdArgs& a, bool split,
                        cudaStream_t s);
@@ -66,6 +68,11 @@ int bwd_fused_step_rows();
 cudaError_t launch_bwd_fused(bool bf16, int D, const BwdMaps& maps, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& maps, const BwdArgs& a,
                             cudaStream_t s);
+// Piecewise key side in one pass with 64-query steps (dV, dK1, dK2 of a
+// key tile; maps.q64, q264, dO64 and the output maps), for the head
+// dimensions bwd_pw_steps_supported() accepts.
+bool bwd_pw_steps_supported(int D);
+cudaError_t launch_bwd_pw_steps(bool bf16, const BwdMaps& maps, const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& maps, const BwdArgs& a, cudaStream_t s);
 
 // Backward of the JVP.  Maps of the eight [BH, S, D] 16-bit inputs with
