@@ -1,7 +1,7 @@
 """Benchmark: attention forward + backward, bf16, causal, B=1 H=32 M=N=8192 D=128.
 
 One step = one pass of the whole hot path over one batch: attn_fwd (O, L)
-then attn_bwd (delta, dK/dV, dQ) on inputs resident in HBM.  The metric is
+then attn_bwd (dQ with delta, then dK/dV) on inputs resident in HBM.  The metric is
 throughput in TFLOPS with the FLOP count 4*B*H*M*N*D for the forward, 2.5x
 that for the backward, halved for causal (the benchmark harness of "Triton
 fused attention tutorial, updated with JVP support", bench_flash_attention).
@@ -50,9 +50,9 @@ def kernel_algorithmic(name, w=WORKLOAD):
     backward's matmuls (S^T recompute, dP^T, dV, dK, dQ^T).  The two-pass
     backward's attn_bwd_dkdv: four of them (S^T recompute, dP^T, dV, dK);
     attn_bwd_dq: the dQ matmul (its S and dP recomputes are extra work, not
-    counted).  bwd_delta: bytes of O and dO read plus delta written (the
-    step's two-pass backward; attn_bwd_fused's delta pass also zeroes its
-    fp32 dQ accumulator).  bwd_dq_convert: the accumulator read, dQ
+    counted; in the two-pass backward it also forms delta from O and dO).
+    bwd_delta: bytes of O and dO read plus delta written (attn_bwd_fused's
+    delta pass, which also zeroes its fp32 dQ accumulator).  bwd_dq_convert: the accumulator read, dQ
     written."""
     f = flops_fwd(w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"])
     rows = w["B"] * w["H"] * w["M"]
@@ -332,7 +332,7 @@ def fp8_measure(ta, torch, si, dev, stream, w, bf16_peak, iters=10):
 def bwd_fused_measure(ta, torch, dev, stream, g, o, lse, w, bf16_peak, iters=10):
     """Times the two backward paths on the benchmark's shape and inputs,
     outside the step's timed region, alternating calls (L2 flushed before
-    each): attn_bwd (delta, dK/dV pass, dQ pass) and attn_bwd_fused (delta,
+    each): attn_bwd (dQ pass forming delta, dK/dV pass) and attn_bwd_fused (delta,
     one key-stationary pass with the fp32 dQ accumulator, dQ conversion).
     Both against the backward's algorithmic FLOPs (2.5x the forward)."""
     flops = 2.5 * flops_fwd(w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"])

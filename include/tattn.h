@@ -85,6 +85,9 @@ size_t attn_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype dt);
  * In: q,k,v, o and lse from attn_fwd, dO [B,H,M,D].  Out: dq [B,H,M,D],
  * dk, dv [B,H,N,D] (dt).  ws: >= attn_bwd_workspace_bytes(...) bytes of
  * device memory, 16-byte aligned, contents need not be initialised.
+ * In 16-bit types the dQ pass forms delta itself (from O and dO, while
+ * its first score products run) and stores it in ws for the dK/dV pass that
+ * follows; in fp32 a delta pass runs first.
  * Returns TA_ERR_INVALID_ARG if ws is null or too small. */
 ta_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
                    const void* dO, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B, int H,

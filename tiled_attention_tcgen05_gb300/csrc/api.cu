@@ -433,16 +433,22 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
     return cuda_status(e);
   }
   const bool use_acc = fused && !pw && !p.f32 && p.N > 0;
+  // The standard two-pass backward forms delta inside its dQ pass, which then
+  // runs before the dK/dV pass; every other path runs the delta pass first.
+  const bool dq_forms_delta = !pw && !p.f32 && !use_acc;
   const size_t db = delta_bytes(p.BH, p.M);
   if (ws_bytes < db || (use_acc && ws_bytes - db < dq_acc_bytes(p.BH, p.M, p.D))) return TA_ERR_INVALID_ARG;
   float* delta = static_cast<float*>(ws);
   float* acc = use_acc ? reinterpret_cast<float*>(static_cast<char*>(ws) + db) : nullptr;
-  prof_begin("bwd_delta", s);
-  cudaError_t e = p.f32 ? launch_f32_delta(p.D, static_cast<const float*>(o), static_cast<const float*>(dO),
-                                           delta, p.BH * p.M, s)
-                        : launch_delta(p.bf16, p.D, o, dO, delta, p.BH * p.M, s, acc);
-  prof_end(s);
-  if (e != cudaSuccess) return TA_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (!dq_forms_delta) {
+    prof_begin("bwd_delta", s);
+    e = p.f32 ? launch_f32_delta(p.D, static_cast<const float*>(o), static_cast<const float*>(dO), delta,
+                                 p.BH * p.M, s)
+              : launch_delta(p.bf16, p.D, o, dO, delta, p.BH * p.M, s, acc);
+    prof_end(s);
+    if (e != cudaSuccess) return TA_ERR_CUDA;
+  }
   const size_t q_bytes = static_cast<size_t>(p.BH) * p.M * p.D * p.esize;
   if (p.N == 0) {
     e = launch_zero(dq, q_bytes, s);
@@ -488,6 +494,19 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
     if (e != cudaSuccess) return TA_ERR_CUDA;
     prof_begin("bwd_dq_convert", s);
     e = launch_dq_convert(p.bf16, p.D, acc, dq, p.BH * p.M, p.sm_scale, s);
+    prof_end(s);
+    return cuda_status(e);
+  }
+  if (dq_forms_delta) {  // dQ and delta, then dK/dV
+    if (!make_map(&maps.o, o, p.BH, p.M, p.D, p.bf16)) return TA_ERR_CUDA;
+    a.delta_out = delta;
+    prof_begin("attn_bwd_dq", s);
+    e = launch_bwd_dq(mode, p.bf16, kernel_d(p.D), maps, a, s);
+    prof_end(s);
+    if (e != cudaSuccess) return TA_ERR_CUDA;
+    a.delta_out = nullptr;
+    prof_begin("attn_bwd_dkdv", s);
+    e = launch_bwd_dkdv(mode, p.bf16, kernel_d(p.D), maps, a, s);
     prof_end(s);
     return cuda_status(e);
   }

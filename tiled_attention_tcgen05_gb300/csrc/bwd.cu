@@ -884,19 +884,58 @@ __device__ __forceinline__ void mma_tY_g(uint32_t d_tmem, uint32_t x_tmem, uint3
 // slot joins the ring.  The softmax warps also release the S buffer as soon
 // as they have loaded S(t), so S(t + 1) is computed while they work on t:
 //   S(0) dP(0) | S(t+1) | dQ(t) dP(t+1) | ...
+// When args.delta_out is set the kernel also forms the backward preprocess
+// delta = rowsum(dO o O) of its query tile ("Triton fused attention tutorial,
+// updated with JVP support", _attn_bwd_preprocess): O arrives after the first
+// K/V tile, in a slot of its own and on a barrier of its own, and each
+// softmax group sums half of every row's columns (dO from TMEM) while the
+// first score MMAs run.  The sum is used here and written to delta_out for
+// the dK/dV pass, which then runs after this one.
 template <int D>
 struct DqStdCfg {
   static constexpr int BLK = kBM * 128;
   static constexpr int TILE = (D / 64) * BLK;
   static constexpr int STAGE = 2 * TILE;  // K, V
-  static constexpr int ST_FIT = (kSmemMax - 2048) / STAGE;
+  static constexpr int ST_FIT = (kSmemMax - 2048 - TILE) / STAGE;
   static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
-  static constexpr int SMEM = STAGES * STAGE + 1024;
+  static constexpr int OFF_O = STAGES * STAGE;  // the O tile (delta), after the ring
+  static constexpr int SMEM = OFF_O + TILE + 1024;
   static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DQ = 256;
   static constexpr uint32_t COL_QT = 256 + D, COL_DOT = 256 + D + D / 2;
   static_assert(STAGES >= 3, "K/V ring too shallow");
+  static_assert(SMEM + 2048 <= kSmemMax, "shared memory overflow");
   static_assert(COL_DOT + D / 2 <= 512, "TMEM overflow");
 };
+
+// Half of <dO_r, O_r>, the elements [half * D / 2, (half + 1) * D / 2) of row
+// r, summed in fp32: dO from the calling thread's TMEM lane (the row as
+// tile_row_to_tmem stores it, two 16-bit elements per column from column
+// a_tmem), O from its K-major 128-byte-swizzled tile in shared memory.
+template <typename T, int D>
+__device__ __forceinline__ float row_dot_half(uint32_t a_tmem, const uint8_t* b, int r, int half) {
+  constexpr int NC = D / 4;  // columns of half a row
+  uint32_t x[NC];
+  if constexpr (NC == 32) {
+    tmem_ld_x32(a_tmem + half * NC, x);
+    tmem_ld_wait(x);
+  } else {
+    static_assert(NC == 16, "D = 64 or 128");
+    tmem_ld_x16(a_tmem + half * NC, x);
+    tmem_ld_wait(x);
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int c8 = 0; c8 < D / 16; ++c8) {
+    const int gc = half * (D / 16) + c8;  // 16-byte chunk of the row
+    const uint4 y = *reinterpret_cast<const uint4*>(b + (gc >> 3) * (kBM * 128) + r * 128 + (((gc & 7) ^ (r & 7)) * 16));
+    const uint4 xv = make_uint4(x[4 * c8], x[4 * c8 + 1], x[4 * c8 + 2], x[4 * c8 + 3]);
+    const T* xp = reinterpret_cast<const T*>(&xv);
+    const T* yp = reinterpret_cast<const T*>(&y);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(static_cast<float>(xp[i]), static_cast<float>(yp[i]), acc);
+  }
+  return acc;
+}
 
 // d = A B^T over D with A (128 rows x D, 16-bit) in TMEM, 8 packed columns
 // per K-step from a_tmem, and B a 128-row x D K-major swizzled tile in smem.
@@ -918,14 +957,15 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_std_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                           const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args) {
+                           const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_o,
+                           const BwdArgs args) {
   using C = DqStdCfg<D>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
 
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q, bar_qfree, bar_kv[STAGES], bar_kvempty[STAGES];
-  __shared__ __align__(8) uint64_t bar_s, bar_consumed, bar_dp, bar_ds[2], bar_done;
+  __shared__ __align__(8) uint64_t bar_s, bar_consumed, bar_dp, bar_ds[2], bar_done, bar_o;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -937,12 +977,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int qt = num_q_tiles - 1 - rank;  // heaviest causal tiles first
   const int q0 = qt * kBM;
   const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
+  const bool make_delta = args.delta_out != nullptr;
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto sK = [&](int st) { return base + st * C::STAGE; };
   auto sV = [&](int st) { return base + st * C::STAGE + C::TILE; };
   uint8_t* sQ = sK(STAGES - 1);  // Q and dO transit through the last ring slot
   uint8_t* sDO = sV(STAGES - 1);
+  uint8_t* sO = base + C::OFF_O;
 
   WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
   if (threadIdx.x == 0) {
@@ -959,6 +1001,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_ds[0], kRowWarps);
     mbar_init(&bar_ds[1], kRowWarps);
     mbar_init(&bar_done, 1);
+    mbar_init(&bar_o, 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -977,6 +1020,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       load_tile_b<D>(sQ, &tm_q, &bar_q, q0, bh);
       load_tile_b<D>(sDO, &tm_do, &bar_q, q0, bh);
       int issued = 0;
+      bool o_issued = false;
       for (int t = 0; t < nkv; ++t) {
         const int st = t % STAGES;
         if (t >= STAGES) {
@@ -988,10 +1032,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         load_tile_b<D>(sK(st), &tm_k, &bar_kv[st], t * kBN, bh);
         load_tile_b<D>(sV(st), &tm_v, &bar_kv[st], t * kBN, bh);
         issued = t + 1;
+        if (t == 0 && make_delta) {  // O for delta, behind the first K/V tile
+          mbar_expect_tx(&bar_o, C::TILE);
+          load_tile_b<D>(sO, &tm_o, &bar_o, q0, bh);
+          o_issued = true;
+        }
       }
       int zero = 0;
       WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
       mbar_wait(&bar_q, 0, drain, kErrTimeoutTma);
+      if (o_issued) mbar_wait(&bar_o, 0, drain, kErrTimeoutTma);
       for (int t = issued - STAGES > 0 ? issued - STAGES : 0; t < issued; ++t)
         mbar_wait(&bar_kv[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
     }
@@ -1044,7 +1094,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool in_m = row < args.M;
     const size_t g = static_cast<size_t>(bh) * args.M + (in_m ? row : 0);
     const float neg_L2 = in_m ? -args.lse[g] * kLog2e : -INFINITY;
-    const float dlt = in_m ? args.delta[g] : 0.f;
+    float dlt = (in_m && !make_delta) ? args.delta[g] : 0.f;
     bool ok = true;
     if (nkv > 0) {  // group 0 copies Q, group 1 copies dO into TMEM
       ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma);
@@ -1055,6 +1105,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_qfree);
       }
+    }
+    if (make_delta) {
+      // This group's half of delta while S(0) and dP(0) are computed: dO is
+      // in TMEM once all eight warps have arrived on bar_qfree.  Rows past M
+      // and columns past the stored D read as zeros; a tile that sees no key
+      // has O = 0 and keeps delta = 0.
+      float half = 0.f;
+      if (nkv > 0 && ok) {
+        ok = warp_wait(&bar_qfree, 0, ctl, kErrTimeoutSoftmax) && warp_wait(&bar_o, 0, ctl, kErrTimeoutTma);
+        if (ok) {
+          tc_fence_after();
+          half = row_dot_half<T, D>(lane_addr + C::COL_DOT, sO, r, hc);
+        }
+      }
+      // the groups swap halves through the O tile once both have read it
+      float* halves = reinterpret_cast<float*>(sO);
+      named_bar_sync(1, kRowWarps * 32);
+      halves[hc * kBM + r] = half;
+      named_bar_sync(1, kRowWarps * 32);
+      dlt = halves[r] + halves[kBM + r];
+      if (hc == 0 && in_m) args.delta_out[g] = dlt;
     }
     for (int t = 0; ok && t < nkv; ++t) {
       const int k0 = t * kBN;
@@ -1572,7 +1643,8 @@ static cudaError_t launch_dq_std_t(const BwdMaps& m, const BwdArgs& a, cudaStrea
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.dq, a);
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.dq,
+                                                                    a.delta_out ? m.o : m.q, a);
   return cudaGetLastError();
 }
 

@@ -59,6 +59,7 @@ struct BwdArgs {
   float sm_scale;
   int dg;  // head dimension of the tensors in memory (row stride, columns stored)
   float* dq_acc;  // fused backward: fp32 dQ accumulator [BH, M, D] (zeroed by the delta pass)
+  float* delta_out;  // standard dQ pass: form delta = rowsum(dO o O) from O and store it here
   uint32_t* err;
   uint64_t timeout_ns;
 };

@@ -22,6 +22,7 @@ struct BwdMaps {
   CUtensorMap dq, dk, dv;   // outputs, stored by TMA (built where not null)
   CUtensorMap dq2, dk2;     // piecewise outputs
   CUtensorMap q64, q264, dO64;  // piecewise D = 128: Q1, Q2, dO in 64-row boxes (the one-pass key side)
+  CUtensorMap o;                // standard dQ pass forming delta (BwdArgs::delta_out)
 };
 
 // split: run the one-query-tile forward as two-CTA clusters that share each
