@@ -392,7 +392,8 @@ def jvp_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
     (attn_bwd_jvp) on the JVP workload's shape, [2, 8, 1024, 64] fp16, causal
     and not, outside the step's timed region, by the library's per-launch
     events; L2 is flushed before each timed call (the inputs, 2 MB a tensor,
-    fit in it).  Algorithmic FLOPs: the JVP
+    fit in it).  Also on a long key range ([1, 4, 1024 x 8192], where the key
+    split pays) and on [1, 32, 4096, 64], which fills the GPU.  Algorithmic FLOPs: the JVP
     forward is 3x the primal forward (6 matmul-equivalents of 2 M N D), the
     backward of the JVP 15 matmul-equivalents (S, T, dtO V^T, dO V^T + dtO tV^T
     and the nine gradient products), i.e. 7.5x the primal forward."""
@@ -443,6 +444,27 @@ def jvp_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
     out["long_keys"] = {"shape": "B1 H4 M=1024 N=8192 D64 fp16, non-causal (32 query tiles of 64 key tiles)",
                         "fwd_kv_split": ta.fwd_kv_split("attn_fwd_jvp", Bl, Hl, Ml, Nl, D, torch.float16, False),
                         "fwd_ms": res["auto"], "fwd_ms_unsplit": res["never"], "fwd_ms_split": res["always"]}
+    # a shape that fills the GPU several times over: 1024 query tiles
+    Bw, Hw, Mw = 1, 32, 4096
+    gw = {n: t.to(dev) for n, t in si.attention_inputs(Bw, Hw, Mw, Mw, D, "f16", 4, names=names).items()}
+    wide = {"shape": "B1 H32 M=N=4096 D64 fp16"}
+    for causal in (False, True):
+        fwd = lambda: ta.attn_fwd_jvp(*(gw[n] for n in names[:6]), causal=causal, with_tlse=True, stream=stream)
+        o, lse, to, tlse = fwd()
+        ws = torch.empty(max(16, ta.load().attn_bwd_jvp_workspace_bytes(Bw, Hw, Mw, Mw, D, 0)), device=dev,
+                         dtype=torch.uint8)
+        bwd = lambda: ta.attn_bwd_jvp(*(gw[n] for n in names[:6]), o, lse, to, tlse, gw["do"], gw["dto"],
+                                      causal=causal, ws=ws, stream=stream)
+        fwd()
+        bwd()
+        f = flops_fwd(Bw, Hw, Mw, Mw, D, causal)
+        tf = timed_calls(ta, torch, dev, stream, flush, fwd, iters)[0]
+        tb = timed_calls(ta, torch, dev, stream, flush, bwd, iters)[0]
+        wide["causal" if causal else "noncausal"] = {
+            "fwd_ms": tf, "bwd_ms": tb, "fwd_tflops": 3 * f / (tf * 1e-3) / 1e12,
+            "bwd_tflops": 7.5 * f / (tb * 1e-3) / 1e12, "fwd_frac": 3 * f / (tf * 1e-3) / 1e12 / bf16_peak,
+            "bwd_frac": 7.5 * f / (tb * 1e-3) / 1e12 / bf16_peak}
+    out["wide"] = wide
     return out
 
 
@@ -450,14 +472,21 @@ def configs_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
     """Times one fwd+bwd step (forward then backward, inputs resident) on the
     other workloads: 1 (B1 H2 S128 D64 fp16, non-causal), 2 (B4 H16 S2048 D128
     bf16 causal) and 5 (piecewise, B2 H16 S4096 D64 bf16 causal, w = 512),
-    as the device time of the step's kernels (timed_calls).  L2 is flushed
+    and workload 5's shape at D = 128 (piecewise) and at D = 64 and 128 as
+    standard attention, for comparison, as the device time of the step's
+    kernels (timed_calls).  L2 is flushed
     before each timed step.  FLOPs are the standard count
     (4 M N D per head forward, x 3.5 for forward + backward, x 0.5 causal); the
     piecewise path's second score products on straddling tiles are overhead."""
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     out = {}
-    for wid in (1, 2, 5):
-        w = si.WORKLOADS[wid]
+    w5 = si.WORKLOADS[5]
+    cases = [(str(wid), wid, si.WORKLOADS[wid]) for wid in (1, 2, 5)]
+    cases.append(("5_d128", 5, dict(w5, D=128, name="piecewise fwd+bwd bf16 causal B2 H16 S4096 D128 w512")))
+    for d in (64, 128):
+        cases.append((f"5_std_d{d}", 5, dict(w5, D=d, mode="fwdbwd", w=None,
+                                             name=f"fwd+bwd bf16 causal B2 H16 S4096 D{d} (standard)")))
+    for key, wid, w in cases:
         B, H, M, N, D, causal = w["B"], w["H"], w["M"], w["N"], w["D"], w["causal"]
         pw = w["mode"] == "piecewise"
         names = ("q1", "k1", "q2", "k2", "v", "do") if pw else ("q", "k", "v", "do")
@@ -477,8 +506,8 @@ def configs_measure(ta, torch, si, dev, stream, bf16_peak, iters=20):
         ms, call_ms = timed_calls(ta, torch, dev, stream, flush, fn, iters)
         f = flops_fwd(B, H, M, N, D, causal) * 3.5
         tf = f / (ms * 1e-3) / 1e12
-        out[str(wid)] = {"workload": w["name"], "ms_per_step": ms, "tflops": tf, "frac": tf / bf16_peak,
-                         "call_ms_per_step": call_ms}
+        out[key] = {"workload": w["name"], "ms_per_step": ms, "tflops": tf, "frac": tf / bf16_peak,
+                    "call_ms_per_step": call_ms}
     return out
 
 

@@ -198,7 +198,8 @@ size_t piecewise_bwd_workspace_bytes(int B, int H, int M, int N, int D, ta_dtype
  * Out: dq1, dq2 [B,H,M,D], dk1, dk2, dv [B,H,N,D] (dt).
  * At D = 128 in 16-bit the key-stationary pass streams the queries in
  * 64-row steps, so that tensor memory holds all three accumulators of a
- * 128-key tile beside its score buffers and one pass forms dv, dk1, dk2. */
+ * 128-key tile beside its score buffers and one pass forms dv, dk1, dk2.
+ * In 16-bit types the dQ pass runs first and forms delta, as in attn_bwd. */
 ta_status piecewise_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
                         const void* o, const float* lse, const void* dO, void* dq1, void* dk1, void* dq2,
                         void* dk2, void* dv, void* ws, size_t ws_bytes, int B, int H, int M, int N, int D,

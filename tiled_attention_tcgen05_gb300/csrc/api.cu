@@ -433,9 +433,10 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
     return cuda_status(e);
   }
   const bool use_acc = fused && !pw && !p.f32 && p.N > 0;
-  // The standard two-pass backward forms delta inside its dQ pass, which then
-  // runs before the dK/dV pass; every other path runs the delta pass first.
-  const bool dq_forms_delta = !pw && !p.f32 && !use_acc;
+  // The 16-bit two-pass backward (standard and piecewise) forms delta inside
+  // its dQ pass, which then runs before the key side; the fp32 mode and the
+  // fused backward run the delta pass first.
+  const bool dq_forms_delta = !p.f32 && !use_acc;
   const size_t db = delta_bytes(p.BH, p.M);
   if (ws_bytes < db || (use_acc && ws_bytes - db < dq_acc_bytes(p.BH, p.M, p.D))) return TA_ERR_INVALID_ARG;
   float* delta = static_cast<float*>(ws);
@@ -497,19 +498,15 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
     prof_end(s);
     return cuda_status(e);
   }
-  if (dq_forms_delta) {  // dQ and delta, then dK/dV
-    if (!make_map(&maps.o, o, p.BH, p.M, p.D, p.bf16)) return TA_ERR_CUDA;
-    a.delta_out = delta;
-    prof_begin("attn_bwd_dq", s);
-    e = launch_bwd_dq(mode, p.bf16, kernel_d(p.D), maps, a, s);
-    prof_end(s);
-    if (e != cudaSuccess) return TA_ERR_CUDA;
-    a.delta_out = nullptr;
-    prof_begin("attn_bwd_dkdv", s);
-    e = launch_bwd_dkdv(mode, p.bf16, kernel_d(p.D), maps, a, s);
-    prof_end(s);
-    return cuda_status(e);
-  }
+  // dQ, forming delta (dq_forms_delta holds on every path that reaches here),
+  // then the key side, which reads delta
+  if (!make_map(&maps.o, o, p.BH, p.M, p.D, p.bf16)) return TA_ERR_CUDA;
+  a.delta_out = delta;
+  prof_begin(pw ? "piecewise_bwd_dq" : "attn_bwd_dq", s);
+  e = launch_bwd_dq(mode, p.bf16, kernel_d(p.D), maps, a, s);
+  prof_end(s);
+  if (e != cudaSuccess) return TA_ERR_CUDA;
+  a.delta_out = nullptr;
   prof_begin(pw ? "piecewise_bwd_dkdv" : "attn_bwd_dkdv", s);
   if (pw && bwd_pw_steps_supported(kernel_d(p.D))) {  // the key side in one pass, 64-query steps
     if (!make_map(&maps.q64, q, p.BH, p.M, p.D, p.bf16, 64) || !make_map(&maps.q264, q2, p.BH, p.M, p.D, p.bf16, 64) ||
@@ -521,10 +518,6 @@ static ta_status run_bwd(int mode, const Problem& p, const void* q, const void* 
   } else {
     e = launch_bwd_dkdv(mode, p.bf16, kernel_d(p.D), maps, a, s);
   }
-  prof_end(s);
-  if (e != cudaSuccess) return TA_ERR_CUDA;
-  prof_begin(pw ? "piecewise_bwd_dq" : "attn_bwd_dq", s);
-  e = launch_bwd_dq(mode, p.bf16, kernel_d(p.D), maps, a, s);
   prof_end(s);
   return cuda_status(e);
 }

@@ -503,6 +503,70 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // ======================================================================
 //                         dQ (query-stationary)
 // ======================================================================
+// Half of <dO_r, O_r>, the elements [half * D / 2, (half + 1) * D / 2) of row
+// r, summed in fp32: dO from the calling thread's TMEM lane (the row as
+// tile_row_to_tmem stores it, two 16-bit elements per column from column
+// a_tmem), O from its K-major 128-byte-swizzled tile in shared memory.
+template <typename T, int D>
+__device__ __forceinline__ float row_dot_half_tmem(uint32_t a_tmem, const uint8_t* b, int r, int half) {
+  constexpr int NC = D / 4;  // columns of half a row
+  uint32_t x[NC];
+  if constexpr (NC == 32) {
+    tmem_ld_x32(a_tmem + half * NC, x);
+    tmem_ld_wait(x);
+  } else {
+    static_assert(NC == 16, "D = 64 or 128");
+    tmem_ld_x16(a_tmem + half * NC, x);
+    tmem_ld_wait(x);
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int c8 = 0; c8 < D / 16; ++c8) {
+    const int gc = half * (D / 16) + c8;  // 16-byte chunk of the row
+    const uint4 y = *reinterpret_cast<const uint4*>(b + (gc >> 3) * (kBM * 128) + r * 128 + (((gc & 7) ^ (r & 7)) * 16));
+    const uint4 xv = make_uint4(x[4 * c8], x[4 * c8 + 1], x[4 * c8 + 2], x[4 * c8 + 3]);
+    const T* xp = reinterpret_cast<const T*>(&xv);
+    const T* yp = reinterpret_cast<const T*>(&y);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(static_cast<float>(xp[i]), static_cast<float>(yp[i]), acc);
+  }
+  return acc;
+}
+
+// d = A B^T over D with A (128 rows x D, 16-bit) in TMEM, 8 packed columns
+// per K-step from a_tmem, and B a 128-row x D K-major swizzled tile in smem.
+template <int D>
+__device__ __forceinline__ void mma_tB(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc) {
+  const uint64_t db0 = sdesc_sw128(b_smem, 16, 1024);
+  uint32_t a[D / 16];
+  uint64_t b[D / 16];
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    a[kk] = a_tmem + kk * 8;
+    b[kk] = db0 + static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
+  }
+  mma_ts_n<D / 16>(d_tmem, a, b, idesc, 0u);
+}
+
+
+// The same with dO from its K-major 128-byte-swizzled tile in shared memory.
+template <typename T, int D>
+__device__ __forceinline__ float row_dot_half_smem(const uint8_t* a, const uint8_t* b, int r, int half) {
+  float acc = 0.f;
+#pragma unroll
+  for (int c8 = 0; c8 < D / 16; ++c8) {
+    const int gc = half * (D / 16) + c8;  // 16-byte chunk of the row
+    const int off = (gc >> 3) * (kBM * 128) + r * 128 + (((gc & 7) ^ (r & 7)) * 16);
+    const uint4 x = *reinterpret_cast<const uint4*>(a + off);
+    const uint4 y = *reinterpret_cast<const uint4*>(b + off);
+    const T* xp = reinterpret_cast<const T*>(&x);
+    const T* yp = reinterpret_cast<const T*>(&y);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc = fmaf(static_cast<float>(xp[i]), static_cast<float>(yp[i]), acc);
+  }
+  return acc;
+}
+
 template <int MODE, int D>
 struct DqCfg {
   static constexpr int BLK = kBM * 128;
@@ -511,15 +575,17 @@ struct DqCfg {
   static constexpr int NKT = (MODE == kStd) ? 2 : 3;   // K, V | K1, K2, V
   static constexpr int STAGE = NKT * TILE;
   static constexpr int RESERVE = 2048;
-  static constexpr int ST_FIT = (kSmemMax - RESERVE - NRES * TILE) / STAGE;
+  static constexpr int ST_FIT = (kSmemMax - RESERVE - (NRES + 1) * TILE) / STAGE;
   static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
-  static constexpr int SMEM = NRES * TILE + STAGES * STAGE + 1024;
+  static constexpr int OFF_O = NRES * TILE + STAGES * STAGE;  // the O tile (delta), after the ring
+  static constexpr int SMEM = OFF_O + TILE + 1024;
   static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DQ = 256, COL_DQ2 = 256 + D;
   // Piecewise with room for a second 128-column S buffer (D = 64) and two
   // K/V stages: the next tile's S is computed while this tile's dS is formed.
   static constexpr bool DBUF = (MODE == kPiecewise) && (256 + 2 * D + 128 <= 512) && STAGES >= 2;
   static constexpr uint32_t COL_C = 256 + 2 * D;
   static_assert(STAGES >= 1, "tile does not fit in shared memory");
+  static_assert(SMEM + RESERVE <= kSmemMax, "shared memory overflow");
   static_assert(COL_DQ2 + (MODE == kPiecewise ? D : 0) <= 512, "TMEM overflow");
 };
 
@@ -529,7 +595,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
                        const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dq2,
-                       const BwdArgs args) {
+                       const __grid_constant__ CUtensorMap tm_o, const BwdArgs args) {
   using C = DqCfg<MODE, D>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
@@ -539,6 +605,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ __align__(8) uint64_t bar_q, bar_kv[STAGES], bar_kvempty[STAGES];
   __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_consumed, bar_ds, bar_done;
   __shared__ __align__(8) uint64_t bar_sb[2];  // DBUF: S of even / odd tiles ready
+  __shared__ __align__(8) uint64_t bar_o;      // delta: the O tile landed
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   // DBUF: tile t's S buffer
@@ -552,12 +619,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int qt = num_q_tiles - 1 - rank;  // heaviest causal tiles first
   const int q0 = qt * kBM;
   const int nkv = kv_tiles_for(q0, args.M, args.N, args.P_SEQ, args.causal);
+  const bool make_delta = args.delta_out != nullptr;
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = base;
   uint8_t* sQ2 = base + C::TILE;
   uint8_t* sDO = base + (C::NRES - 1) * C::TILE;
   uint8_t* sStages = base + C::NRES * C::TILE;
+  uint8_t* sO = base + C::OFF_O;
   auto sK = [&](int st) { return sStages + st * C::STAGE; };
   auto sK2 = [&](int st) { return sStages + st * C::STAGE + C::TILE; };
   auto sV = [&](int st) { return sStages + st * C::STAGE + (C::NKT - 1) * C::TILE; };
@@ -577,6 +646,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&bar_consumed, kRowWarps);
     mbar_init(&bar_ds, kRowWarps);
     mbar_init(&bar_done, 1);
+    mbar_init(&bar_o, 1);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -591,6 +661,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && nkv > 0) {
+      bool o_issued = false;
       mbar_expect_tx(&bar_q, C::NRES * C::TILE);
       load_tile_b<D>(sQ, &tm_q, &bar_q, q0, bh);
       if constexpr (PW) load_tile_b<D>(sQ2, &tm_q2, &bar_q, q0, bh);
@@ -608,10 +679,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (cls & kFarB) load_tile_b<D>(sK2(st), &tm_k2, &bar_kv[st], k0, bh);
         load_tile_b<D>(sV(st), &tm_v, &bar_kv[st], k0, bh);
         issued = t + 1;
+        if (t == 0 && make_delta) {  // O for delta, behind the first K/V tile
+          mbar_expect_tx(&bar_o, C::TILE);
+          load_tile_b<D>(sO, &tm_o, &bar_o, q0, bh);
+          o_issued = true;
+        }
       }
       int zero = 0;
       WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
       mbar_wait(&bar_q, 0, drain, kErrTimeoutTma);
+      if (o_issued) mbar_wait(&bar_o, 0, drain, kErrTimeoutTma);
       for (int t = issued - STAGES > 0 ? issued - STAGES : 0; t < issued; ++t)
         mbar_wait(&bar_kv[t % STAGES], (t / STAGES) & 1, drain, kErrTimeoutTma);
     }
@@ -728,10 +805,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool in_m = row < args.M;
     const size_t g = static_cast<size_t>(bh) * args.M + (in_m ? row : 0);
     const float neg_L2 = in_m ? -args.lse[g] * kLog2e : -INFINITY;
-    const float dlt = in_m ? args.delta[g] : 0.f;
+    float dlt = (in_m && !make_delta) ? args.delta[g] : 0.f;
     bool ok = true;
+    if (make_delta) {
+      // delta of this tile's rows, each softmax group summing half of every
+      // row from the resident dO tile and the O tile, while S(0) and dP(0)
+      // are computed.  Rows past M and columns past the stored D read as
+      // zeros; a tile that sees no key has O = 0 and keeps delta = 0.
+      const int r = threadIdx.x & 127;
+      float half = 0.f;
+      if (nkv > 0) {
+        ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma) && warp_wait(&bar_o, 0, ctl, kErrTimeoutTma);
+        if (ok) half = row_dot_half_smem<T, D>(sDO, sO, r, hc);
+      }
+      // the groups swap halves through the O tile once both have read it
+      float* halves = reinterpret_cast<float*>(sO);
+      named_bar_sync(1, kRowWarps * 32);
+      halves[hc * kBM + r] = half;
+      named_bar_sync(1, kRowWarps * 32);
+      dlt = halves[r] + halves[kBM + r];
+      if (hc == 0 && in_m) args.delta_out[g] = dlt;
+    }
     bool touched1 = false, touched2 = false;
-    for (int t = 0; t < nkv; ++t) {
+    for (int t = 0; ok && t < nkv; ++t) {
       const int k0 = t * kBN;
       if constexpr (C::DBUF) {
         if (!(ok = warp_wait(&bar_sb[t & 1], (t >> 1) & 1, ctl, kErrTimeoutMma))) break;
@@ -907,52 +1003,6 @@ struct DqStdCfg {
   static_assert(COL_DOT + D / 2 <= 512, "TMEM overflow");
 };
 
-// Half of <dO_r, O_r>, the elements [half * D / 2, (half + 1) * D / 2) of row
-// r, summed in fp32: dO from the calling thread's TMEM lane (the row as
-// tile_row_to_tmem stores it, two 16-bit elements per column from column
-// a_tmem), O from its K-major 128-byte-swizzled tile in shared memory.
-template <typename T, int D>
-__device__ __forceinline__ float row_dot_half(uint32_t a_tmem, const uint8_t* b, int r, int half) {
-  constexpr int NC = D / 4;  // columns of half a row
-  uint32_t x[NC];
-  if constexpr (NC == 32) {
-    tmem_ld_x32(a_tmem + half * NC, x);
-    tmem_ld_wait(x);
-  } else {
-    static_assert(NC == 16, "D = 64 or 128");
-    tmem_ld_x16(a_tmem + half * NC, x);
-    tmem_ld_wait(x);
-  }
-  float acc = 0.f;
-#pragma unroll
-  for (int c8 = 0; c8 < D / 16; ++c8) {
-    const int gc = half * (D / 16) + c8;  // 16-byte chunk of the row
-    const uint4 y = *reinterpret_cast<const uint4*>(b + (gc >> 3) * (kBM * 128) + r * 128 + (((gc & 7) ^ (r & 7)) * 16));
-    const uint4 xv = make_uint4(x[4 * c8], x[4 * c8 + 1], x[4 * c8 + 2], x[4 * c8 + 3]);
-    const T* xp = reinterpret_cast<const T*>(&xv);
-    const T* yp = reinterpret_cast<const T*>(&y);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc = fmaf(static_cast<float>(xp[i]), static_cast<float>(yp[i]), acc);
-  }
-  return acc;
-}
-
-// d = A B^T over D with A (128 rows x D, 16-bit) in TMEM, 8 packed columns
-// per K-step from a_tmem, and B a 128-row x D K-major swizzled tile in smem.
-template <int D>
-__device__ __forceinline__ void mma_tB(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem, uint32_t idesc) {
-  const uint64_t db0 = sdesc_sw128(b_smem, 16, 1024);
-  uint32_t a[D / 16];
-  uint64_t b[D / 16];
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    a[kk] = a_tmem + kk * 8;
-    b[kk] = db0 + static_cast<uint64_t>(((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4);
-  }
-  mma_ts_n<D / 16>(d_tmem, a, b, idesc, 0u);
-}
-
-
 template <typename T, int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_std_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1116,7 +1166,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = warp_wait(&bar_qfree, 0, ctl, kErrTimeoutSoftmax) && warp_wait(&bar_o, 0, ctl, kErrTimeoutTma);
         if (ok) {
           tc_fence_after();
-          half = row_dot_half<T, D>(lane_addr + C::COL_DOT, sO, r, hc);
+          half = row_dot_half_tmem<T, D>(lane_addr + C::COL_DOT, sO, r, hc);
         }
       }
       // the groups swap halves through the O tile once both have read it
@@ -1609,7 +1659,7 @@ static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t 
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, m.dq, m.dq2,
-                                                                    a);
+                                                                    a.delta_out ? m.o : m.q, a);
   return cudaGetLastError();
 }
 
