@@ -970,16 +970,16 @@ __device__ __forceinline__ void fwd2_body(const CUtensorMap& tm_q, const CUtenso
       const float2 nm2 = make_float2(neg_m, neg_m);
       float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+      for (int c = 0; c < 8; ++c) {  // 16 columns of S, 8 packed columns of P, at a time
+        uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 y = ffma2(make_float2(x[32 * c + 2 * e], x[32 * c + 2 * e + 1]), sc2, nm2);
+        for (int e = 0; e < 8; ++e) {
+          const float2 y = ffma2(make_float2(x[16 * c + 2 * e], x[16 * c + 2 * e + 1]), sc2, nm2);
           const float2 pr = make_float2(ex2(y.x), ex2(y.y));
           rs2[e & 3] = fadd2(rs2[e & 3], pr);
           pk[e] = pack2<BF>(pr.x, pr.y);
         }
-        tmem_st_x16(lane_addr + col_s[w] + 16 * c, pk);
+        tmem_st_x8(lane_addr + col_s[w] + 8 * c, pk);
       }
       const float2 rsa = fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3]));
       const float rs = rsa.x + rsa.y;
