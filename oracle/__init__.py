@@ -70,6 +70,7 @@ __all__ = [
     "attention_jvp_bhsd", "piecewise_fwd_bhsd", "piecewise_bwd_bhsd", "default_scale",
     "lse_merge_fwd", "lse_merge_bwd", "lse_merge_fwd_bhsd", "lse_merge_bwd_bhsd",
     "attention_jvp_tl", "attention_jvp_tl_bhsd", "attention_jvp_bwd", "attention_jvp_bwd_bhsd",
+    "bwd_delta", "bwd_delta_bhsd",
 ]
 
 
@@ -137,6 +138,14 @@ def attention_bwd(q, k, v, do, causal: bool, sm_scale=None):
     dq = s * (dS @ k)
     dk = s * (dS.T @ q)
     return dq, dk, dv
+
+
+def bwd_delta(o, do):
+    """One head: the backward preprocess delta_i = sum_d dO_id O_id from a
+    given (stored) O [M,D] and dO [M,D] -- tutorial ``_attn_bwd_preprocess``,
+    piecewise ``_bwd_preprocess``."""
+    o, do = _f64(o, do)
+    return (do * o).sum(axis=1)
 
 
 def attention_jvp(q, k, v, tq, tk, tv, causal: bool, sm_scale=None):
@@ -321,6 +330,11 @@ def attention_fwd_bhsd(q, k, v, causal, sm_scale=None, heads=None):
 
 def attention_bwd_bhsd(q, k, v, do, causal, sm_scale=None, heads=None):
     return _run_bhsd(attention_bwd, (q, k, v, do), (causal, sm_scale), heads, 3)
+
+
+def bwd_delta_bhsd(o, do, heads=None):
+    """[B,H,M,D] O and dO -> delta [B,H,M]."""
+    return _run_bhsd(lambda a, b: (bwd_delta(a, b),), (o, do), (), heads, 1)[0]
 
 
 def attention_jvp_bhsd(q, k, v, tq, tk, tv, causal, sm_scale=None, heads=None):

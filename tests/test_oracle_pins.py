@@ -255,6 +255,22 @@ def test_sum_of_dk_over_keys_is_zero(causal):
     np.testing.assert_allclose(dk.sum(axis=0), 0.0, atol=1e-13)
 
 
+@pytest.mark.parametrize("M,N,causal", [(5, 7, False), (6, 6, True), (7, 4, True)])
+def test_delta_is_the_row_sum_of_p_times_dp(M, N, causal):
+    """delta_i = <dO_i, O_i> equals sum_j P_ij dP_ij with dP = dO V^T, P taken
+    by the brute-force loops (V = identity makes the loop's output P itself);
+    rows that see no key have O = 0 and delta = 0."""
+    D = 3
+    q, k, v, do = rand(M, D), rand(N, D), rand(N, D), rand(M, D)
+    P, _ = brute_fwd(q, k, np.eye(N), causal, 0.7)
+    O = P @ v
+    want = [sum(P[i, j] * sum(do[i, d] * v[j, d] for d in range(D)) for j in range(N)) for i in range(M)]
+    np.testing.assert_allclose(oracle.bwd_delta(O, do), want, atol=1e-12)
+    got = oracle.bwd_delta_bhsd(O[None, None], do[None, None])
+    assert got.shape == (1, 1, M)
+    np.testing.assert_allclose(got[0, 0], want, atol=1e-12)
+
+
 # --------------------------------------------- piecewise special cases
 def test_piecewise_all_far_or_all_near_reduces_to_attention():
     M, N, D = 6, 6, 4
