@@ -987,29 +987,42 @@ __device__ __forceinline__ void mma_tY_g(uint32_t d_tmem, uint32_t x_tmem, uint3
 // softmax group sums half of every row's columns (dO from TMEM) while the
 // first score MMAs run.  The sum is used here and written to delta_out for
 // the dK/dV pass, which then runs after this one.
-template <int D>
+//
+// Piecewise mode (PW, D = 64: TMEM has room for Q2 and dQ2 beside the rest):
+// Q1, Q2 and dO are the resident A operands and each ring slot holds K1, K2
+// and V, of which a key tile loads the K its class needs.  A tile whose keys
+// straddle the distance w gets both score products in turn in the S buffer:
+// S(q1, k1), read by the softmax warps, then S(q2, k2), merged by distance
+// ("FlagAttention piecewise.py", _bwd_q_kernel).  Its dS goes to dQ1 through
+// the near part and to dQ2 through the far part, which the softmax warps
+// write beside the near part in the columns dP has vacated.
+template <int D, bool PW = false>
 struct DqStdCfg {
   static constexpr int BLK = kBM * 128;
   static constexpr int TILE = (D / 64) * BLK;
-  static constexpr int STAGE = 2 * TILE;  // K, V
+  static constexpr int NKT = PW ? 3 : 2;  // K, V | K1, K2, V
+  static constexpr int STAGE = NKT * TILE;
   static constexpr int ST_FIT = (kSmemMax - 2048 - TILE) / STAGE;
   static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
   static constexpr int OFF_O = STAGES * STAGE;  // the O tile (delta), after the ring
   static constexpr int SMEM = OFF_O + TILE + 1024;
   static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DQ = 256;
   static constexpr uint32_t COL_QT = 256 + D, COL_DOT = 256 + D + D / 2;
+  static constexpr uint32_t COL_DQ2 = 256 + 2 * D, COL_Q2T = 256 + 3 * D;  // piecewise
+  static_assert(!PW || D == 64, "piecewise mode at D = 64 only");
   static_assert(STAGES >= 3, "K/V ring too shallow");
   static_assert(SMEM + 2048 <= kSmemMax, "shared memory overflow");
-  static_assert(COL_DOT + D / 2 <= 512, "TMEM overflow");
+  static_assert(COL_DOT + D / 2 <= 512 && (!PW || COL_Q2T + D / 2 <= 512), "TMEM overflow");
 };
 
-template <typename T, int D>
+template <typename T, int D, bool PW>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dq_std_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                            const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_o,
-                           const BwdArgs args) {
-  using C = DqStdCfg<D>;
+                           const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
+                           const __grid_constant__ CUtensorMap tm_dq2, const BwdArgs args) {
+  using C = DqStdCfg<D, PW>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int STAGES = C::STAGES;
 
@@ -1031,10 +1044,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   auto sK = [&](int st) { return base + st * C::STAGE; };
-  auto sV = [&](int st) { return base + st * C::STAGE + C::TILE; };
-  uint8_t* sQ = sK(STAGES - 1);  // Q and dO transit through the last ring slot
+  auto sK2 = [&](int st) { return base + st * C::STAGE + C::TILE; };  // piecewise
+  auto sV = [&](int st) { return base + st * C::STAGE + (C::NKT - 1) * C::TILE; };
+  uint8_t* sQ = sK(STAGES - 1);  // Q (Q1, Q2) and dO transit through the last ring slot
+  uint8_t* sQ2 = sK2(STAGES - 1);
   uint8_t* sDO = sV(STAGES - 1);
   uint8_t* sO = base + C::OFF_O;
+  // piecewise: which score products key tile t needs (kNearB | kFarB bits)
+  auto cls_of = [&](int t) { return PW ? pw_class_b(q0, t * kBN, args.P_SEQ, args.w) : kNearB; };
 
   WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
   if (threadIdx.x == 0) {
@@ -1066,8 +1083,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && nkv > 0) {
-      mbar_expect_tx(&bar_q, 2 * C::TILE);
+      mbar_expect_tx(&bar_q, (PW ? 3 : 2) * C::TILE);
       load_tile_b<D>(sQ, &tm_q, &bar_q, q0, bh);
+      if constexpr (PW) load_tile_b<D>(sQ2, &tm_q2, &bar_q, q0, bh);
       load_tile_b<D>(sDO, &tm_do, &bar_q, q0, bh);
       int issued = 0;
       bool o_issued = false;
@@ -1078,8 +1096,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         } else if (st == STAGES - 1) {  // the slot still holds Q and dO until they are in TMEM
           if (!mbar_wait(&bar_qfree, 0, ctl, kErrTimeoutSoftmax)) break;
         }
-        mbar_expect_tx(&bar_kv[st], 2 * C::TILE);
-        load_tile_b<D>(sK(st), &tm_k, &bar_kv[st], t * kBN, bh);
+        const int cls = cls_of(t);
+        mbar_expect_tx(&bar_kv[st], (((cls & kNearB) ? 1 : 0) + ((cls & kFarB) ? 1 : 0) + 1) * C::TILE);
+        if (cls & kNearB) load_tile_b<D>(sK(st), &tm_k, &bar_kv[st], t * kBN, bh);
+        if (PW && (cls & kFarB)) load_tile_b<D>(sK2(st), &tm_k2, &bar_kv[st], t * kBN, bh);
         load_tile_b<D>(sV(st), &tm_v, &bar_kv[st], t * kBN, bh);
         issued = t + 1;
         if (t == 0 && make_delta) {  // O for delta, behind the first K/V tile
@@ -1100,11 +1120,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (nkv > 0) {
       constexpr uint32_t idesc_s = idesc_f16(kBM, kBN, BF, false, false);
       constexpr uint32_t idesc_g = idesc_f16(kBM, D, BF, false, true);
+      // the first (or only) score product of key tile t: S = Q K^T (piecewise:
+      // S(q1, k1) if any of the tile is near, else S(q2, k2))
+      auto issue_s = [&](int t, int st) {
+        if (!PW || (cls_of(t) & kNearB)) {
+          mma_tB<D>(tmem + C::COL_A, tmem + C::COL_QT, smem_u32(sK(st)), idesc_s);
+        } else if constexpr (PW) {
+          mma_tB<D>(tmem + C::COL_A, tmem + C::COL_Q2T, smem_u32(sK2(st)), idesc_s);
+        }
+        commit_el(&bar_s);
+      };
+      int ncons = 0;  // phases of bar_consumed waited for (piecewise: two on a tile that straddles w)
+      bool acc1 = false, acc2 = false;  // piecewise: dQ1, dQ2 hold a product
       bool ok = warp_wait(&bar_qfree, 0, ctl, kErrTimeoutSoftmax) && warp_wait(&bar_kv[0], 0, ctl, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
-        mma_tB<D>(tmem + C::COL_A, tmem + C::COL_QT, smem_u32(sK(0)), idesc_s);   // S = Q K^T
-        commit_el(&bar_s);
+        issue_s(0, 0);
         mma_tB<D>(tmem + C::COL_B, tmem + C::COL_DOT, smem_u32(sV(0)), idesc_s);  // dP = dO V^T
         commit_el(&bar_dp);
       }
@@ -1112,20 +1143,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int st = t % STAGES;
         const int st1 = (t + 1) % STAGES;
         const bool next = t + 1 < nkv;
+        const int cls = cls_of(t);
+        if constexpr (PW) {
+          if (cls == (kNearB | kFarB)) {  // S(q2, k2) once the softmax warps hold S(q1, k1)
+            if (!(ok = warp_wait(&bar_consumed, ncons & 1, ctl, kErrTimeoutSoftmax))) break;
+            ++ncons;
+            tc_fence_after();
+            mma_tB<D>(tmem + C::COL_A, tmem + C::COL_Q2T, smem_u32(sK2(st)), idesc_s);
+            commit_el(&bar_s);
+          }
+        }
         if (next) {
-          if (!(ok = warp_wait(&bar_consumed, t & 1, ctl, kErrTimeoutSoftmax))) break;
+          if (!(ok = warp_wait(&bar_consumed, ncons & 1, ctl, kErrTimeoutSoftmax))) break;
+          ++ncons;
           if (!(ok = warp_wait(&bar_kv[st1], ((t + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
           tc_fence_after();
-          mma_tB<D>(tmem + C::COL_A, tmem + C::COL_QT, smem_u32(sK(st1)), idesc_s);
-          commit_el(&bar_s);
+          issue_s(t + 1, st1);
         }
         // dQ += dS K, chunk group 0 as soon as the softmax warps have formed it
+        // (piecewise: dQ1 += dS_near K1, dQ2 += dS_far K2, the far part beside
+        // the near one when the tile straddles w)
         if (!(ok = warp_wait(&bar_ds[0], t & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_tY_g<0>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, t > 0);
+        if constexpr (!PW) {
+          mma_tY_g<0>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, t > 0);
+        } else {
+          if (cls & kNearB) mma_tY_g<0>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, acc1);
+          if (cls & kFarB)
+            mma_tY_g<0>(tmem + C::COL_DQ2, tmem + C::COL_B + (cls == kFarB ? 0u : 32u), smem_u32(sK2(st)), idesc_g,
+                        acc2);
+        }
         if (!(ok = warp_wait(&bar_ds[1], t & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
-        mma_tY_g<1>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, true);
+        if constexpr (!PW) {
+          mma_tY_g<1>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, true);
+        } else {
+          if (cls & kNearB) mma_tY_g<1>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, true);
+          if (cls & kFarB)
+            mma_tY_g<1>(tmem + C::COL_DQ2, tmem + C::COL_B + (cls == kFarB ? 0u : 32u), smem_u32(sK2(st)), idesc_g,
+                        true);
+          acc1 |= (cls & kNearB) != 0;
+          acc2 |= (cls & kFarB) != 0;
+        }
         commit_el(&bar_kvempty[st]);
         if (next) {
           mma_tB<D>(tmem + C::COL_B, tmem + C::COL_DOT, smem_u32(sV(st1)), idesc_s);
@@ -1146,10 +1205,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float neg_L2 = in_m ? -args.lse[g] * kLog2e : -INFINITY;
     float dlt = (in_m && !make_delta) ? args.delta[g] : 0.f;
     bool ok = true;
-    if (nkv > 0) {  // group 0 copies Q, group 1 copies dO into TMEM
+    if (nkv > 0) {  // group 0 copies Q (Q1 and Q2), group 1 copies dO into TMEM
       ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma);
       if (ok) {
         tile_row_to_tmem<D>(hc == 0 ? sQ : sDO, r, lane_addr + (hc == 0 ? C::COL_QT : C::COL_DOT));
+        if constexpr (PW) {
+          if (hc == 0) tile_row_to_tmem<D>(sQ2, r, lane_addr + C::COL_Q2T);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -1177,15 +1239,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       dlt = halves[r] + halves[kBM + r];
       if (hc == 0 && in_m) args.delta_out[g] = dlt;
     }
+    int sph = 0;  // phases of bar_s seen (piecewise: two on a tile that straddles w)
+    bool touched1 = false, touched2 = false;  // piecewise: some key tile fed dQ1 / dQ2
     for (int t = 0; ok && t < nkv; ++t) {
       const int k0 = t * kBN;
-      if (!(ok = warp_wait(&bar_s, t & 1, ctl, kErrTimeoutMma))) break;
+      const int cls = cls_of(t);
+      if (!(ok = warp_wait(&bar_s, sph & 1, ctl, kErrTimeoutMma))) break;
+      ++sph;
       tc_fence_after();
       uint32_t sv[64];
       tmem_ld_x32(lane_addr + C::COL_A + cb, TB_CHUNK(sv, 0));
       tmem_ld_x32(lane_addr + C::COL_A + cb + 32, TB_CHUNK(sv, 1));
       tmem_ld_wait(TB_CHUNK(sv, 0));
       tmem_ld_wait(TB_CHUNK(sv, 1));
+      // piecewise: key column j of the tile is far iff j <= pwl
+      const long long pwl = PW ? (long long)row + args.P_SEQ - k0 - args.w : 0;
+      if constexpr (PW) {
+        touched1 |= (cls & kNearB) != 0;
+        touched2 |= (cls & kFarB) != 0;
+        if (cls == (kNearB | kFarB)) {  // S(q1, k1) is held: take S(q2, k2) where far
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_consumed);
+          if (!(ok = warp_wait(&bar_s, sph & 1, ctl, kErrTimeoutMma))) break;
+          ++sph;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t s2[32];
+            tmem_ld_x32(lane_addr + C::COL_A + cb + 32 * c, s2);
+            tmem_ld_wait(s2);
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (cb + 32 * c + e <= pwl) sv[32 * c + e] = s2[e];
+          }
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_consumed);  // S buffer free for S(t + 1)
@@ -1207,6 +1296,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!(ok = warp_wait(&bar_dp, t & 1, ctl, kErrTimeoutMma))) break;
       tc_fence_after();
+      if (PW && cls == (kNearB | kFarB)) {
+        // dS split by distance: the near part over dP as usual, the far part
+        // 32 columns further (chunk 0's once dP's chunk 1 has been read)
+        uint32_t far0[16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dp[32];
+          tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, dp);
+          tmem_ld_wait(dp);
+          uint32_t nk[16], fk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = 32 * c + 2 * e;
+            const float2 ds = fmul2(make_float2(p[c0], p[c0 + 1]),
+                                    fadd2(make_float2(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                          make_float2(-dlt, -dlt)));
+            const bool f0 = cb + c0 <= pwl, f1 = cb + c0 + 1 <= pwl;
+            nk[e] = pack2<BF>(f0 ? 0.f : ds.x, f1 ? 0.f : ds.y);
+            fk[e] = pack2<BF>(f0 ? ds.x : 0.f, f1 ? ds.y : 0.f);
+          }
+          tmem_st_x16(lane_addr + C::COL_B + cb + 16 * c, nk);
+          if (c == 0) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) far0[e] = fk[e];
+            continue;
+          }
+          tmem_st_x16(lane_addr + C::COL_B + cb + 32, far0);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_ds[0]);
+          tmem_st_x16(lane_addr + C::COL_B + cb + 48, fk);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_ds[1]);
+        }
+        continue;
+      }
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t dp[32];
@@ -1235,24 +1363,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // written by TMA stores, which clip rows past M and columns past D.
     (void)g;
     const bool live = ok && nkv > 0;
+    // (piecewise: dQ1 over the first slot's K1, dQ2 over its K2; an output no
+    // key tile fed is zero)
+    auto stage_out = [&](uint8_t* tile, uint32_t col, bool fed) {
 #pragma unroll
-    for (int cc = 0; cc < D / 64; ++cc) {
-      const int c = hc * (D / 64) + cc;  // this thread's 32-column chunks of the row
-      uint32_t v[32];
-      if (live) {
-        tmem_ld_x32(lane_addr + C::COL_DQ + 32 * c, v);
-        tmem_ld_wait(v);
-      } else {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = hc * (D / 64) + cc;  // this thread's 32-column chunks of the row
+        uint32_t v[32];
+        if (live && fed) {
+          tmem_ld_x32(lane_addr + col + 32 * c, v);
+          tmem_ld_wait(v);
+        } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = 0u;
+          for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        stage_row_chunk_sw128<BF>(smem_u32(tile), r, c, v, args.sm_scale);
       }
-      stage_row_chunk_sw128<BF>(smem_u32(sK(0)), r, c, v, args.sm_scale);
-    }
+    };
+    stage_out(sK(0), C::COL_DQ, !PW || touched1);
+    if constexpr (PW) stage_out(sK2(0), C::COL_DQ2, touched2);
     fence_proxy_async_smem();
     named_bar_sync(1, kRowWarps * 32);
     if (warp == 0 && lane == 0 && q0 < args.M) {
 #pragma unroll
-      for (int kb = 0; kb < D / 64; ++kb) tma_store_3d(&tm_dq, sK(0) + kb * (kBM * 128), kb * 64, q0, bh);
+      for (int kb = 0; kb < D / 64; ++kb) {
+        tma_store_3d(&tm_dq, sK(0) + kb * (kBM * 128), kb * 64, q0, bh);
+        if constexpr (PW) tma_store_3d(&tm_dq2, sK2(0) + kb * (kBM * 128), kb * 64, q0, bh);
+      }
       tma_store_commit_and_wait_read();
     }
   }
@@ -1684,24 +1821,26 @@ cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& m, const 
   return cudaErrorNotSupported;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool PW = false>
 static cudaError_t launch_dq_std_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
-  using C = DqStdCfg<D>;
-  auto kern = attn_bwd_dq_std_kernel<T, D>;
+  using C = DqStdCfg<D, PW>;
+  auto kern = attn_bwd_dq_std_kernel<T, D, PW>;
   static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.M + kBM - 1) / kBM);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
   kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.dq,
-                                                                    a.delta_out ? m.o : m.q, a);
+                                                                    a.delta_out ? m.o : m.q, PW ? m.q2 : m.q,
+                                                                    PW ? m.k2 : m.k, PW ? m.dq2 : m.dq, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq(int mode, bool bf16, int D, const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   if (mode == kStd && D == 64) return bf16 ? launch_dq_std_t<__nv_bfloat16, 64>(m, a, s) : launch_dq_std_t<__half, 64>(m, a, s);
   if (mode == kStd && D == 128) return bf16 ? launch_dq_std_t<__nv_bfloat16, 128>(m, a, s) : launch_dq_std_t<__half, 128>(m, a, s);
-  if (mode == kPiecewise && D == 64) return bf16 ? launch_dq_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dq_t<__half, kPiecewise, 64>(m, a, s);
+  if (mode == kPiecewise && D == 64)  // the standard kernel's structure with Q2 and dQ2 in TMEM
+    return bf16 ? launch_dq_std_t<__nv_bfloat16, 64, true>(m, a, s) : launch_dq_std_t<__half, 64, true>(m, a, s);
   if (mode == kPiecewise && D == 128) return bf16 ? launch_dq_t<__nv_bfloat16, kPiecewise, 128>(m, a, s) : launch_dq_t<__half, kPiecewise, 128>(m, a, s);
   return cudaErrorNotSupported;
 }
