@@ -38,13 +38,13 @@
 // gradient MMAs read the packed operand's 8-column K-steps from both halves.
 //
 // The standard mode runs the specialised attn_bwd_dkdv_std_kernel /
-// attn_bwd_dq_std_kernel further down.  Of the generic kernels, the
-// piecewise mode overlaps more at D = 64, where TMEM has room: dK/dV keeps
-// P^T in its last 64 columns so the next query tile's S^T starts as soon as
-// the softmax holds S^T in registers, and dQ alternates two S buffers.  At
-// D = 128, where TMEM cannot hold all three accumulators beside a 128-query
-// tile's S^T and dP^T, the piecewise key side runs in bwd_pw_steps.cu with
-// 64-query steps instead.
+// attn_bwd_dq_std_kernel further down, and so does the piecewise dQ at
+// D = 64 (attn_bwd_dq_std_kernel's piecewise mode).  The generic kernels
+// serve the rest of the piecewise mode: dK/dV at D = 64, which keeps P^T in
+// its last 64 TMEM columns so the next query tile's S^T starts as soon as
+// the softmax holds S^T in registers, and dQ at D = 128.  At D = 128, where
+// TMEM cannot hold all three accumulators beside a 128-query tile's S^T and
+// dP^T, the piecewise key side runs in bwd_pw_steps.cu with 64-query steps.
 #include "bwd_common.cuh"
 #include "common.cuh"
 #include "launch.h"
@@ -580,10 +580,6 @@ struct DqCfg {
   static constexpr int OFF_O = NRES * TILE + STAGES * STAGE;  // the O tile (delta), after the ring
   static constexpr int SMEM = OFF_O + TILE + 1024;
   static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DQ = 256, COL_DQ2 = 256 + D;
-  // Piecewise with room for a second 128-column S buffer (D = 64) and two
-  // K/V stages: the next tile's S is computed while this tile's dS is formed.
-  static constexpr bool DBUF = (MODE == kPiecewise) && (256 + 2 * D + 128 <= 512) && STAGES >= 2;
-  static constexpr uint32_t COL_C = 256 + 2 * D;
   static_assert(STAGES >= 1, "tile does not fit in shared memory");
   static_assert(SMEM + RESERVE <= kSmemMax, "shared memory overflow");
   static_assert(COL_DQ2 + (MODE == kPiecewise ? D : 0) <= 512, "TMEM overflow");
@@ -604,12 +600,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q, bar_kv[STAGES], bar_kvempty[STAGES];
   __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_consumed, bar_ds, bar_done;
-  __shared__ __align__(8) uint64_t bar_sb[2];  // DBUF: S of even / odd tiles ready
-  __shared__ __align__(8) uint64_t bar_o;      // delta: the O tile landed
+  __shared__ __align__(8) uint64_t bar_o;  // delta: the O tile landed
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  // DBUF: tile t's S buffer
-  auto sbuf = [](int t) -> uint32_t { return (C::DBUF && (t & 1)) ? C::COL_C : C::COL_A; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -640,8 +633,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&bar_kvempty[s], 1);
     }
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_sb[0], 1);
-    mbar_init(&bar_sb[1], 1);
     mbar_init(&bar_dp, 1);
     mbar_init(&bar_consumed, kRowWarps);
     mbar_init(&bar_ds, kRowWarps);
@@ -700,60 +691,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = warp_wait(&bar_q, 0, ctl, kErrTimeoutTma);
       bool acc1 = false, acc2 = false;
       int nstr = 0;
-      if constexpr (C::DBUF) {
-        // S(t + 1) (its near, or only, product) is issued before dQ(t); a
-        // tile that needs both products gets S(q2, k2) in COL_B after dQ(t).
-        auto cls_of = [&](int t) { return pw_class_b(q0, t * kBN, args.P_SEQ, args.w); };
-        auto issue_s1 = [&](int t, int st) {
-          const int cls = cls_of(t);
-          if (cls == kFarB) mma_abT<D>(tmem + sbuf(t), smem_u32(sQ2), smem_u32(sK2(st)), idesc_s);
-          else mma_abT<D>(tmem + sbuf(t), smem_u32(sQ), smem_u32(sK(st)), idesc_s);
-          if (cls != (kNearB | kFarB)) commit_el(&bar_sb[t & 1]);
-        };
-        auto issue_s2_dp = [&](int t, int st) -> bool {
-          if (cls_of(t) == (kNearB | kFarB)) {
-            mma_abT<D>(tmem + C::COL_B, smem_u32(sQ2), smem_u32(sK2(st)), idesc_s);
-            commit_el(&bar_sb[t & 1]);
-            if (!warp_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax)) return false;
-            tc_fence_after();
-            ++nstr;
-          }
-          mma_abT<D>(tmem + C::COL_B, smem_u32(sDO), smem_u32(sV(st)), idesc_s);  // dP = dO V^T
-          commit_el(&bar_dp);
-          return true;
-        };
-        if (ok) ok = warp_wait(&bar_kv[0], 0, ctl, kErrTimeoutTma);
-        if (ok) {
-          tc_fence_after();
-          issue_s1(0, 0);
-          ok = issue_s2_dp(0, 0);
-        }
-        for (int t = 0; ok && t < nkv; ++t) {
-          const int st = t % STAGES, st1 = (t + 1) % STAGES;
-          const bool more = t + 1 < nkv;
-          if (more) {
-            if (!(ok = warp_wait(&bar_kv[st1], ((t + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
-            tc_fence_after();
-            issue_s1(t + 1, st1);
-          }
-          if (!(ok = warp_wait(&bar_ds, t & 1, ctl, kErrTimeoutSoftmax))) break;
-          tc_fence_after();
-          const int cls = cls_of(t);
-          if (cls & kNearB) {
-            mma_tY<D>(tmem + C::COL_DQ, tmem + C::COL_B, smem_u32(sK(st)), idesc_g, acc1);
-            acc1 = true;
-          }
-          if (cls & kFarB) {  // the far part of dS: COL_B when the whole tile is far
-            const uint32_t src = (cls == kFarB) ? C::COL_B : sbuf(t) + 32;
-            mma_tY<D>(tmem + C::COL_DQ2, tmem + src, smem_u32(sK2(st)), idesc_g, acc2);
-            acc2 = true;
-          }
-          commit_el(&bar_kvempty[st]);
-          if (more && !(ok = issue_s2_dp(t + 1, st1))) break;
-        }
-        if (ok) commit_el(&bar_done);
-      }
-      for (int t = 0; !C::DBUF && ok && t < nkv; ++t) {
+      for (int t = 0; ok && t < nkv; ++t) {
         const int st = t % STAGES;
         if (!(ok = warp_wait(&bar_kv[st], (t / STAGES) & 1, ctl, kErrTimeoutTma))) break;
         tc_fence_after();
@@ -794,7 +732,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         commit_el(&bar_kvempty[st]);
       }
-      if (!C::DBUF && ok) commit_el(&bar_done);
+      if (ok) commit_el(&bar_done);
     }
   } else {
     // --------------------------------------------- query-row softmax gradient
@@ -829,17 +767,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool touched1 = false, touched2 = false;
     for (int t = 0; ok && t < nkv; ++t) {
       const int k0 = t * kBN;
-      if constexpr (C::DBUF) {
-        if (!(ok = warp_wait(&bar_sb[t & 1], (t >> 1) & 1, ctl, kErrTimeoutMma))) break;
-      } else {
-        if (!(ok = warp_wait(&bar_s, t & 1, ctl, kErrTimeoutMma))) break;
-      }
+      if (!(ok = warp_wait(&bar_s, t & 1, ctl, kErrTimeoutMma))) break;
       tc_fence_after();
       int cls = kNearB;
       if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
       touched1 |= (cls & kNearB) != 0;
       touched2 |= (cls & kFarB) != 0;
-      const uint32_t s_col = sbuf(t);
+      const uint32_t s_col = C::COL_A;
       uint32_t s[64];
       tmem_ld_x32(lane_addr + s_col + cb, TB_CHUNK(s, 0));
       tmem_ld_x32(lane_addr + s_col + cb + 32, TB_CHUNK(s, 1));
