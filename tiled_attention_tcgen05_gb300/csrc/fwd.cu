@@ -923,13 +923,13 @@ __device__ __forceinline__ void fwd2_body(const CUtensorMap& tm_q, const CUtenso
           // far iff key k0 + c satisfies row + P_SEQ - (k0 + c) >= w: take S(q2, k2) there
           const long long pwl = (long long)row + args.P_SEQ - k0 - args.w;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t s2[32];
-            tmem_ld_x32(lane_addr + C::COL_X + 32 * c, s2);
+          for (int c = 0; c < 8; ++c) {  // 16 columns at a time: the row's 128 scores are live
+            uint32_t s2[16];
+            tmem_ld_x16(lane_addr + C::COL_X + 16 * c, s2);
             tmem_ld_wait(s2);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (32 * c + j <= pwl) x[32 * c + j] = __uint_as_float(s2[j]);
+            for (int j = 0; j < 16; ++j)
+              if (16 * c + j <= pwl) x[16 * c + j] = __uint_as_float(s2[j]);
           }
           tc_fence_before();
           __syncwarp();
