@@ -1,7 +1,7 @@
 // Backward attention kernels for sm_103a (tcgen05 + TMA), standard and
 // piecewise.
 //
-// Two kernels, each one CTA per 128-row tile, 320 threads:
+// Three kernels, each one CTA per 128-row tile, 320 threads:
 //   warps 0-7  element-wise softmax gradient; TMEM lane = row (warp % 4
 //              selects the 32-lane quarter), and warp / 4 selects which half
 //              of the tile's 128 columns the thread handles;
@@ -9,15 +9,22 @@
 //   warp 9     TMEM allocator and MMA issuer (the whole warp; one elected
 //              lane issues each K-loop of MMAs as a single asm block).
 //
-//  * attn_bwd_dkdv_kernel: key-stationary.  The CTA keeps a 128-key tile of K
-//    and V in shared memory and walks the query tiles that see it.  Per query
-//    tile: S^T = K Q^T and dP^T = V dO^T (tcgen05, into TMEM); thread j (key
-//    row j) recomputes P^T = exp2(S^T * c - L * log2 e) and
+//  * attn_bwd_dkdv_std_kernel: key-stationary.  The CTA keeps a 128-key tile
+//    of K and V in shared memory and walks the query tiles that see it.  Per
+//    query tile: S^T = K Q^T and dP^T = V dO^T (tcgen05, into TMEM); thread j
+//    (key row j) recomputes P^T = exp2(S^T * c - L * log2 e) and
 //    dS^T = P^T o (dP^T - delta), writes both back into TMEM as 16-bit
 //    operands; then dV += P^T dO and dK += dS^T Q read them straight from
-//    TMEM.  dK is scaled by sm_scale at the end.
-//  * attn_bwd_dq_kernel: query-stationary.  Per key tile: S = Q K^T,
-//    dP = dO V^T, dS = P o (dP - delta), dQ += dS K; dQ * sm_scale at the end.
+//    TMEM.  dK is scaled by sm_scale at the end.  Standard mode, and the
+//    piecewise mode at D = 64.
+//  * attn_bwd_dq_std_kernel: query-stationary.  Per key tile: S = Q K^T,
+//    dP = dO V^T, dS = P o (dP - delta), dQ += dS K; dQ * sm_scale at the
+//    end; it also forms delta.  Standard mode, and the piecewise mode at
+//    D = 64.
+//  * attn_bwd_dq_kernel: the same for the piecewise mode at D = 128, with Q1,
+//    Q2 and dO resident in shared memory.  (The piecewise key side at D = 128
+//    runs in bwd_pw_steps.cu with 64-query steps: TMEM cannot hold all three
+//    accumulators beside a 128-query tile's S^T and dP^T.)
 //
 // Page sources: "Triton fused attention tutorial, updated with JVP support",
 // _attn_bwd / _attn_bwd_dkdv / _attn_bwd_dq (pT = exp2(qkT - m), dv += pT do,
@@ -29,22 +36,10 @@
 //
 // Departures from the pages, all result-preserving: P^T and dS^T stay in
 // TMEM as MMA operands; piecewise tiles that are entirely near or entirely
-// far run one score MMA and one gradient MMA instead of two.
-//
-// TMEM operand placement: a thread of column half h (h = warp / 4) owns the
-// score columns [64h, 64h + 64) of its 128-column buffer; it writes its
-// 16-bit results (64 values = 32 packed columns) at [64h, 64h + 32) and, for
-// the far half of a straddling piecewise tile, at [64h + 32, 64h + 64).  The
-// gradient MMAs read the packed operand's 8-column K-steps from both halves.
-//
-// The standard mode runs the specialised attn_bwd_dkdv_std_kernel /
-// attn_bwd_dq_std_kernel further down, and so does the piecewise dQ at
-// D = 64 (attn_bwd_dq_std_kernel's piecewise mode).  The generic kernels
-// serve the rest of the piecewise mode: dK/dV at D = 64, which keeps P^T in
-// its last 64 TMEM columns so the next query tile's S^T starts as soon as
-// the softmax holds S^T in registers, and dQ at D = 128.  At D = 128, where
-// TMEM cannot hold all three accumulators beside a 128-query tile's S^T and
-// dP^T, the piecewise key side runs in bwd_pw_steps.cu with 64-query steps.
+// far run one score MMA and one gradient MMA instead of two, and a tile
+// that straddles w runs its two score products in turn in one buffer.
+#include <type_traits>
+
 #include "bwd_common.cuh"
 #include "common.cuh"
 #include "launch.h"
@@ -84,421 +79,6 @@ __device__ __forceinline__ void mma_tY(uint32_t d_tmem, uint32_t x_tmem, uint32_
   mma_ts_n<8>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
-
-// ======================================================================
-//                        dK, dV (key-stationary)
-// ======================================================================
-// The generic key-stationary kernel (piecewise D = 64: dV, dK1 and dK2).
-template <int MODE, int D>
-struct DkdvCfg {
-  static constexpr int BLK = kBM * 128;
-  static constexpr int TILE = (D / 64) * BLK;
-  static constexpr int NRES = (MODE == kStd) ? 2 : 3;  // K, V | K1, K2, V
-  static constexpr int NQT = (MODE == kStd) ? 2 : 3;   // Q, dO | Q1, Q2, dO
-  static constexpr int STAGE = NQT * TILE;
-  static constexpr int RESERVE = 2048 + 4 * 1024;      // alignment + static (barriers, L, delta)
-  static constexpr int ST_FIT = (kSmemMax - RESERVE - NRES * TILE) / STAGE;
-  static constexpr int STAGES = ST_FIT > 4 ? 4 : ST_FIT;
-  static constexpr int SMEM = NRES * TILE + STAGES * STAGE + 1024;
-  static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D;
-  static constexpr uint32_t COL_DK2 = 256 + 2 * D;
-  // Piecewise, all outputs, with 64 spare columns for P^T (D = 64) and two
-  // query stages: P^T lives there, so S^T's buffer frees as soon as the
-  // softmax holds S^T in registers and the next tile's score MMA can start.
-  static constexpr bool EARLY = (MODE == kPiecewise) && (256 + 3 * D + 64 <= 512) && STAGES >= 2;
-  static constexpr uint32_t COL_P = 256 + 3 * D;
-  static_assert(STAGES >= 1, "tile does not fit in shared memory");
-  static_assert(COL_DK2 + (MODE == kPiecewise ? D : 0) <= 512, "TMEM overflow");
-};
-
-template <typename T, int MODE, int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                         const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
-                         const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dk,
-                         const __grid_constant__ CUtensorMap tm_dk2, const BwdArgs args) {
-  using C = DkdvCfg<MODE, D>;
-  constexpr bool BF = DT<T>::bf16;
-  constexpr int STAGES = C::STAGES;
-  constexpr bool PW = (MODE == kPiecewise);
-
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_kv, bar_q[STAGES], bar_qempty[STAGES];
-  __shared__ __align__(8) uint64_t bar_s, bar_dp, bar_consumed, bar_ds, bar_done;
-  __shared__ __align__(8) uint64_t bar_sfree, bar_pfree;  // EARLY: S^T in registers; P^T read by dV
-  __shared__ __align__(16) float sL[STAGES][kBM];      // L * log2(e) of the tile's queries
-  __shared__ __align__(16) float sDelta[STAGES][kBM];  // delta of the tile's queries
-  __shared__ uint32_t tmem_slot;
-  __shared__ int abort_flag;
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  int bh, kt;  // key tiles with the most query tiles (the first ones, causal) first
-  if (!grouped_tile(blockIdx.x, args.BH, (args.N + kBN - 1) / kBN, kGroupHeads, &bh, &kt)) return;
-  const int k0 = kt * kBN;
-  const int num_q_tiles = (args.M + kBM - 1) / kBM;
-  const int i0 = first_q_tile_for(k0, args.P_SEQ, args.causal);
-  const int nq = num_q_tiles > i0 ? num_q_tiles - i0 : 0;
-
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = base;                       // K | K1
-  uint8_t* sK2 = base + C::TILE;            // piecewise K2
-  uint8_t* sV = base + (C::NRES - 1) * C::TILE;
-  uint8_t* sStages = base + C::NRES * C::TILE;
-  auto sQ = [&](int st) { return sStages + st * C::STAGE; };                 // Q | Q1
-  auto sQ2 = [&](int st) { return sStages + st * C::STAGE + C::TILE; };      // Q2
-  auto sDO = [&](int st) { return sStages + st * C::STAGE + (C::NQT - 1) * C::TILE; };
-
-  WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    mbar_init(&bar_kv, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bar_q[s], 2);  // TMA bytes + L/delta stores
-      mbar_init(&bar_qempty[s], 1);
-    }
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_dp, 1);
-    mbar_init(&bar_consumed, kRowWarps);
-    mbar_init(&bar_ds, kRowWarps);
-    mbar_init(&bar_done, 1);
-    mbar_init(&bar_sfree, kRowWarps);
-    mbar_init(&bar_pfree, 1);
-    fence_mbar_init();
-  }
-  if (warp == kWarpMma) {
-    tmem_alloc(&tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_slot;
-
-  if (warp == kWarpProducer) {
-    // ------------------------------------------------------------ producer
-    if (nq > 0) {
-      if (lane == 0) {
-        mbar_expect_tx(&bar_kv, C::NRES * C::TILE);
-        load_tile_b<D>(sK, &tm_k, &bar_kv, k0, bh);
-        if constexpr (PW) load_tile_b<D>(sK2, &tm_k2, &bar_kv, k0, bh);
-        load_tile_b<D>(sV, &tm_v, &bar_kv, k0, bh);
-      }
-      // L * log2(e) and delta of a query tile are fetched into registers one
-      // tile ahead, so that when a stage frees the TMA is issued at once and
-      // the global-load latency stays off the critical path.  A stage's
-      // barrier takes two arrivals: the TMA byte count and the L/delta stores.
-      float lv[kBM / 32], dv[kBM / 32];
-      auto fetch = [&](int u) {
-        const int q0 = (i0 + u) * kBM;
-#pragma unroll
-        for (int e = 0; e < kBM / 32; ++e) {
-          const int q = q0 + lane + 32 * e;
-          const size_t g = static_cast<size_t>(bh) * args.M + q;
-          lv[e] = (q < args.M) ? args.lse[g] * kLog2e : INFINITY;
-          dv[e] = (q < args.M) ? args.delta[g] : 0.f;
-        }
-      };
-      fetch(0);
-      int issued = 0;
-      for (int u = 0; u < nq; ++u) {
-        const int st = u % STAGES;
-        if (u >= STAGES) {
-          if (!warp_wait(&bar_qempty[st], ((u / STAGES) - 1) & 1, ctl, kErrTimeoutMma)) break;
-        }
-        const int q0 = (i0 + u) * kBM;
-        if (lane == 0) {
-          mbar_expect_tx(&bar_q[st], C::NQT * C::TILE);
-          load_tile_b<D>(sQ(st), &tm_q, &bar_q[st], q0, bh);
-          if constexpr (PW) load_tile_b<D>(sQ2(st), &tm_q2, &bar_q[st], q0, bh);
-          load_tile_b<D>(sDO(st), &tm_do, &bar_q[st], q0, bh);
-        }
-#pragma unroll
-        for (int e = 0; e < kBM / 32; ++e) {
-          sL[st][lane + 32 * e] = lv[e];
-          sDelta[st][lane + 32 * e] = dv[e];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_q[st]);
-        issued = u + 1;
-        if (u + 1 < nq) fetch(u + 1);
-      }
-      if (lane == 0) {  // never leave a TMA write in flight behind an early exit
-        int zero = 0;
-        WaitCtl drain{args.err, args.timeout_ns, reinterpret_cast<volatile int*>(&zero)};
-        mbar_wait(&bar_kv, 0, drain, kErrTimeoutTma);
-        for (int u = issued - STAGES > 0 ? issued - STAGES : 0; u < issued; ++u)
-          mbar_wait(&bar_q[u % STAGES], (u / STAGES) & 1, drain, kErrTimeoutTma);
-      }
-    }
-  } else if (warp == kWarpMma) {
-    // ----------------------------------------------------------------- MMA
-    if (nq > 0) {
-      constexpr uint32_t idesc_s = idesc_f16(kBN, kBM, BF, false, false);  // M = keys, N = queries
-      constexpr uint32_t idesc_g = idesc_f16(kBN, D, BF, false, true);     // M = keys, N = D
-      bool ok = warp_wait(&bar_kv, 0, ctl, kErrTimeoutTma);
-      bool acc1 = false, acc2 = false;
-      int nstr = 0;
-      if constexpr (C::EARLY) {
-        auto cls_of = [&](int u) { return pw_class_b((i0 + u) * kBM, k0, args.P_SEQ, args.w); };
-        // S^T(u), its near (or only) product, into COL_A; bar_s unless the tile needs both
-        auto issue_s1 = [&](int u, int st) {
-          const int cls = cls_of(u);
-          if (cls == kFarB) mma_abT<D>(tmem + C::COL_A, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
-          else mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(st)), idesc_s);
-          if (cls != (kNearB | kFarB)) commit_el(&bar_s);
-        };
-        bool s_issued = false;  // S^T(u) went out early, under tile u - 1
-        for (int u = 0; ok && u < nq; ++u) {
-          const int st = u % STAGES;
-          const int cls = cls_of(u);
-          if (!s_issued) {
-            if (!(ok = warp_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
-            tc_fence_after();
-            issue_s1(u, st);
-          }
-          if (cls == (kNearB | kFarB)) {
-            mma_abT<D>(tmem + C::COL_B, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
-            commit_el(&bar_s);
-            if (!(ok = warp_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
-            tc_fence_after();
-            ++nstr;
-          }
-          mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(st)), idesc_s);  // dP^T = V dO^T
-          commit_el(&bar_dp);
-          s_issued = false;
-          // a tile that needs both products keeps its far dS^T in COL_A: no early S^T after it
-          if (u + 1 < nq && cls != (kNearB | kFarB)) {
-            const int st1 = (u + 1) % STAGES;
-            if (!(ok = warp_wait(&bar_sfree, u & 1, ctl, kErrTimeoutSoftmax))) break;
-            if (!(ok = warp_wait(&bar_q[st1], ((u + 1) / STAGES) & 1, ctl, kErrTimeoutTma))) break;
-            tc_fence_after();
-            issue_s1(u + 1, st1);
-            s_issued = true;
-          }
-          if (!(ok = warp_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
-          tc_fence_after();
-          mma_tY<D, 32>(tmem + C::COL_DV, tmem + C::COL_P, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
-          commit_el(&bar_pfree);
-          if (cls & kNearB) {
-            mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
-            acc1 = true;
-          }
-          if (cls & kFarB) {
-            const uint32_t src = (cls == kFarB) ? C::COL_B : C::COL_A + 32;
-            mma_tY<D>(tmem + C::COL_DK2, tmem + src, smem_u32(sQ2(st)), idesc_g, acc2);
-            acc2 = true;
-          }
-          commit_el(&bar_qempty[st]);
-        }
-        if (ok) commit_el(&bar_done);
-      }
-      for (int u = 0; !C::EARLY && ok && u < nq; ++u) {
-        const int st = u % STAGES;
-        const int q0 = (i0 + u) * kBM;
-        if (!(ok = warp_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
-        tc_fence_after();
-        int cls = kNearB;
-        if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
-        if (cls == kNearB) {
-          mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(st)), idesc_s);
-        } else if (cls == kFarB) {
-          mma_abT<D>(tmem + C::COL_A, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
-        } else {
-          mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(st)), idesc_s);
-          mma_abT<D>(tmem + C::COL_B, smem_u32(sK2), smem_u32(sQ2(st)), idesc_s);
-        }
-        commit_el(&bar_s);
-        if (cls == (kNearB | kFarB)) {
-          if (!(ok = warp_wait(&bar_consumed, nstr & 1, ctl, kErrTimeoutSoftmax))) break;
-          tc_fence_after();
-          ++nstr;
-        }
-        mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(st)), idesc_s);  // dP^T = V dO^T
-        commit_el(&bar_dp);
-        if (!(ok = warp_wait(&bar_ds, u & 1, ctl, kErrTimeoutSoftmax))) break;
-        tc_fence_after();
-        mma_tY<D>(tmem + C::COL_DV, tmem + C::COL_A, smem_u32(sDO(st)), idesc_g, u > 0);  // dV += P^T dO
-        if constexpr (!PW) {
-          mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, u > 0);  // dK += dS^T Q
-        } else {
-          if (cls & kNearB) {
-            mma_tY<D>(tmem + C::COL_DK, tmem + C::COL_B, smem_u32(sQ(st)), idesc_g, acc1);
-            acc1 = true;
-          }
-          if (cls & kFarB) {  // the far part of dS: COL_B when the whole tile is far
-            const uint32_t src = (cls == kFarB) ? C::COL_B : C::COL_A + 32;
-            mma_tY<D>(tmem + C::COL_DK2, tmem + src, smem_u32(sQ2(st)), idesc_g, acc2);
-            acc2 = true;
-          }
-        }
-        commit_el(&bar_qempty[st]);
-      }
-      if (!C::EARLY && ok) commit_el(&bar_done);
-    }
-  } else {
-    // ------------------------------------------- key-row softmax gradient
-    const int hc = warp >> 2;      // column half of the tile this thread handles
-    const int cb = 64 * hc;        // first column of that half
-    const int j = k0 + (threadIdx.x & 127);  // this thread's key
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    bool ok = true;
-    bool touched1 = false, touched2 = false;
-    for (int u = 0; u < nq; ++u) {
-      const int st = u % STAGES;
-      const int q0 = (i0 + u) * kBM;
-      if (!(ok = warp_wait(&bar_q[st], (u / STAGES) & 1, ctl, kErrTimeoutTma))) break;
-      if (!(ok = warp_wait(&bar_s, u & 1, ctl, kErrTimeoutMma))) break;
-      tc_fence_after();
-      int cls = kNearB;
-      if constexpr (PW) cls = pw_class_b(q0, k0, args.P_SEQ, args.w);
-      touched1 |= (cls & kNearB) != 0;
-      touched2 |= (cls & kFarB) != 0;
-      uint32_t s[64];
-      tmem_ld_x32(lane_addr + C::COL_A + cb, TB_CHUNK(s, 0));
-      tmem_ld_x32(lane_addr + C::COL_A + cb + 32, TB_CHUNK(s, 1));
-      tmem_ld_wait(TB_CHUNK(s, 0));
-      tmem_ld_wait(TB_CHUNK(s, 1));
-      // far iff column c >= fl (query q0 + c, key j: q0 + c + P_SEQ - j >= w)
-      const long long fl = (long long)j + args.w - args.P_SEQ - q0;
-      if (cls == (kNearB | kFarB)) {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t s2[32];
-          tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, s2);
-          tmem_ld_wait(s2);
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (cb + 32 * c + e >= fl) s[32 * c + e] = s2[e];
-        }
-      }
-      if constexpr (C::EARLY) {  // S^T is in registers: its buffer may take the next tile's
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_sfree);
-      }
-      // L * log2(e) of the 64 queries, four per vector load
-      const float4* L4 = reinterpret_cast<const float4*>(&sL[st][cb]);
-      float p[64];
-#pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = L4[c4];
-        p[4 * c4 + 0] = ex2(fmaf(__uint_as_float(s[4 * c4 + 0]), args.scale_log2, -l4.x));
-        p[4 * c4 + 1] = ex2(fmaf(__uint_as_float(s[4 * c4 + 1]), args.scale_log2, -l4.y));
-        p[4 * c4 + 2] = ex2(fmaf(__uint_as_float(s[4 * c4 + 2]), args.scale_log2, -l4.z));
-        p[4 * c4 + 3] = ex2(fmaf(__uint_as_float(s[4 * c4 + 3]), args.scale_log2, -l4.w));
-      }
-      // causal: key j visible from query q0 + c iff c >= j - P_SEQ - q0
-      if (args.causal && k0 + kBN - 1 > q0 + args.P_SEQ) {
-        const int lo = j - args.P_SEQ - q0 - cb;
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < lo) p[c] = 0.f;
-      }
-      if constexpr (C::EARLY) {  // P^T goes to its own columns once dV(u - 1) has read them
-        if (u > 0 && !(ok = warp_wait(&bar_pfree, (u - 1) & 1, ctl, kErrTimeoutMma))) break;
-        tc_fence_after();
-      }
-      const uint32_t p_col = C::EARLY ? C::COL_P + 32 * hc : C::COL_A + cb;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) pk[e] = pack2<BF>(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
-        tmem_st_x16(lane_addr + p_col + 16 * c, pk);
-      }
-      if (cls == (kNearB | kFarB)) {
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_consumed);
-      }
-      if (!(ok = warp_wait(&bar_dp, u & 1, ctl, kErrTimeoutMma))) break;
-      tc_fence_after();
-      const float4* D4 = reinterpret_cast<const float4*>(&sDelta[st][cb]);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dp[32];
-        tmem_ld_x32(lane_addr + C::COL_B + cb + 32 * c, dp);
-        tmem_ld_wait(dp);
-        float ds[32];
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 d4 = D4[8 * c + e4];
-          ds[4 * e4 + 0] = p[32 * c + 4 * e4 + 0] * (__uint_as_float(dp[4 * e4 + 0]) - d4.x);
-          ds[4 * e4 + 1] = p[32 * c + 4 * e4 + 1] * (__uint_as_float(dp[4 * e4 + 1]) - d4.y);
-          ds[4 * e4 + 2] = p[32 * c + 4 * e4 + 2] * (__uint_as_float(dp[4 * e4 + 2]) - d4.z);
-          ds[4 * e4 + 3] = p[32 * c + 4 * e4 + 3] * (__uint_as_float(dp[4 * e4 + 3]) - d4.w);
-        }
-        uint32_t pk1[16];
-        if (cls == (kNearB | kFarB)) {
-          uint32_t pk2[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const bool f0 = cb + 32 * c + 2 * e >= fl, f1 = cb + 32 * c + 2 * e + 1 >= fl;
-            pk1[e] = pack2<BF>(f0 ? 0.f : ds[2 * e], f1 ? 0.f : ds[2 * e + 1]);
-            pk2[e] = pack2<BF>(f0 ? ds[2 * e] : 0.f, f1 ? ds[2 * e + 1] : 0.f);
-          }
-          tmem_st_x16(lane_addr + C::COL_A + cb + 32 + 16 * c, pk2);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) pk1[e] = pack2<BF>(ds[2 * e], ds[2 * e + 1]);
-        }
-        tmem_st_x16(lane_addr + C::COL_B + cb + 16 * c, pk1);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_ds);
-    }
-    // ------------------------------------------------------------ epilogue
-    if (nq > 0 && ok) ok = warp_wait(&bar_done, 0, ctl, kErrTimeoutMma);
-    tc_fence_after();
-    const bool live = ok && nq > 0;
-    (void)j;
-    // The launch's outputs (dV, dK or dK1, dK2), rounded, are staged over the
-    // resident K / K2 / V tiles (free: every MMA has finished) in the output
-    // maps' swizzled box layout and written by TMA stores, which clip rows
-    // past N and columns past D.  An output no query tile touched is zero.
-    const int r = threadIdx.x & 127;  // this thread's key within the tile
-    auto stage_out = [&](int slot, uint32_t col, bool touched, float scale) {
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = hc * (D / 64) + cc;  // this thread's 32-column chunks of the row
-        uint32_t v[32];
-        if (live && touched) {
-          tmem_ld_x32(lane_addr + col + 32 * c, v);
-          tmem_ld_wait(v);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0u;
-        }
-        stage_row_chunk_sw128<BF>(smem_u32(base + slot * C::TILE), r, c, v, scale);
-      }
-    };
-    stage_out(0, C::COL_DV, true, 1.f);
-    stage_out(1, C::COL_DK, !PW || touched1, args.sm_scale);
-    if constexpr (PW) stage_out(2, C::COL_DK2, touched2, args.sm_scale);
-    fence_proxy_async_smem();
-    named_bar_sync(1, kRowWarps * 32);
-    if (warp == 0 && lane == 0 && k0 < args.N) {
-#pragma unroll
-      for (int kb = 0; kb < D / 64; ++kb) {
-        const int off = kb * (kBM * 128);
-        tma_store_3d(&tm_dv, base + off, kb * 64, k0, bh);
-        tma_store_3d(&tm_dk, base + C::TILE + off, kb * 64, k0, bh);
-        if constexpr (PW) tma_store_3d(&tm_dk2, base + 2 * C::TILE + off, kb * 64, k0, bh);
-      }
-      tma_store_commit_and_wait_read();
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
-}
 
 // ======================================================================
 //                         dQ (query-stationary)
@@ -1354,13 +934,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // leave too little room for a full 1024-byte alignment allowance, so the
 // kernel checks the actual padding against PAD at run time and reports
 // kErrSmemLayout instead of running if it does not fit.
-template <int D>
+//
+// Piecewise mode (PW, D = 64): K1, K2 and V stationary, each Q ring slot
+// holds Q1 and Q2 (loaded as the query tile's class needs), and TMEM has the
+// room for dK2 beside dV and dK1 and for the far part of dS^T of a query tile
+// that straddles w (Q2 is its B operand), written densely in the last 64
+// columns.  Such a tile computes S^T(k1, q1), then, once the softmax warps
+// hold it, S^T(k2, q2) in the same buffer, merged per element by distance
+// ("FlagAttention piecewise.py", _bwd_kv_kernel).  Its dS phase is a separate
+// instance of the code, so the other tiles run the standard one.
+template <int D, bool PW = false>
 struct DkdvStdCfg {
   static constexpr int BLK = kBM * 128;
   static constexpr int TILE = (D / 64) * BLK;
-  static constexpr int QST = (D == 128) ? 3 : 4;  // Q ring depth
-  static constexpr int OST = (D == 128) ? 2 : 4;  // dO ring depth
-  static constexpr int LD_OFF = (2 + QST + OST) * TILE;  // L / delta: [buffer][half][L, delta][64] floats
+  static constexpr int NKT = PW ? 3 : 2;  // stationary K, V | K1, K2, V
+  static constexpr int NQT = PW ? 2 : 1;  // tiles of a Q ring slot: Q | Q1, Q2
+  static constexpr int QST = PW ? 3 : (D == 128) ? 3 : 4;  // Q ring depth
+  static constexpr int OST = PW ? 3 : (D == 128) ? 2 : 4;  // dO ring depth
+  static constexpr int LD_OFF = (NKT + NQT * QST + OST) * TILE;  // L / delta: [buffer][half][L, delta][64] floats
   static constexpr int LD_BYTES = 2 * 2 * 2 * 64 * 4;
   static constexpr int BAR_OFF = LD_OFF + LD_BYTES;
   static constexpr int BAR_BYTES = 256;
@@ -1368,10 +959,29 @@ struct DkdvStdCfg {
   static constexpr int PAD = (kSmemMax - USED) < 1023 ? (kSmemMax - USED) : 1023;  // alignment allowance
   static constexpr int SMEM = USED + PAD;
   static constexpr uint32_t COL_A = 0, COL_B = 128, COL_DV = 256, COL_DK = 256 + D;
+  static constexpr uint32_t COL_DK2 = 256 + 2 * D, COL_DSF = 256 + 3 * D;  // piecewise
+  static_assert(!PW || D == 64, "piecewise mode at D = 64 only");
   static_assert(PAD >= 0 && SMEM <= kSmemMax, "tiles do not fit in shared memory");
   static_assert(BAR_BYTES >= 8 * (1 + 2 * QST + 2 * OST + 6 + 4) + 8, "barrier area too small");
-  static_assert(COL_DK + D <= 512, "TMEM overflow");
+  static_assert(COL_DK + D <= 512 && (!PW || COL_DSF + 64 <= 512), "TMEM overflow");
 };
+
+// d (+)= X Y over the K-steps of chunk group G, X with dense K-steps: step kk
+// at x + 8 kk; Y as in mma_tY_il_g.  Whole converged warp.
+template <int G>
+__device__ __forceinline__ void mma_tY_dense_g(uint32_t d_tmem, uint32_t x_tmem, uint32_t y_smem, uint32_t idesc,
+                                               bool accumulate) {
+  const uint64_t dy = sdesc_sw128(y_smem, kBM * 128, 1024);
+  uint32_t a[4];
+  uint64_t b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int kk = chunk_kstep(G, i);
+    a[i] = x_tmem + kk * 8;
+    b[i] = dy + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+  }
+  mma_ts_n<4>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
+}
 
 // d (+)= X Y with X's K-steps interleaved: step kk at x + (kk / 2) * 32 +
 // (kk % 2) * 8 (16 packed columns in each 32-column chunk); Y as in mma_tY.
@@ -1389,13 +999,14 @@ __device__ __forceinline__ void mma_tY_il(uint32_t d_tmem, uint32_t x_tmem, uint
   mma_ts_n<8>(d_tmem, a, b, idesc, accumulate ? 1u : 0u);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool PW>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_dkdv_std_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                              const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                             const BwdArgs args) {
-  using C = DkdvStdCfg<D>;
+                             const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_k2,
+                             const __grid_constant__ CUtensorMap tm_dk2, const BwdArgs args) {
+  using C = DkdvStdCfg<D, PW>;
   constexpr bool BF = DT<T>::bf16;
   constexpr int QST = C::QST, OST = C::OST;
 
@@ -1430,10 +1041,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int i0 = first_q_tile_for(k0, args.P_SEQ, args.causal);
   const int nq = num_q_tiles > i0 ? num_q_tiles - i0 : 0;
 
-  uint8_t* sK = base;
-  uint8_t* sV = base + C::TILE;
-  auto sQ = [&](int i) { return base + (2 + i) * C::TILE; };
-  auto sDO = [&](int i) { return base + (2 + QST + i) * C::TILE; };
+  uint8_t* sK = base;             // K (piecewise: K1)
+  uint8_t* sK2 = base + C::TILE;  // piecewise
+  uint8_t* sV = base + (C::NKT - 1) * C::TILE;
+  auto sQ = [&](int i) { return base + (C::NKT + C::NQT * i) * C::TILE; };       // Q (Q1)
+  auto sQ2 = [&](int i) { return base + (C::NKT + C::NQT * i + 1) * C::TILE; };  // piecewise
+  auto sDO = [&](int i) { return base + (C::NKT + C::NQT * QST + i) * C::TILE; };
+  // piecewise: which score products query tile u needs (kNearB | kFarB bits)
+  auto cls_of = [&](int u) { return PW ? pw_class_b((i0 + u) * kBM, k0, args.P_SEQ, args.w) : kNearB; };
 
   WaitCtl ctl{args.err, args.timeout_ns, &abort_flag};
   if (threadIdx.x == 0) {
@@ -1474,16 +1089,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint64_t* empty = is_q ? bar_qe : bar_oe;
       const CUtensorMap* map = is_q ? &tm_q : &tm_do;
       if (is_q) {
-        mbar_expect_tx(&bar_kv, 2 * C::TILE);
+        mbar_expect_tx(&bar_kv, C::NKT * C::TILE);
         load_tile_b<D>(sK, &tm_k, &bar_kv, k0, bh);
+        if constexpr (PW) load_tile_b<D>(sK2, &tm_k2, &bar_kv, k0, bh);
         load_tile_b<D>(sV, &tm_v, &bar_kv, k0, bh);
       }
       int issued = 0;
       for (int u = 0; u < nq; ++u) {
         const int st = u % depth;
         if (u >= depth && !mbar_wait(&empty[st], ((u / depth) - 1) & 1, ctl, kErrTimeoutMma)) break;
-        mbar_expect_tx(&full[st], C::TILE);
-        load_tile_b<D>(is_q ? sQ(st) : sDO(st), map, &full[st], (i0 + u) * kBM, bh);
+        if (PW && is_q) {  // Q1 if any of the tile is near, Q2 if any is far
+          const int cls = cls_of(u);
+          mbar_expect_tx(&full[st], (((cls & kNearB) ? 1 : 0) + ((cls & kFarB) ? 1 : 0)) * C::TILE);
+          if (cls & kNearB) load_tile_b<D>(sQ(st), &tm_q, &full[st], (i0 + u) * kBM, bh);
+          if (cls & kFarB) load_tile_b<D>(sQ2(st), &tm_q2, &full[st], (i0 + u) * kBM, bh);
+        } else {
+          mbar_expect_tx(&full[st], C::TILE);
+          load_tile_b<D>(is_q ? sQ(st) : sDO(st), map, &full[st], (i0 + u) * kBM, bh);
+        }
         issued = u + 1;
       }
       int zero = 0;
@@ -1497,12 +1120,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (nq > 0) {
       constexpr uint32_t idesc_s = idesc_f16(kBN, kBM, BF, false, false);  // M = keys, N = queries
       constexpr uint32_t idesc_g = idesc_f16(kBN, D, BF, false, true);     // M = keys, N = D
+      // the first (or only) score product of query tile u: S^T = K Q^T
+      // (piecewise: S^T(k1, q1) if any of the tile is near, else S^T(k2, q2))
+      auto issue_s = [&](int u, int sq) {
+        if (!PW || (cls_of(u) & kNearB)) {
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(sq)), idesc_s);
+        } else if constexpr (PW) {
+          mma_abT<D>(tmem + C::COL_A, smem_u32(sK2), smem_u32(sQ2(sq)), idesc_s);
+        }
+        commit_el(&bar_s);
+      };
+      int ncons = 0;  // phases of bar_consumed waited for (piecewise: two on a tile that straddles w)
+      bool acc1 = false, acc2 = false;  // piecewise: dK1, dK2 hold a product
       bool ok = warp_wait(&bar_kv, 0, ctl, kErrTimeoutTma) && warp_wait(&bar_qf[0], 0, ctl, kErrTimeoutTma) &&
                 warp_wait(&bar_of[0], 0, ctl, kErrTimeoutTma);
       if (ok) {
         tc_fence_after();
-        mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(0)), idesc_s);   // S^T = K Q^T
-        commit_el(&bar_s);
+        issue_s(0, 0);
         mma_abT<D>(tmem + C::COL_B, smem_u32(sV), smem_u32(sDO(0)), idesc_s);  // dP^T = V dO^T
         commit_el(&bar_dp);
       }
@@ -1510,24 +1144,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int sq = u % QST, so = u % OST;
         const int sq1 = (u + 1) % QST, so1 = (u + 1) % OST;
         const bool next = u + 1 < nq;
+        const int cls = cls_of(u);
+        if constexpr (PW) {
+          if (cls == (kNearB | kFarB)) {  // S^T(k2, q2) once the softmax warps hold S^T(k1, q1)
+            if (!(ok = warp_wait(&bar_consumed, ncons & 1, ctl, kErrTimeoutSoftmax))) break;
+            ++ncons;
+            tc_fence_after();
+            mma_abT<D>(tmem + C::COL_A, smem_u32(sK2), smem_u32(sQ2(sq)), idesc_s);
+            commit_el(&bar_s);
+          }
+        }
         if (next) {
-          if (!(ok = warp_wait(&bar_consumed, u & 1, ctl, kErrTimeoutSoftmax))) break;
+          if (!(ok = warp_wait(&bar_consumed, ncons & 1, ctl, kErrTimeoutSoftmax))) break;
+          ++ncons;
           if (!(ok = warp_wait(&bar_qf[sq1], ((u + 1) / QST) & 1, ctl, kErrTimeoutTma))) break;
           tc_fence_after();
-          mma_abT<D>(tmem + C::COL_A, smem_u32(sK), smem_u32(sQ(sq1)), idesc_s);
-          commit_el(&bar_s);
+          issue_s(u + 1, sq1);
         }
         // dV += P^T dO and dK += dS^T Q, chunk group 0 as soon as the softmax
-        // warps have formed it
+        // warps have formed it (piecewise: dK1 += dS_near^T Q1, dK2 += dS_far^T
+        // Q2; the far part sits in its own columns when the tile straddles w)
         if (!(ok = warp_wait(&bar_ds[0], u & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         mma_tY_il_g<0>(tmem + C::COL_DV, tmem + C::COL_B, smem_u32(sDO(so)), idesc_g, u > 0);
-        mma_tY_il_g<0>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, u > 0);
+        if constexpr (!PW) {
+          mma_tY_il_g<0>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, u > 0);
+        } else {
+          if (cls == kFarB) {
+            mma_tY_il_g<0>(tmem + C::COL_DK2, tmem + C::COL_B + 16, smem_u32(sQ2(sq)), idesc_g, acc2);
+          } else {
+            mma_tY_il_g<0>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, acc1);
+            if (cls & kFarB) mma_tY_dense_g<0>(tmem + C::COL_DK2, tmem + C::COL_DSF, smem_u32(sQ2(sq)), idesc_g, acc2);
+          }
+        }
         if (!(ok = warp_wait(&bar_ds[1], u & 1, ctl, kErrTimeoutSoftmax))) break;
         tc_fence_after();
         mma_tY_il_g<1>(tmem + C::COL_DV, tmem + C::COL_B, smem_u32(sDO(so)), idesc_g, true);
         commit_el(&bar_oe[so]);
-        mma_tY_il_g<1>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, true);
+        if constexpr (!PW) {
+          mma_tY_il_g<1>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, true);
+        } else {
+          if (cls == kFarB) {
+            mma_tY_il_g<1>(tmem + C::COL_DK2, tmem + C::COL_B + 16, smem_u32(sQ2(sq)), idesc_g, true);
+          } else {
+            mma_tY_il_g<1>(tmem + C::COL_DK, tmem + C::COL_B + 16, smem_u32(sQ(sq)), idesc_g, true);
+            if (cls & kFarB) mma_tY_dense_g<1>(tmem + C::COL_DK2, tmem + C::COL_DSF, smem_u32(sQ2(sq)), idesc_g, true);
+          }
+          acc1 |= (cls & kNearB) != 0;
+          acc2 |= (cls & kFarB) != 0;
+        }
         commit_el(&bar_qe[sq]);
         if (next) {
           if (!(ok = warp_wait(&bar_of[so1], ((u + 1) / OST) & 1, ctl, kErrTimeoutTma))) break;
@@ -1563,11 +1228,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(&bar_pub[hc]);
     }
     bool ok = true;
+    int sph = 0;  // phases of bar_s seen (piecewise: two on a tile that straddles w)
+    bool touched1 = false, touched2 = false;  // piecewise: some query tile fed dK1 / dK2
     for (int u = 0; u < nq; ++u) {
       const int q0 = (i0 + u) * kBM;
       const int qb = q0 + cb;  // first query of this thread's columns
+      const int cls = cls_of(u);
       const float pre = (u + 1 < nq) ? ld_fetch(u + 1) : 0.f;
-      if (!(ok = warp_wait(&bar_s, u & 1, ctl, kErrTimeoutMma))) break;
+      if (!(ok = warp_wait(&bar_s, sph & 1, ctl, kErrTimeoutMma))) break;
+      ++sph;
       tc_fence_after();
       // 16-lane shapes: in each 16-lane group g of its warp, thread t holds
       // keys (t / 4) and (t / 4 + 8) at the query pairs 8 jj + 2 m, +1
@@ -1579,6 +1248,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld_16x256b_x8(lane_addr + (16u << 16) + C::COL_A + cb, TB_CHUNK(sv, 1));
       tmem_ld_wait(TB_CHUNK(sv, 0));
       tmem_ld_wait(TB_CHUNK(sv, 1));
+      // piecewise: element (g, jj, e) (key k0 + 32 (warp % 4) + lane / 4 + 16 g
+      // + 8 (e / 2), query qb + 2 m + 8 jj + e % 2) is far, its distance
+      // query + P_SEQ - key at least w, iff 8 jj + (e & 1) >= fl + 16 g + 8 (e >> 1)
+      int fl = 0;
+      if constexpr (PW) {
+        const long long f = (long long)args.w - args.P_SEQ - qb - 2 * (lane & 3) + k0 + 32 * (warp & 3) + (lane >> 2);
+        fl = f < -128 ? -128 : (f > 128 ? 128 : static_cast<int>(f));
+        touched1 |= (cls & kNearB) != 0;
+        touched2 |= (cls & kFarB) != 0;
+        if (cls == (kNearB | kFarB)) {  // S^T(k1, q1) is held: take S^T(k2, q2) where far
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_consumed);
+          if (!(ok = warp_wait(&bar_s, sph & 1, ctl, kErrTimeoutMma))) break;
+          ++sph;
+          tc_fence_after();
+#pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            uint32_t s2[32];
+            tmem_ld_16x256b_x8(lane_addr + (static_cast<uint32_t>(16 * g) << 16) + C::COL_A + cb, s2);
+            tmem_ld_wait(s2);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (8 * jj + (e & 1) >= fl + 16 * g + 8 * (e >> 1)) sv[32 * g + 4 * jj + e] = s2[4 * jj + e];
+          }
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_consumed);  // score buffer free for S^T(u + 1)
@@ -1616,46 +1314,68 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (!(ok = warp_wait(&bar_dp, u & 1, ctl, kErrTimeoutMma))) break;
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        // chunk c (32 queries): read dP^T, write P^T and dS^T (16 packed
-        // columns each, pair 4 jq + m) back into the same 32 columns
-        uint32_t dp[32];  // [g][16]
-        tmem_ld_16x256b_x4(lane_addr + C::COL_B + cb + 32 * c, TB_CHUNK16(dp, 0));
-        tmem_ld_16x256b_x4(lane_addr + (16u << 16) + C::COL_B + cb + 32 * c, TB_CHUNK16(dp, 1));
-        tmem_ld_wait(TB_CHUNK16(dp, 0));
-        tmem_ld_wait(TB_CHUNK16(dp, 1));
-        float2 nd2[4];  // -delta of the thread's query pairs
-#pragma unroll
-        for (int jq = 0; jq < 4; ++jq) {
-          const float2 d2 = *reinterpret_cast<const float2*>(sD + 8 * (4 * c + jq));
-          nd2[jq] = make_float2(-d2.x, -d2.y);
-        }
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          uint32_t pp[8], pd[8];
-#pragma unroll
+      // P^T and dS^T of the tile (SPLIT: a piecewise tile that straddles w,
+      // whose dS^T is split by distance), compiled apart so that the other
+      // tiles run the standard code
+      auto write_chunks = [&](auto split_tag) {
+        constexpr bool SPLIT = decltype(split_tag)::value;
+  #pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          // chunk c (32 queries): read dP^T, write P^T and dS^T (16 packed
+          // columns each, pair 4 jq + m) back into the same 32 columns
+          uint32_t dp[32];  // [g][16]
+          tmem_ld_16x256b_x4(lane_addr + C::COL_B + cb + 32 * c, TB_CHUNK16(dp, 0));
+          tmem_ld_16x256b_x4(lane_addr + (16u << 16) + C::COL_B + cb + 32 * c, TB_CHUNK16(dp, 1));
+          tmem_ld_wait(TB_CHUNK16(dp, 0));
+          tmem_ld_wait(TB_CHUNK16(dp, 1));
+          float2 nd2[4];  // -delta of the thread's query pairs
+  #pragma unroll
           for (int jq = 0; jq < 4; ++jq) {
-            const int i = 32 * g + 4 * (4 * c + jq);
-            const int di = 16 * g + 4 * jq;
-            pp[2 * jq] = pack2<BF>(p[i], p[i + 1]);
-            pp[2 * jq + 1] = pack2<BF>(p[i + 2], p[i + 3]);
-            const float2 s0 = fmul2(make_float2(p[i], p[i + 1]),
-                                    fadd2(make_float2(__uint_as_float(dp[di]), __uint_as_float(dp[di + 1])), nd2[jq]));
-            const float2 s1 = fmul2(make_float2(p[i + 2], p[i + 3]),
-                                    fadd2(make_float2(__uint_as_float(dp[di + 2]), __uint_as_float(dp[di + 3])), nd2[jq]));
-            pd[2 * jq] = pack2<BF>(s0.x, s0.y);
-            pd[2 * jq + 1] = pack2<BF>(s1.x, s1.y);
+            const float2 d2 = *reinterpret_cast<const float2*>(sD + 8 * (4 * c + jq));
+            nd2[jq] = make_float2(-d2.x, -d2.y);
           }
-          const uint32_t ga = lane_addr + (static_cast<uint32_t>(16 * g) << 16) + C::COL_B + cb + 32 * c;
-          tmem_st_16x128b_x4(ga, pp);
-          tmem_st_16x128b_x4(ga + 16, pd);
+  #pragma unroll
+          for (int g = 0; g < 2; ++g) {
+            uint32_t pp[8], pd[8];
+            uint32_t pf[8];  // SPLIT: the far part of dS^T (pd keeps the near part)
+  #pragma unroll
+            for (int jq = 0; jq < 4; ++jq) {
+              const int i = 32 * g + 4 * (4 * c + jq);
+              const int di = 16 * g + 4 * jq;
+              pp[2 * jq] = pack2<BF>(p[i], p[i + 1]);
+              pp[2 * jq + 1] = pack2<BF>(p[i + 2], p[i + 3]);
+              const float2 s0 = fmul2(make_float2(p[i], p[i + 1]),
+                                      fadd2(make_float2(__uint_as_float(dp[di]), __uint_as_float(dp[di + 1])), nd2[jq]));
+              const float2 s1 = fmul2(make_float2(p[i + 2], p[i + 3]),
+                                      fadd2(make_float2(__uint_as_float(dp[di + 2]), __uint_as_float(dp[di + 3])), nd2[jq]));
+              if constexpr (SPLIT) {
+                const int jj = 4 * c + jq;
+                const bool f0 = 8 * jj >= fl + 16 * g, f1 = 8 * jj + 1 >= fl + 16 * g;
+                const bool f2 = 8 * jj >= fl + 16 * g + 8, f3 = 8 * jj + 1 >= fl + 16 * g + 8;
+                pd[2 * jq] = pack2<BF>(f0 ? 0.f : s0.x, f1 ? 0.f : s0.y);
+                pd[2 * jq + 1] = pack2<BF>(f2 ? 0.f : s1.x, f3 ? 0.f : s1.y);
+                pf[2 * jq] = pack2<BF>(f0 ? s0.x : 0.f, f1 ? s0.y : 0.f);
+                pf[2 * jq + 1] = pack2<BF>(f2 ? s1.x : 0.f, f3 ? s1.y : 0.f);
+              } else {
+                pd[2 * jq] = pack2<BF>(s0.x, s0.y);
+                pd[2 * jq + 1] = pack2<BF>(s1.x, s1.y);
+              }
+            }
+            const uint32_t ga = lane_addr + (static_cast<uint32_t>(16 * g) << 16) + C::COL_B + cb + 32 * c;
+            tmem_st_16x128b_x4(ga, pp);
+            tmem_st_16x128b_x4(ga + 16, pd);
+            if constexpr (SPLIT)
+              tmem_st_16x128b_x4(lane_addr + (static_cast<uint32_t>(16 * g) << 16) + C::COL_DSF + (cb >> 1) + 16 * c,
+                                 pf);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_ds[c]);  // chunk group c of P^T / dS^T is in place
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_ds[c]);  // chunk group c of P^T / dS^T is in place
-      }
+      };
+      if (PW && cls == (kNearB | kFarB)) write_chunks(std::true_type{});
+      else write_chunks(std::false_type{});
       if (u + 1 < nq) {  // every warp of the half is past tile u - 1, the buffer's previous tile
         ld_slot(u + 1)[ld_arr * 64 + ld_col] = pre;
         __syncwarp();
@@ -1671,20 +1391,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     (void)j;
     const int r = threadIdx.x & 127;  // this thread's key within the tile
     const bool live = ok && nq > 0;
+    // (piecewise: dK2 over K2; an output no query tile fed is zero)
 #pragma unroll
-    for (int a = 0; a < 2; ++a) {  // 0: dV over K, 1: dK over V
+    for (int a = 0; a < (PW ? 3 : 2); ++a) {  // 0: dV over K, 1: dK over V, 2: dK2 over K2
+      const bool fed = !PW || a == 0 || (a == 1 ? touched1 : touched2);
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         const int c = hc * (D / 64) + cc;  // this thread's 32-column chunks of the row
         uint32_t v[32];
-        if (live) {
-          tmem_ld_x32(lane_addr + (a ? C::COL_DK : C::COL_DV) + 32 * c, v);
+        if (live && fed) {
+          tmem_ld_x32(lane_addr + (a == 0 ? C::COL_DV : a == 1 ? C::COL_DK : C::COL_DK2) + 32 * c, v);
           tmem_ld_wait(v);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) v[e] = 0u;
         }
-        stage_row_chunk_sw128<BF>(smem_u32(a ? sV : sK), r, c, v, a ? args.sm_scale : 1.f);
+        stage_row_chunk_sw128<BF>(smem_u32(a == 0 ? sK : a == 1 ? sV : sK2), r, c, v, a ? args.sm_scale : 1.f);
       }
     }
     fence_proxy_async_smem();
@@ -1694,6 +1416,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int kb = 0; kb < D / 64; ++kb) {
         tma_store_3d(&tm_dv, sK + kb * (kBM * 128), kb * 64, k0, bh);
         tma_store_3d(&tm_dk, sV + kb * (kBM * 128), kb * 64, k0, bh);
+        if constexpr (PW) tma_store_3d(&tm_dk2, sK2 + kb * (kBM * 128), kb * 64, k0, bh);
       }
       tma_store_commit_and_wait_read();
     }
@@ -1706,20 +1429,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-template <typename T, int MODE, int D>
-static cudaError_t launch_dkdv_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
-  using C = DkdvCfg<MODE, D>;
-  auto kern = attn_bwd_dkdv_kernel<T, MODE, D>;
-  static std::atomic<bool> attr[kMaxDevices];
-  cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
-  if (e_attr != cudaSuccess) return e_attr;
-  const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
-  if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.q2, m.k2, m.dv, m.dk,
-                                                                    m.dk2, a);
-  return cudaGetLastError();
-}
-
 template <typename T, int MODE, int D>
 static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   using C = DqCfg<MODE, D>;
@@ -1734,23 +1443,26 @@ static cudaError_t launch_dq_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t 
   return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool PW = false>
 static cudaError_t launch_dkdv_std_t(const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
-  using C = DkdvStdCfg<D>;
-  auto kern = attn_bwd_dkdv_std_kernel<T, D>;
+  using C = DkdvStdCfg<D, PW>;
+  auto kern = attn_bwd_dkdv_std_kernel<T, D, PW>;
   static std::atomic<bool> attr[kMaxDevices];
   cudaError_t e_attr = smem_attr_once(kern, C::SMEM, attr);
   if (e_attr != cudaSuccess) return e_attr;
   const long long blocks = static_cast<long long>(a.BH) * ((a.N + kBN - 1) / kBN);
   if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv, a);
+  kern<<<static_cast<unsigned>(blocks), kBwdThreads, C::SMEM, s>>>(m.q, m.k, m.v, m.dO, m.dk, m.dv,
+                                                                    PW ? m.q2 : m.q, PW ? m.k2 : m.k,
+                                                                    PW ? m.dk2 : m.dk, a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(int mode, bool bf16, int D, const BwdMaps& m, const BwdArgs& a, cudaStream_t s) {
   if (mode == kStd && D == 64) return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 64>(m, a, s) : launch_dkdv_std_t<__half, 64>(m, a, s);
   if (mode == kStd && D == 128) return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 128>(m, a, s) : launch_dkdv_std_t<__half, 128>(m, a, s);
-  if (mode == kPiecewise && D == 64) return bf16 ? launch_dkdv_t<__nv_bfloat16, kPiecewise, 64>(m, a, s) : launch_dkdv_t<__half, kPiecewise, 64>(m, a, s);
+  if (mode == kPiecewise && D == 64)  // the standard kernel's structure with K2, Q2 and dK2
+    return bf16 ? launch_dkdv_std_t<__nv_bfloat16, 64, true>(m, a, s) : launch_dkdv_std_t<__half, 64, true>(m, a, s);
   // piecewise D = 128: the one-pass kernel of bwd_pw_steps.cu (launch_bwd_pw_steps)
   return cudaErrorNotSupported;
 }
